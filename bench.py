@@ -1,0 +1,381 @@
+"""Throughput of the fused linear cross-entropy forward + backward on GB300.
+
+One step = one flce_forward_backward call over the whole batch (every chunk:
+logits GEMM with its log-sum-exp epilogue, combine, dlogits, dx GEMM, dW
+GEMM, loss reduction). Default workload: the Llama-3-shaped batch,
+N = 16384 tokens (4 x 4096), H = 4096, V = 128256, bf16, Zipf(1.1) targets,
+5% ignored. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload, on the host cores.
+Under torchrun each rank runs an independent replica of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FLCE fwd+bwd tokens/s & % of bf16 tensor peak (6·N·H·V FLOPs); peak HBM GB"
+UNIT = "tokens/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HBM_BOUND = {"dlogits_inplace", "lse_combine", "dx_split_reduce", "count_valid", "loss_finalize"}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="llama3_bf16")
+    p.add_argument("--chunk", type=int, default=0)
+    p.add_argument("--budget-gib", type=float, default=0.0)
+    p.add_argument("--dlogits", choices=["auto", "inplace", "recompute"], default="auto")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend, rank=rank, world_size=ws)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, value: float, device=None) -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+# ------------------------------------------------------------------- peaks
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_cross_entropy_token_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str, chunk: int):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, or
+    None if there is none for this workload or the kernels changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    if not k or d.get("workload") != workload or d.get("chunk") != chunk:
+        return None
+    return k.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------- cpu oracle
+
+def oracle_sample_rate(w, target_s: float, max_tokens: int = 4096):
+    """The fp64 oracle on the first n tokens of the workload (all of W), n
+    grown until one run takes about target_s seconds. Returns tokens/s, n,
+    seconds, cores."""
+    import numpy as np
+    import oracle
+    Wd = w.W_f64()
+    cores = len(os.sched_getaffinity(0))
+    n = 8
+    while True:
+        xs = w.x_f64(np.arange(n))
+        t0 = time.perf_counter()
+        oracle.flce_reference(xs, Wd, w.t[:n], w.ignore_index)
+        dt = time.perf_counter() - t0
+        if dt >= target_s * 0.5 or n >= max_tokens:
+            return n / dt, n, dt, cores
+        n = min(max_tokens, max(n * 2, int(n * target_s / max(dt, 1e-3))))
+
+
+# -------------------------------------------------------------------- main
+
+def run_reference(args, ws, rank):
+    """--impl reference: the fp64 CPU oracle, timed on the host cores."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import workloads
+    w = workloads.make(args.config)
+    Wd = w.W_f64()
+    _, n, dt, cores = oracle_sample_rate(w, target_s=min(args.cpu_seconds, 6.0))
+    xs = w.x_f64(np.arange(n))
+    ts = w.t[:n]
+    for _ in range(args.warmup):
+        oracle.flce_reference(xs, Wd, ts, w.ignore_index)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.flce_reference(xs, Wd, ts, w.ignore_index)
+    el = time.perf_counter() - t0
+    value = n * args.steps / el
+    sample = (f"first {n} tokens of {args.config} (N={w.N}, H={w.H}, V={w.V}) per step, "
+              f"float64 numpy oracle, all of W")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.config, "N": w.N, "H": w.H, "V": w.V,
+                                            "sample_tokens": n},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import numpy as np
+    import torch
+
+    import workloads
+    from linear_cross_entropy_token_gb300 import FLCE
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workloads.make(args.config)
+    N, H, V = w.N, w.H, w.V
+    x_h = torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16)
+    W_h = torch.from_numpy(w.W.view(np.int16)).view(torch.bfloat16)
+    t_h = torch.from_numpy(w.t)
+    x, W, t = x_h.to(dev), W_h.to(dev), t_h.to(dev)
+    dx = torch.empty_like(x)
+    dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    budget = int(args.budget_gib * (1 << 30))
+    h = FLCE("bf16", local, hbm_budget_bytes=budget, dlogits_mode=args.dlogits)
+    stream = torch.cuda.current_stream(dev)
+
+    free0, _ = torch.cuda.mem_get_info(dev)
+    h.forward_backward(x, W, t, chunk=args.chunk, dx=dx, dW=dW)
+    free1, _ = torch.cuda.mem_get_info(dev)
+    plan = h.last_plan()
+    for _ in range(max(0, args.warmup - 1)):
+        h.forward_backward(x, W, t, chunk=args.chunk, dx=dx, dW=dW)
+
+    # ---------------------------------------------------- timed region
+    h.set_profiling(True)
+    h.profile_reset()
+    launches0 = h.launch_count()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    losses = []
+    for _ in range(args.steps):
+        loss, _, _ = h.forward_backward(x, W, t, chunk=args.chunk, dx=dx, dW=dW)
+        losses.append(loss)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clk = clocks.stop()
+    launches = h.launch_count() - launches0
+    ms = ev0.elapsed_time(ev1) / args.steps
+    prof = h.profile()
+    h.set_profiling(False)
+    ms_max = max_over_ranks(ws, ms, dev if ws > 1 else None)
+
+    tokens = N
+    value = ws * tokens / (ms_max / 1e3)
+    flops = 6.0 * N * H * V
+    tflops = flops / (ms_max / 1e3) / 1e12
+    peaks, peaks_kind = load_peaks()
+    sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+
+    # dominant kernel and its roofline
+    dom = max(prof.items(), key=lambda kv: kv[1]["total_ms"])
+    name, pk = dom
+    per_launch_ms = pk["total_ms"] / pk["launches"]
+    if name in HBM_BOUND:
+        achieved = pk["bytes"] / pk["launches"] / (per_launch_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        achieved = pk["flops"] / pk["launches"] / (per_launch_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_for(name, args.config, plan["chunk"])
+    roof["kernel"] = name
+    roof["peak_source"] = f"{peaks_kind} ({'sustained bf16' if roof['bound'] == 'tensor' else 'hbm copy'})"
+    kernels = {k: {"launches": v["launches"], "ms_per_launch": v["total_ms"] / v["launches"],
+                   "share": v["total_ms"] / sum(q["total_ms"] for q in prof.values()),
+                   ("tflops" if k not in HBM_BOUND else "gbs"):
+                       (v["flops"] / v["total_ms"] / 1e9 if k not in HBM_BOUND
+                        else v["bytes"] / v["total_ms"] / 1e6)}
+               for k, v in prof.items()}
+
+    # ---------------------------------------------- end to end, host buffers
+    e2e = None
+    if not args.no_e2e:
+        xp, Wp, tp = x_h.pin_memory(), W_h.pin_memory(), t_h.pin_memory()
+        h.forward_backward_host(xp, Wp, tp, chunk=args.chunk, dx=dx, dW=dW)
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            h.forward_backward_host(xp, Wp, tp, chunk=args.chunk, dx=dx, dW=dW)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        ems = max_over_ranks(ws, e0.elapsed_time(e1) / args.steps, dev if ws > 1 else None)
+        e2e = {"value": ws * tokens / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(x_h.numel() * 2 + W_h.numel() * 2 + t_h.numel() * 8),
+               "d2h_bytes_per_step": 4, "ms_per_step": ems,
+               "path": "flce_forward_backward_host: pinned host x, W, t copied in; loss read back"}
+
+    # --------------------------------------------------- cpu oracle sample
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, n, dt, cores = oracle_sample_rate(w, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {n} tokens of the workload with all of W, float64 numpy oracle, "
+                         f"{dt:.1f} s"}
+
+    h.close()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.config, "N": N, "H": H, "V": V, "chunk": plan["chunk"],
+                   "num_chunks": plan["num_chunks"], "dx_splits": plan["dx_splits"],
+                   "dlogits": "recompute" if args.dlogits == "recompute" else "inplace",
+                   "targets": w.spec.targets, "ignore_frac": float(w.spec.ignore_frac),
+                   "l2": "inputs larger than L2 (W is 1.05 GB bf16; the chunk buffer 1.05 GB)",
+                   "parallelism": "replicas" if ws > 1 else "single"},
+        "tflops": tflops, "frac_of_bf16_peak": tflops / sustained,
+        "frac_of_bf16_peak_burst": tflops / peaks["bf16_tflops"],
+        "peak_source": peaks_kind,
+        "peak_extra_hbm_gb": plan["workspace_bytes"] / 1e9,
+        "peak_extra_hbm_measured_gb": max(0, free0 - free1) / 1e9,
+        "full_logits_gb": N * V * 2 / 1e9,
+        "loss": losses[-1],
+        "gpu_launches": launches,
+        "kernels": kernels,
+        "roofline": roof,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

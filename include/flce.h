@@ -1,0 +1,228 @@
+/*
+ * flce.h — fused linear cross-entropy (FLCE) on one NVIDIA GB300 (sm_103a).
+ *
+ * Given final hidden states x (N x H), an LM-head weight W (V x H) and integer
+ * targets t (N), the library returns the mean cross-entropy of the logits
+ * z = x·Wᵀ over the tokens whose target is not ignore_index, together with
+ * dx = d loss / d x and dW = d loss / d W. It never holds the N x V logits:
+ * tokens are processed in chunks of C, and only one chunk's C x V logits
+ * buffer exists at a time.
+ *
+ * The operation is the one the FLCE pages define:
+ *   - "Fused Linear Cross-Entropy: LLM 학습 logits 메모리 병목 없애기"
+ *     (42jerrykim.github.io), section "FLCE의 핵심 아이디어: logits을 오래 들고
+ *     있지 않는다": per chunk, (1) project the chunk to C x V logits, (2) take
+ *     the CE loss and overwrite the same buffer with softmax - one_hot,
+ *     (3) dx_chunk = dlogits·W at once, (4) dW += dlogits_chunkᵀ·x_chunk;
+ *     drop the chunk buffers and move on.
+ *   - "Unsloth 심층 아키텍처 …" (techknowgenie.com), section "스트리밍 청크
+ *     기반 Fast CrossEntropy 손실 커널": per-token loss -z_y + log sum_j exp z_j,
+ *     gradient softmax(z) - 1(i = y), and the running max / sum-exp kept on
+ *     chip while the vocabulary is swept in blocks.
+ *   - "메모리 아끼면서 Cross Entropy Loss 계산하기 — 128K Context LLM 학습 실전
+ *     가이드" (sigco.tistory.com), section "즉시 적용할 수 있는 팁": bf16 logits,
+ *     fp32 loss accumulation.
+ * The mean runs over n_valid = #{i : t_i != ignore_index} tokens (PyTorch's
+ * cross_entropy(reduction="mean") semantics, which the FLCE page's listing
+ * calls per chunk). If n_valid == 0 the loss, dx and dW are all zero.
+ *
+ * Conventions for every entry point below:
+ *   - Status codes, never exceptions or aborts. On failure, flce_last_error()
+ *     gives a one-line reason.
+ *   - Device pointers are CUDA device addresses on the handle's device,
+ *     contiguous row-major, 16-byte aligned. Host pointers are ordinary host
+ *     memory (page-locked memory makes the copies asynchronous).
+ *   - "stream" is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream. All device work of a call is ordered on that stream.
+ *   - A handle is not thread-safe: one host thread drives it at a time.
+ *   - The caller owns x, W, t, dx, dW. The library owns only its workspace
+ *     and, for the host-buffer entry point, its input staging buffers.
+ *   - Outputs are overwritten, never accumulated into.
+ */
+#ifndef FLCE_H
+#define FLCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FLCE_ABI_VERSION 1
+
+typedef struct flce_handle_s* flce_handle_t;
+
+typedef enum flce_status {
+    FLCE_OK = 0,
+    FLCE_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or layout */
+    FLCE_ERR_UNSUPPORTED = 2,   /* device is not compute capability 10.3, or dtype */
+    FLCE_ERR_BUDGET = 3,        /* workspace above the budget, or allocation failed */
+    FLCE_ERR_BAD_TARGET = 4,    /* a target outside [0, V) that is not ignore_index */
+    FLCE_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out */
+    FLCE_ERR_CUDA = 6           /* a CUDA runtime or driver call failed */
+} flce_status;
+
+/* element type of x, W and dx; dW is always fp32, the loss always fp32 */
+enum { FLCE_DTYPE_BF16 = 0, FLCE_DTYPE_FP32 = 1 };
+
+/* How the dlogits of a chunk are formed (bf16 only; fp32 always in place).
+ *  INPLACE:   the logits GEMM stores bf16 logits; a second pass overwrites
+ *             them with (softmax - onehot)/n_valid (the FLCE page's step 2).
+ *  RECOMPUTE: the logits GEMM keeps only per-row statistics; a second GEMM
+ *             recomputes each logits tile and writes dlogits directly.
+ *  AUTO:      INPLACE, the faster of the two on GB300 by measurement. */
+enum { FLCE_DLOGITS_AUTO = 0, FLCE_DLOGITS_INPLACE = 1, FLCE_DLOGITS_RECOMPUTE = 2 };
+
+typedef struct flce_config {
+    int32_t dtype;               /* FLCE_DTYPE_*                                       */
+    int32_t device;              /* CUDA device ordinal                                */
+    uint64_t hbm_budget_bytes;   /* workspace budget for the chunk planner; 0 = 1.25 GiB*/
+    int32_t dlogits_mode;        /* FLCE_DLOGITS_*                                     */
+    int32_t timeout_ms;          /* limit of every device-side wait; 0 = 2000 ms       */
+} flce_config;
+
+/* The chunk plan of one call (token-chunk scheduler). */
+typedef struct flce_plan {
+    int64_t chunk;               /* C, tokens per chunk                                */
+    int64_t num_chunks;          /* ceil(N / C)                                        */
+    int64_t vocab_tiles;         /* ceil(V / 256): log-sum-exp partials per token      */
+    int64_t ldv;                 /* row stride, in elements, of the chunk logits buffer */
+    int64_t dx_splits;           /* split of the V reduction of the dx GEMM            */
+    uint64_t workspace_bytes;    /* device bytes one call needs                        */
+    uint64_t logits_bytes;       /* of which the C x ldv logits / dlogits buffer       */
+} flce_plan;
+
+/* Kernel kinds, for the per-kernel timing of flce_profile_read(). */
+enum {
+    FLCE_K_COUNT_VALID = 0,      /* n_valid and target range check                     */
+    FLCE_K_GEMM_LOGITS = 1,      /* x_c·Wᵀ on tcgen05, online max/sum-exp epilogue     */
+    FLCE_K_LSE_COMBINE = 2,      /* per-token log-sum-exp from the vocab-tile partials  */
+    FLCE_K_DLOGITS = 3,          /* (softmax - onehot)/n_valid in place                */
+    FLCE_K_GEMM_DLOGITS = 4,     /* recompute variant: x_c·Wᵀ with dlogits epilogue    */
+    FLCE_K_GEMM_DX = 5,          /* dx_c = dlogits·W on tcgen05                        */
+    FLCE_K_DX_REDUCE = 6,        /* sums the dx split partials into bf16 dx            */
+    FLCE_K_GEMM_DW = 7,          /* dW (+)= dlogitsᵀ·x_c on tcgen05, fp32              */
+    FLCE_K_LOSS_FINALIZE = 8,    /* fixed-order sum of token losses / n_valid          */
+    FLCE_K_SIMT_GEMM = 9,        /* fp32 path: CUDA-core GEMMs                         */
+    FLCE_K_SIMT_TILE_STATS = 10, /* fp32 path: per-vocab-tile max/sum-exp              */
+    FLCE_K_NUM_KINDS = 11
+};
+
+typedef struct flce_kernel_profile {
+    int64_t launches;            /* launches of this kind since the last reset         */
+    double total_ms;             /* summed device time, CUDA events on the call stream */
+    double flops;                /* algorithmic FLOPs of those launches                */
+    double bytes;                /* algorithmic HBM bytes of those launches            */
+} flce_kernel_profile;
+
+/* ABI version of the loaded library (FLCE_ABI_VERSION). Host only. */
+int32_t flce_abi_version(void);
+
+/* Human-readable name of a status code. Host only; never NULL. */
+const char* flce_status_string(flce_status s);
+
+/* Plan one call without touching a device (host only).
+ * The token-chunk scheduler: C = chunk if chunk > 0 (clamped to N), else the
+ * largest C whose workspace fits cfg->hbm_budget_bytes, rounded to a multiple
+ * of 128 and then evened out over ceil(N / C) chunks. This replaces the
+ * chunk-size rule the FLCE page quotes from Liger (section "실전에서
+ * 마주치는 트레이드오프", item 1), which sizes chunk logits to about N·H
+ * elements: on GB300 the dW GEMM's intensity grows with C, so the budget, not
+ * N·H, sets C. num_sms picks the dx split; 0 means 152.
+ * Errors: INVALID_ARG for a NULL or negative argument, BUDGET if even one
+ * 128-token chunk (or N, if smaller) does not fit the budget. */
+flce_status flce_make_plan(const flce_config* cfg, int64_t N, int64_t H, int64_t V,
+                           int64_t chunk, int32_t num_sms, flce_plan* out);
+
+/* Create a handle on cfg->device. Checks that the device is compute
+ * capability 10.3 (GB300) and returns UNSUPPORTED otherwise: there is no
+ * other code path. Allocates nothing on the device yet. *out is NULL on error. */
+flce_status flce_create(flce_handle_t* out, const flce_config* cfg);
+
+/* Free everything the library allocated (workspace, staging) and the handle.
+ * Waits for the handle's outstanding work first. NULL is ignored. */
+void flce_destroy(flce_handle_t h);
+
+/* Give the handle caller-owned device memory as its workspace (at least
+ * flce_plan.workspace_bytes for the calls that follow; NULL/0 returns to
+ * library-allocated workspace). The memory must stay valid until the handle
+ * is destroyed or another workspace is set. Errors: INVALID_ARG. */
+flce_status flce_set_workspace(flce_handle_t h, void* dev_ptr, uint64_t bytes);
+
+/* The fused forward + backward.
+ *   x   device, N x H, dtype of the handle (bf16 or fp32), row-major
+ *   W   device, V x H, same dtype, row-major
+ *   t   device, N int64 targets; t_i == ignore_index skips token i
+ *   ignore_index  usually -100
+ *   chunk   tokens per chunk, 0 = planned from the HBM budget
+ *   loss    host, receives the fp32 mean loss
+ *   dx      device, N x H, same dtype as x, overwritten
+ *   dW      device, V x H fp32, overwritten (not accumulated into)
+ * Returns after the stream has drained (the loss is read back), so the
+ * outputs are ready. Steps on the stream: count n_valid; per chunk the
+ * tcgen05 logits GEMM with its log-sum-exp epilogue, the log-sum-exp combine,
+ * dlogits, the dx GEMM and the dW GEMM; the loss reduction.
+ * Layout rules: bf16 needs H % 8 == 0 (TMA row strides are multiples of 16
+ * bytes); fp32 takes any H. N may be 0 (loss 0, dW zeroed).
+ * Errors: INVALID_ARG, UNSUPPORTED, BUDGET (workspace), BAD_TARGET (outputs
+ * then unspecified), TIMEOUT, CUDA. */
+flce_status flce_forward_backward(flce_handle_t h, const void* x, const void* W,
+                                  const int64_t* t, int64_t N, int64_t H, int64_t V,
+                                  int64_t ignore_index, int64_t chunk, float* loss,
+                                  void* dx, float* dW, void* stream);
+
+/* The same call with x, W and t in HOST memory: the library copies them into
+ * its own device staging buffers on the stream (one cudaMemcpyAsync each),
+ * then runs flce_forward_backward. dx and dW are device outputs as above.
+ * Errors as flce_forward_backward, plus BUDGET if staging cannot be allocated. */
+flce_status flce_forward_backward_host(flce_handle_t h, const void* x_host,
+                                       const void* W_host, const int64_t* t_host,
+                                       int64_t N, int64_t H, int64_t V,
+                                       int64_t ignore_index, int64_t chunk, float* loss,
+                                       void* dx, float* dW, void* stream);
+
+/* Copy the per-token losses of the last call (N fp32, 0 for ignored tokens)
+ * into device memory out. N must equal the last call's N. Errors: INVALID_ARG. */
+flce_status flce_token_losses(flce_handle_t h, float* out, int64_t N, void* stream);
+
+/* The plan the last call ran with. Errors: INVALID_ARG before any call. */
+flce_status flce_last_plan(flce_handle_t h, flce_plan* out);
+
+/* Per-kernel timing. While enabled, every launch is bracketed by CUDA
+ * events recorded on the call's stream. */
+flce_status flce_set_profiling(flce_handle_t h, int32_t enable);
+/* Totals for one kernel kind since the last reset; synchronises on the
+ * recorded events. Errors: INVALID_ARG for an unknown kind. */
+flce_status flce_profile_read(flce_handle_t h, int32_t kind, flce_kernel_profile* out);
+void flce_profile_reset(flce_handle_t h);
+/* Name of a kernel kind (static string), "?" if unknown. */
+const char* flce_kernel_name(int32_t kind);
+/* Number of kernels this handle has launched (memsets and copies excluded). */
+int64_t flce_launch_count(flce_handle_t h);
+
+/* One-line reason for the handle's last failure ("" if none). */
+const char* flce_last_error(flce_handle_t h);
+
+/* ---- checks of single parts (used by the tests) ------------------------- */
+
+/* The tcgen05 GEMM core alone: C[M x N] (fp32, row-major, device) = A·B over
+ * K, bf16 operands. a_mn_major = 0: A is M x K row-major (K contiguous);
+ * 1: A is K x M row-major (M contiguous). b_mn_major = 0: B is N x K
+ * row-major; 1: B is K x N row-major. M, N, K >= 1; the contiguous extent of
+ * each operand must be a multiple of 8. Synchronises. Errors: INVALID_ARG,
+ * UNSUPPORTED, TIMEOUT, CUDA. */
+flce_status flce_check_gemm(flce_handle_t h, int32_t a_mn_major, int32_t b_mn_major,
+                            const void* A, const void* B, float* C, int64_t M, int64_t N,
+                            int64_t K, void* stream);
+
+/* Runs one device-side wait on a barrier that nothing ever completes, with a
+ * limit of timeout_us microseconds, and reports how it ended: TIMEOUT is the
+ * expected result (the kernel gave up, recorded the error and returned
+ * normally; the context stays usable). Synchronises. */
+flce_status flce_check_wait_timeout(flce_handle_t h, uint32_t timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLCE_H */

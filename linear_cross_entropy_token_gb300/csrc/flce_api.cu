@@ -1,0 +1,801 @@
+// Host runtime of the FLCE library: the C ABI of include/flce.h, the token-chunk
+// scheduler, the workspace, TMA descriptors, per-kernel timing, and the
+// chunk loop that enqueues the kernels on the caller's stream.
+//
+// The chunk loop is the schedule of the FLCE page ("Fused Linear
+// Cross-Entropy: LLM 학습 logits 메모리 병목 없애기", section "FLCE의 핵심
+// 아이디어: logits을 오래 들고 있지 않는다"): for each chunk of C tokens,
+// project to C x V logits, take the CE loss and turn the same buffer into
+// softmax - onehot, compute that chunk's dx at once and add its
+// dlogitsᵀ·x_chunk into dW; only one chunk buffer exists at a time. Streams
+// follow the pattern of "Unlocking asynchronicity in continuous batching"
+// (pogovet.com): all work is ordered on one caller stream and the host blocks
+// once per call, on the loss read-back.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/flce.h"
+#include "flce_internal.h"
+
+using namespace flce;
+
+namespace {
+
+constexpr uint64_t kDefaultBudget = 5ull << 28;  // 1.25 GiB
+constexpr int64_t kMaxChunk = 32768;
+constexpr int64_t kMaxDim = (1ll << 31) - 1;
+constexpr uint64_t kAlign = 1024;
+
+uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------ driver entry
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// --------------------------------------------------------------- profiling
+
+struct EventPair {
+  cudaEvent_t start = nullptr, stop = nullptr;
+  int kind = 0;
+  double flops = 0, bytes = 0;
+};
+
+struct Profiler {
+  bool enabled = false;
+  std::vector<EventPair> pool;
+  size_t used = 0;
+  flce_kernel_profile totals[FLCE_K_NUM_KINDS] = {};
+};
+
+// ------------------------------------------------------------- workspace
+
+struct Layout {
+  uint64_t ctrl = 0, logits = 0, partials = 0, zt = 0, lse = 0, token_loss = 0, dxpart = 0;
+  uint64_t total = 0;
+};
+
+Layout make_layout(int64_t N, int64_t H, int64_t C, int64_t ldv, int64_t vt, int64_t splits,
+                   int esize) {
+  Layout L;
+  uint64_t off = 0;
+  auto take = [&](uint64_t bytes) {
+    const uint64_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  L.ctrl = take(kCtrlWords * 4);
+  L.logits = take(static_cast<uint64_t>(C) * ldv * esize);
+  L.partials = take(static_cast<uint64_t>(C) * vt * 8);
+  L.zt = take(static_cast<uint64_t>(C) * 4);
+  L.lse = take(static_cast<uint64_t>(C) * 4);
+  L.token_loss = take(static_cast<uint64_t>(std::max<int64_t>(N, 1)) * 4);
+  L.dxpart = take(splits > 1 ? static_cast<uint64_t>(splits) * C * H * 4 : 0);
+  L.total = off;
+  return L;
+}
+
+int pick_dx_splits(int64_t C, int64_t H, int64_t V, int num_sms) {
+  const int64_t tiles = cdiv(C, kBM) * cdiv(H, kBN);
+  const int64_t kb = cdiv(V, kBK);
+  int best = 1;
+  double best_score = -1;
+  for (int s = 1; s <= 4; ++s) {
+    if (s > 1 && kb / s < 16) break;
+    const int64_t units = tiles * s;
+    const int64_t waves = cdiv(units, num_sms);
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * num_sms);
+    const double score = eff - 0.01 * (s - 1);
+    if (score > best_score + 1e-12) {
+      best_score = score;
+      best = s;
+    }
+  }
+  return best;
+}
+
+flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, int64_t chunk,
+                      int num_sms, flce_plan* out, std::string* why) {
+  if (!cfg || !out) {
+    *why = "null config or plan";
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (N < 0 || H < 1 || V < 1 || chunk < 0 || N > kMaxDim || H > kMaxDim || V > kMaxDim) {
+    *why = "sizes must satisfy N >= 0, H >= 1, V >= 1, chunk >= 0";
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (cfg->dtype != FLCE_DTYPE_BF16 && cfg->dtype != FLCE_DTYPE_FP32) {
+    *why = "dtype must be FLCE_DTYPE_BF16 or FLCE_DTYPE_FP32";
+    return FLCE_ERR_UNSUPPORTED;
+  }
+  if (num_sms <= 0) num_sms = 152;
+  const bool bf16 = cfg->dtype == FLCE_DTYPE_BF16;
+  const int esize = bf16 ? 2 : 4;
+  const uint64_t budget = cfg->hbm_budget_bytes ? cfg->hbm_budget_bytes : kDefaultBudget;
+  std::memset(out, 0, sizeof(*out));
+  out->ldv = static_cast<int64_t>(align_up(static_cast<uint64_t>(V), 64));
+  out->vocab_tiles = cdiv(V, kVocabTile);
+  auto splits_for = [&](int64_t C) { return bf16 ? pick_dx_splits(C, H, V, num_sms) : 1; };
+  auto ws = [&](int64_t C) {
+    return make_layout(N, H, C, out->ldv, out->vocab_tiles, splits_for(C), esize).total;
+  };
+  int64_t C;
+  if (N == 0) {
+    C = 0;
+  } else if (chunk > 0) {
+    C = std::min<int64_t>(std::min(chunk, N), kMaxChunk);
+    if (ws(C) > budget) {
+      char b[200];
+      std::snprintf(b, sizeof b, "chunk %lld needs %llu workspace bytes, above the budget %llu",
+                    static_cast<long long>(C), static_cast<unsigned long long>(ws(C)),
+                    static_cast<unsigned long long>(budget));
+      *why = b;
+      return FLCE_ERR_BUDGET;
+    }
+  } else {
+    const int64_t cap = std::min<int64_t>(kMaxChunk, static_cast<int64_t>(align_up(N, kBM)));
+    int64_t cmax = 0;
+    for (int64_t c = kBM; c <= cap; c += kBM)
+      if (ws(c) <= budget) cmax = c;
+    if (cmax == 0) {
+      const int64_t c = std::min<int64_t>(N, kBM);
+      if (ws(c) <= budget) cmax = c;
+    }
+    if (cmax == 0) {
+      *why = "not even one 128-token chunk fits the HBM budget";
+      return FLCE_ERR_BUDGET;
+    }
+    const int64_t k = cdiv(N, cmax);
+    C = std::min<int64_t>(static_cast<int64_t>(align_up(cdiv(N, k), kBM)), cmax);
+    C = std::min(C, N);
+  }
+  out->chunk = C;
+  out->num_chunks = C ? cdiv(N, C) : 0;
+  out->dx_splits = C ? splits_for(C) : 1;
+  out->workspace_bytes = make_layout(N, H, C, out->ldv, out->vocab_tiles, out->dx_splits, esize).total;
+  out->logits_bytes = static_cast<uint64_t>(C) * out->ldv * esize;
+  return FLCE_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ handle
+
+struct flce_handle_s {
+  flce_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  uint64_t timeout_ns = 0;
+  std::string err;
+  // workspace
+  void* ws = nullptr;
+  uint64_t ws_bytes = 0;
+  bool ws_external = false;
+  // staging for the host-buffer entry point
+  void* stage = nullptr;
+  uint64_t stage_bytes = 0;
+  uint32_t* host_ctrl = nullptr;  // pinned
+  flce_plan last_plan{};
+  int64_t last_N = -1;
+  uint64_t token_loss_off = 0;
+  bool has_plan = false;
+  int64_t launches = 0;
+  Profiler prof;
+};
+
+namespace {
+
+flce_status fail(flce_handle_t h, flce_status st, const char* fmt, ...) {
+  if (h) {
+    char b[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(b, sizeof b, fmt, ap);
+    va_end(ap);
+    h->err = b;
+  }
+  return st;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+void prof_begin(flce_handle_t h, int kind, cudaStream_t s) {
+  if (!h->prof.enabled) return;
+  Profiler& p = h->prof;
+  if (p.used == p.pool.size()) {
+    EventPair e;
+    cudaEventCreate(&e.start);
+    cudaEventCreate(&e.stop);
+    p.pool.push_back(e);
+  }
+  EventPair& e = p.pool[p.used];
+  e.kind = kind;
+  cudaEventRecord(e.start, s);
+}
+
+void prof_end(flce_handle_t h, cudaStream_t s, double flops, double bytes) {
+  if (!h->prof.enabled) return;
+  Profiler& p = h->prof;
+  EventPair& e = p.pool[p.used];
+  e.flops = flops;
+  e.bytes = bytes;
+  cudaEventRecord(e.stop, s);
+  ++p.used;
+}
+
+void prof_collect(flce_handle_t h) {
+  Profiler& p = h->prof;
+  for (size_t i = 0; i < p.used; ++i) {
+    EventPair& e = p.pool[i];
+    float ms = 0.f;
+    cudaEventSynchronize(e.stop);
+    cudaEventElapsedTime(&ms, e.start, e.stop);
+    flce_kernel_profile& t = p.totals[e.kind];
+    t.launches += 1;
+    t.total_ms += ms;
+    t.flops += e.flops;
+    t.bytes += e.bytes;
+  }
+  p.used = 0;
+}
+
+#define FLCE_LAUNCH(kind, flops, bytes, expr)                                                \
+  do {                                                                                      \
+    prof_begin(h, (kind), s);                                                               \
+    cudaError_t e_ = (expr);                                                                \
+    prof_end(h, s, (flops), (bytes));                                                       \
+    ++h->launches;                                                                          \
+    if (e_ != cudaSuccess)                                                                  \
+      return fail(h, FLCE_ERR_CUDA, "%s: %s", flce_kernel_name(kind), cudaGetErrorString(e_)); \
+  } while (0)
+
+flce_status ensure_workspace(flce_handle_t h, uint64_t bytes) {
+  if (h->ws_external) {
+    if (h->ws_bytes < bytes)
+      return fail(h, FLCE_ERR_BUDGET, "caller workspace has %llu bytes, the call needs %llu",
+                  static_cast<unsigned long long>(h->ws_bytes), static_cast<unsigned long long>(bytes));
+    return FLCE_OK;
+  }
+  if (h->ws_bytes >= bytes) return FLCE_OK;
+  if (h->ws) {
+    cudaFree(h->ws);
+    h->ws = nullptr;
+    h->ws_bytes = 0;
+  }
+  if (cudaMalloc(&h->ws, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    h->ws = nullptr;
+    return fail(h, FLCE_ERR_BUDGET, "cudaMalloc of %llu workspace bytes failed",
+                static_cast<unsigned long long>(bytes));
+  }
+  h->ws_bytes = bytes;
+  return FLCE_OK;
+}
+
+bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, int rank,
+                const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                std::string* why) {
+  if (!get_encode()) {
+    *why = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+  (void)esize;
+  CUresult r = g_encode(m, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd, gs, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char b[160];
+    std::snprintf(b, sizeof b, "cuTensorMapEncodeTiled failed (%d), rank %d, dims %llu x %llu", int(r),
+                  rank, static_cast<unsigned long long>(dims[0]),
+                  static_cast<unsigned long long>(dims[1]));
+    *why = b;
+    return false;
+  }
+  return true;
+}
+
+// 2-D bf16 map over a row-major matrix (inner = contiguous extent)
+bool map_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                 uint32_t box_inner, uint32_t box_outer, std::string* why) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t strides[1] = {row_bytes};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, 2, dims, strides, box, why);
+}
+
+// 3-D fp32 map (col, row, plane) for the fp32 epilogue; box 32 x 128 x 1
+bool map_f32_3d(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, uint64_t planes,
+                uint64_t row_bytes, uint64_t plane_bytes, std::string* why) {
+  const uint64_t dims[3] = {cols, rows, planes};
+  const uint64_t strides[2] = {row_bytes, plane_bytes};
+  const uint32_t box[3] = {32, 128, 1};
+  return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, 3, dims, strides, box, why);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+flce_status read_back(flce_handle_t h, uint32_t* ctrl_dev, cudaStream_t s, float* loss) {
+  cudaError_t e = cudaMemcpyAsync(h->host_ctrl, ctrl_dev, 4 * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "read-back: %s", cudaGetErrorString(e));
+  const uint32_t code = h->host_ctrl[kCtrlError];
+  if (loss) std::memcpy(loss, &h->host_ctrl[kCtrlLoss], 4);
+  if (code == FLCE_ERR_BAD_TARGET)
+    return fail(h, FLCE_ERR_BAD_TARGET, "a target is outside [0, V) and is not ignore_index");
+  if (code == FLCE_ERR_TIMEOUT)
+    return fail(h, FLCE_ERR_TIMEOUT, "a device-side wait ran out (limit %llu ns)",
+                static_cast<unsigned long long>(h->timeout_ns));
+  if (code != 0) return fail(h, FLCE_ERR_CUDA, "device error word %u", code);
+  return FLCE_OK;
+}
+
+flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t* t, int64_t N,
+                   int64_t H, int64_t V, int64_t ignore_index, int64_t chunk, float* loss, void* dx,
+                   float* dW, cudaStream_t s) {
+  if (!x || !W || !t || !loss || !dW || (N > 0 && !dx))
+    return fail(h, FLCE_ERR_INVALID_ARG, "null pointer argument");
+  const bool bf16 = h->cfg.dtype == FLCE_DTYPE_BF16;
+  if (bf16) {
+    if (H % 8 != 0) return fail(h, FLCE_ERR_INVALID_ARG, "bf16 needs H %% 8 == 0 (H = %lld)", (long long)H);
+    if (!aligned16(x) || !aligned16(W) || !aligned16(dW) || (N > 0 && !aligned16(dx)))
+      return fail(h, FLCE_ERR_INVALID_ARG, "x, W, dx and dW must be 16-byte aligned");
+  }
+  flce_plan p;
+  std::string why;
+  flce_status st = plan_impl(&h->cfg, N, H, V, chunk, h->num_sms, &p, &why);
+  if (st != FLCE_OK) return fail(h, st, "%s", why.c_str());
+  st = ensure_workspace(h, p.workspace_bytes);
+  if (st != FLCE_OK) return st;
+  const Layout L = make_layout(N, H, p.chunk, p.ldv, p.vocab_tiles, p.dx_splits, bf16 ? 2 : 4);
+  uint8_t* ws = static_cast<uint8_t*>(h->ws);
+  uint32_t* ctrl = reinterpret_cast<uint32_t*>(ws + L.ctrl);
+  float2* partials = reinterpret_cast<float2*>(ws + L.partials);
+  float* zt = reinterpret_cast<float*>(ws + L.zt);
+  float* lse = reinterpret_cast<float*>(ws + L.lse);
+  float* token_loss = reinterpret_cast<float*>(ws + L.token_loss);
+  h->last_plan = p;
+  h->last_N = N;
+  h->token_loss_off = L.token_loss;
+  h->has_plan = true;
+
+  cudaError_t e = cudaMemsetAsync(ctrl, 0, kCtrlWords * 4, s);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+  if (N == 0) {
+    e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * 4, s);
+    if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+    return read_back(h, ctrl, s, loss);
+  }
+  FLCE_LAUNCH(FLCE_K_COUNT_VALID, 0.0, 8.0 * N, launch_count_valid(t, N, V, ignore_index, ctrl, s));
+
+  const int64_t C = p.chunk, ldv = p.ldv;
+  const int vt = static_cast<int>(p.vocab_tiles);
+  const double dV = static_cast<double>(V), dH = static_cast<double>(H);
+
+  if (!bf16) {
+    // ---------------------------------------------------------- fp32 path
+    const float* xf = static_cast<const float*>(x);
+    const float* Wf = static_cast<const float*>(W);
+    float* dxf = static_cast<float*>(dx);
+    float* logits = reinterpret_cast<float*>(ws + L.logits);
+    for (int64_t c = 0; c < p.num_chunks; ++c) {
+      const int64_t off = c * C;
+      const int rows = static_cast<int>(std::min(C, N - off));
+      const double dr = rows;
+      FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dH * dV, 4 * (dr * dH + dV * dH + dr * dV),
+                  launch_simt_gemm_f32(xf + off * H, H, 1, Wf, 1, H, logits, ldv, rows, V, H, 0, s));
+      FLCE_LAUNCH(FLCE_K_SIMT_TILE_STATS, 0.0, 4 * dr * dV + 12 * dr * vt,
+                  launch_simt_tile_stats(logits, ldv, rows, V, vt, t + off, ignore_index, partials, zt, s));
+      FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
+                  launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
+      FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 8 * dr * dV,
+                  launch_dlogits_f32(logits, ldv, rows, V, lse, t + off, ignore_index, ctrl, s));
+      FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dV * dH, 4 * (dr * dV + dV * dH + dr * dH),
+                  launch_simt_gemm_f32(logits, ldv, 1, Wf, H, 1, dxf + off * H, H, rows, H, V, 0, s));
+      FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dV * dH, 4 * (dr * dV + dr * dH + 2 * dV * dH),
+                  launch_simt_gemm_f32(logits, 1, ldv, xf + off * H, H, 1, dW, H, V, H, rows, c > 0 ? 1 : 0, s));
+    }
+  } else {
+    // ------------------------------------------------- bf16 tcgen05 path
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    __nv_bfloat16* dxb = static_cast<__nv_bfloat16*>(dx);
+    __nv_bfloat16* logits = reinterpret_cast<__nv_bfloat16*>(ws + L.logits);
+    float* dxpart = reinterpret_cast<float*>(ws + L.dxpart);
+    const bool recompute = h->cfg.dlogits_mode == FLCE_DLOGITS_RECOMPUTE;
+    CUtensorMap mW_k, mW_mn, mX_k, mX_mn, mZ_out, mZ_k, mZ_mn, mDx, mDw;
+    if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, 256, &why) ||
+        !map_bf16_2d(&mW_mn, W, H, V, H * 2, 64, 64, &why) ||
+        !map_f32_3d(&mDw, dW, H, V, 1, H * 4, static_cast<uint64_t>(V) * H * 4, &why))
+      return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
+    const int sms = h->num_sms;
+    const int kb_h = static_cast<int>(cdiv(H, kBK));
+    const int kb_v = static_cast<int>(cdiv(V, kBK));
+    for (int64_t c = 0; c < p.num_chunks; ++c) {
+      const int64_t off = c * C;
+      const int rows = static_cast<int>(std::min(C, N - off));
+      const double dr = rows;
+      const void* xc = xb + off * H;
+      if (!map_bf16_2d(&mX_k, xc, H, rows, H * 2, 64, 128, &why) ||
+          !map_bf16_2d(&mX_mn, xc, H, rows, H * 2, 64, 64, &why) ||
+          !map_bf16_2d(&mZ_out, logits, V, rows, ldv * 2, 64, 128, &why) ||
+          !map_bf16_2d(&mZ_k, logits, V, rows, ldv * 2, 64, 128, &why) ||
+          !map_bf16_2d(&mZ_mn, logits, V, rows, ldv * 2, 64, 64, &why))
+        return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
+
+      // 1. projection with the online max / sum-exp epilogue
+      UmmaArgs a{};
+      a.num_m = static_cast<int>(cdiv(rows, kBM));
+      a.num_n = vt;
+      a.num_s = 1;
+      a.kb_total = kb_h;
+      a.kb_per_split = kb_h;
+      a.raster = 0;
+      a.rows = rows;
+      a.cols = static_cast<int>(V);
+      a.vocab_tiles = vt;
+      a.store_logits = recompute ? 0 : 1;
+      a.ignore_index = ignore_index;
+      a.targets = t + off;
+      a.partials = partials;
+      a.zt = zt;
+      a.lse = lse;
+      a.ctrl = ctrl;
+      a.timeout_ns = h->timeout_ns;
+      int units = a.num_m * a.num_n;
+      FLCE_LAUNCH(FLCE_K_GEMM_LOGITS, 2 * dr * dH * dV,
+                  2 * dr * dH + 2 * dV * dH + (recompute ? 0 : 2 * dr * dV) + 8 * dr * vt + 12 * dr,
+                  launch_umma(kUmmaLogits, mX_k, mW_k, mZ_out, a, std::min(units, sms), s));
+      // 2a. cross-tile log-sum-exp and token losses
+      FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
+                  launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
+      // 2b. dlogits = (softmax - onehot) / n_valid over the chunk buffer
+      if (recompute) {
+        FLCE_LAUNCH(FLCE_K_GEMM_DLOGITS, 2 * dr * dH * dV, 2 * dr * dH + 2 * dV * dH + 2 * dr * dV + 12 * dr,
+                    launch_umma(kUmmaDlogits, mX_k, mW_k, mZ_out, a, std::min(units, sms), s));
+      } else {
+        FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 4 * dr * dV,
+                    launch_dlogits_bf16(logits, ldv, rows, V, partials, vt, lse, t + off, ignore_index,
+                                        ctrl, s));
+      }
+      // 3. dx_chunk = dlogits · W
+      const int S_req = static_cast<int>(p.dx_splits);
+      const int kbps = (kb_v + S_req - 1) / S_req;
+      const int S = (kb_v + kbps - 1) / kbps;
+      UmmaArgs b = a;
+      b.num_m = static_cast<int>(cdiv(rows, kBM));
+      b.num_n = static_cast<int>(cdiv(H, kBN));
+      b.num_s = S;
+      b.kb_total = kb_v;
+      b.kb_per_split = kbps;
+      b.raster = 0;
+      b.rows = rows;
+      b.cols = static_cast<int>(H);
+      b.reduce_add = 0;
+      units = b.num_m * b.num_n * b.num_s;
+      if (S == 1) {
+        if (!map_bf16_2d(&mDx, dxb + off * H, H, rows, H * 2, 64, 128, &why))
+          return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
+        FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, 2 * dr * dV + 2 * dV * dH + 2 * dr * dH,
+                    launch_umma(kUmmaDxBf16, mZ_k, mW_mn, mDx, b, std::min(units, sms), s));
+      } else {
+        if (!map_f32_3d(&mDx, dxpart, H, rows, S, H * 4, static_cast<uint64_t>(C) * H * 4, &why))
+          return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
+        FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH,
+                    launch_umma(kUmmaDxF32, mZ_k, mW_mn, mDx, b, std::min(units, sms), s));
+        FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4.0 * S * dr * dH + 2 * dr * dH,
+                    launch_dx_reduce(dxpart, S, C * H, rows, H, dxb + off * H, s));
+      }
+      // 4. dW (+)= dlogitsᵀ · x_chunk, fp32 (stored on the first chunk, added after)
+      UmmaArgs d = a;
+      d.num_m = static_cast<int>(cdiv(V, kBM));
+      d.num_n = static_cast<int>(cdiv(H, kBN));
+      d.num_s = 1;
+      d.kb_total = static_cast<int>(cdiv(rows, kBK));
+      d.kb_per_split = d.kb_total;
+      d.raster = 1;
+      d.rows = static_cast<int>(V);
+      d.cols = static_cast<int>(H);
+      d.reduce_add = c > 0 ? 1 : 0;
+      units = d.num_m * d.num_n;
+      FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dV * dH,
+                  2 * dr * dV + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dV * dH,
+                  launch_umma(kUmmaDw, mZ_mn, mX_mn, mDw, d, std::min(units, sms), s));
+    }
+  }
+  FLCE_LAUNCH(FLCE_K_LOSS_FINALIZE, 0.0, 4.0 * N, launch_loss_finalize(token_loss, N, ctrl, s));
+  return read_back(h, ctrl, s, loss);
+}
+
+}  // namespace
+
+// ================================================================== C ABI
+
+extern "C" {
+
+int32_t flce_abi_version(void) { return FLCE_ABI_VERSION; }
+
+const char* flce_status_string(flce_status s) {
+  switch (s) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_ERR_INVALID_ARG: return "FLCE_ERR_INVALID_ARG";
+    case FLCE_ERR_UNSUPPORTED: return "FLCE_ERR_UNSUPPORTED";
+    case FLCE_ERR_BUDGET: return "FLCE_ERR_BUDGET";
+    case FLCE_ERR_BAD_TARGET: return "FLCE_ERR_BAD_TARGET";
+    case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT";
+    case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA";
+  }
+  return "FLCE_ERR_UNKNOWN";
+}
+
+const char* flce_kernel_name(int32_t kind) {
+  switch (kind) {
+    case FLCE_K_COUNT_VALID: return "count_valid";
+    case FLCE_K_GEMM_LOGITS: return "gemm_logits_lse";
+    case FLCE_K_LSE_COMBINE: return "lse_combine";
+    case FLCE_K_DLOGITS: return "dlogits_inplace";
+    case FLCE_K_GEMM_DLOGITS: return "gemm_dlogits_recompute";
+    case FLCE_K_GEMM_DX: return "gemm_dx";
+    case FLCE_K_DX_REDUCE: return "dx_split_reduce";
+    case FLCE_K_GEMM_DW: return "gemm_dw";
+    case FLCE_K_LOSS_FINALIZE: return "loss_finalize";
+    case FLCE_K_SIMT_GEMM: return "simt_gemm_f32";
+    case FLCE_K_SIMT_TILE_STATS: return "simt_tile_stats_f32";
+    default: return "?";
+  }
+}
+
+flce_status flce_make_plan(const flce_config* cfg, int64_t N, int64_t H, int64_t V, int64_t chunk,
+                           int32_t num_sms, flce_plan* out) {
+  std::string why;
+  return plan_impl(cfg, N, H, V, chunk, num_sms, out, &why);
+}
+
+flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
+  if (!out || !cfg) return FLCE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (cfg->dtype != FLCE_DTYPE_BF16 && cfg->dtype != FLCE_DTYPE_FP32) return FLCE_ERR_UNSUPPORTED;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
+    cudaGetLastError();
+    return FLCE_ERR_UNSUPPORTED;
+  }
+  if (cfg->device < 0 || cfg->device >= count) return FLCE_ERR_INVALID_ARG;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return FLCE_ERR_UNSUPPORTED;
+  if (prop.sharedMemPerBlockOptin < static_cast<size_t>(umma_smem_bytes())) return FLCE_ERR_UNSUPPORTED;
+  flce_handle_t h = new flce_handle_s();
+  h->cfg = *cfg;
+  h->device = cfg->device;
+  h->num_sms = prop.multiProcessorCount;
+  h->timeout_ns = static_cast<uint64_t>(cfg->timeout_ms > 0 ? cfg->timeout_ms : 2000) * 1000000ull;
+  DeviceGuard g(h->device);
+  if (cudaMallocHost(&h->host_ctrl, kCtrlWords * 4) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return FLCE_ERR_CUDA;
+  }
+  *out = h;
+  return FLCE_OK;
+}
+
+void flce_destroy(flce_handle_t h) {
+  if (!h) return;
+  {
+    DeviceGuard g(h->device);
+    cudaDeviceSynchronize();
+    for (auto& e : h->prof.pool) {
+      cudaEventDestroy(e.start);
+      cudaEventDestroy(e.stop);
+    }
+    if (h->ws && !h->ws_external) cudaFree(h->ws);
+    if (h->stage) cudaFree(h->stage);
+    if (h->host_ctrl) cudaFreeHost(h->host_ctrl);
+  }
+  delete h;
+}
+
+flce_status flce_set_workspace(flce_handle_t h, void* dev_ptr, uint64_t bytes) {
+  if (!h) return FLCE_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  if (dev_ptr && (reinterpret_cast<uintptr_t>(dev_ptr) & (kAlign - 1)) != 0)
+    return fail(h, FLCE_ERR_INVALID_ARG, "workspace must be %llu-byte aligned",
+                static_cast<unsigned long long>(kAlign));
+  if (h->ws && !h->ws_external) {
+    cudaDeviceSynchronize();
+    cudaFree(h->ws);
+  }
+  h->ws = dev_ptr;
+  h->ws_bytes = dev_ptr ? bytes : 0;
+  h->ws_external = dev_ptr != nullptr;
+  return FLCE_OK;
+}
+
+flce_status flce_forward_backward(flce_handle_t h, const void* x, const void* W, const int64_t* t,
+                                  int64_t N, int64_t H, int64_t V, int64_t ignore_index,
+                                  int64_t chunk, float* loss, void* dx, float* dW, void* stream) {
+  if (!h) return FLCE_ERR_INVALID_ARG;
+  h->err.clear();
+  DeviceGuard g(h->device);
+  return run_fb(h, x, W, t, N, H, V, ignore_index, chunk, loss, dx, dW,
+                static_cast<cudaStream_t>(stream));
+}
+
+flce_status flce_forward_backward_host(flce_handle_t h, const void* x_host, const void* W_host,
+                                       const int64_t* t_host, int64_t N, int64_t H, int64_t V,
+                                       int64_t ignore_index, int64_t chunk, float* loss, void* dx,
+                                       float* dW, void* stream) {
+  if (!h) return FLCE_ERR_INVALID_ARG;
+  h->err.clear();
+  if (!x_host || !W_host || !t_host || N < 0 || H < 1 || V < 1)
+    return fail(h, FLCE_ERR_INVALID_ARG, "null host pointer or bad size");
+  DeviceGuard g(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint64_t es = h->cfg.dtype == FLCE_DTYPE_BF16 ? 2 : 4;
+  const uint64_t xb = static_cast<uint64_t>(N) * H * es, wb = static_cast<uint64_t>(V) * H * es;
+  const uint64_t tb = static_cast<uint64_t>(N) * 8;
+  const uint64_t ox = 0, ow = align_up(xb, kAlign), ot = ow + align_up(wb, kAlign);
+  const uint64_t need = ot + align_up(std::max<uint64_t>(tb, 8), kAlign);
+  if (h->stage_bytes < need) {
+    if (h->stage) {
+      cudaDeviceSynchronize();
+      cudaFree(h->stage);
+      h->stage = nullptr;
+      h->stage_bytes = 0;
+    }
+    if (cudaMalloc(&h->stage, need) != cudaSuccess) {
+      cudaGetLastError();
+      h->stage = nullptr;
+      return fail(h, FLCE_ERR_BUDGET, "cudaMalloc of %llu staging bytes failed",
+                  static_cast<unsigned long long>(need));
+    }
+    h->stage_bytes = need;
+  }
+  uint8_t* st = static_cast<uint8_t*>(h->stage);
+  cudaError_t e = cudaSuccess;
+  if (xb) e = cudaMemcpyAsync(st + ox, x_host, xb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st + ow, W_host, wb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && tb) e = cudaMemcpyAsync(st + ot, t_host, tb, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "staging copy: %s", cudaGetErrorString(e));
+  return run_fb(h, st + ox, st + ow, reinterpret_cast<const int64_t*>(st + ot), N, H, V, ignore_index,
+                chunk, loss, dx, dW, s);
+}
+
+flce_status flce_token_losses(flce_handle_t h, float* out, int64_t N, void* stream) {
+  if (!h || !out) return FLCE_ERR_INVALID_ARG;
+  if (!h->has_plan || N != h->last_N) return fail(h, FLCE_ERR_INVALID_ARG, "N differs from the last call");
+  if (N == 0) return FLCE_OK;
+  DeviceGuard g(h->device);
+  const float* src = reinterpret_cast<const float*>(static_cast<uint8_t*>(h->ws) + h->token_loss_off);
+  cudaError_t e = cudaMemcpyAsync(out, src, static_cast<size_t>(N) * 4, cudaMemcpyDeviceToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "%s", cudaGetErrorString(e));
+  return FLCE_OK;
+}
+
+flce_status flce_last_plan(flce_handle_t h, flce_plan* out) {
+  if (!h || !out || !h->has_plan) return FLCE_ERR_INVALID_ARG;
+  *out = h->last_plan;
+  return FLCE_OK;
+}
+
+flce_status flce_set_profiling(flce_handle_t h, int32_t enable) {
+  if (!h) return FLCE_ERR_INVALID_ARG;
+  h->prof.enabled = enable != 0;
+  return FLCE_OK;
+}
+
+flce_status flce_profile_read(flce_handle_t h, int32_t kind, flce_kernel_profile* out) {
+  if (!h || !out || kind < 0 || kind >= FLCE_K_NUM_KINDS) return FLCE_ERR_INVALID_ARG;
+  DeviceGuard g(h->device);
+  prof_collect(h);
+  *out = h->prof.totals[kind];
+  return FLCE_OK;
+}
+
+void flce_profile_reset(flce_handle_t h) {
+  if (!h) return;
+  DeviceGuard g(h->device);
+  prof_collect(h);
+  std::memset(h->prof.totals, 0, sizeof(h->prof.totals));
+}
+
+int64_t flce_launch_count(flce_handle_t h) { return h ? h->launches : 0; }
+
+const char* flce_last_error(flce_handle_t h) { return h ? h->err.c_str() : "null handle"; }
+
+flce_status flce_check_gemm(flce_handle_t h, int32_t a_mn_major, int32_t b_mn_major, const void* A,
+                            const void* B, float* C, int64_t M, int64_t N, int64_t K, void* stream) {
+  if (!h) return FLCE_ERR_INVALID_ARG;
+  h->err.clear();
+  if (!A || !B || !C || M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return fail(h, FLCE_ERR_INVALID_ARG, "null pointer or bad size");
+  const int64_t a_inner = a_mn_major ? M : K, b_inner = b_mn_major ? N : K;
+  if (a_inner % 8 || b_inner % 8 || N % 4)
+    return fail(h, FLCE_ERR_INVALID_ARG, "contiguous extents must be multiples of 8 (N of 4)");
+  DeviceGuard g(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  flce_status st = ensure_workspace(h, kAlign);
+  if (st != FLCE_OK) return st;
+  uint32_t* ctrl = static_cast<uint32_t*>(h->ws);
+  std::string why;
+  CUtensorMap ma, mb, mc;
+  bool ok = a_mn_major ? map_bf16_2d(&ma, A, M, K, M * 2, 64, 64, &why)
+                       : map_bf16_2d(&ma, A, K, M, K * 2, 64, 128, &why);
+  ok = ok && (b_mn_major ? map_bf16_2d(&mb, B, N, K, N * 2, 64, 64, &why)
+                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, 256, &why));
+  ok = ok && map_f32_3d(&mc, C, N, M, 1, N * 4, static_cast<uint64_t>(M) * N * 4, &why);
+  if (!ok) return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
+  UmmaArgs a{};
+  a.num_m = static_cast<int>(cdiv(M, kBM));
+  a.num_n = static_cast<int>(cdiv(N, kBN));
+  a.num_s = 1;
+  a.kb_total = static_cast<int>(cdiv(K, kBK));
+  a.kb_per_split = a.kb_total;
+  a.rows = static_cast<int>(M);
+  a.cols = static_cast<int>(N);
+  a.ctrl = ctrl;
+  a.timeout_ns = h->timeout_ns;
+  const int kind = a_mn_major ? (b_mn_major ? kUmmaDw : kUmmaCheckMK) : (b_mn_major ? kUmmaDxF32 : kUmmaCheckKK);
+  cudaError_t e = cudaMemsetAsync(ctrl, 0, kCtrlWords * 4, s);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "%s", cudaGetErrorString(e));
+  const double flops = 2.0 * M * N * K;
+  const int kkind = a_mn_major ? FLCE_K_GEMM_DW : (b_mn_major ? FLCE_K_GEMM_DX : FLCE_K_GEMM_LOGITS);
+  FLCE_LAUNCH(kkind, flops, 2.0 * (M * K + N * K) + 4.0 * M * N,
+              launch_umma(kind, ma, mb, mc, a, std::min(a.num_m * a.num_n, h->num_sms), s));
+  return read_back(h, ctrl, s, nullptr);
+}
+
+flce_status flce_check_wait_timeout(flce_handle_t h, uint32_t timeout_us, void* stream) {
+  if (!h) return FLCE_ERR_INVALID_ARG;
+  h->err.clear();
+  DeviceGuard g(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  flce_status st = ensure_workspace(h, kAlign);
+  if (st != FLCE_OK) return st;
+  uint32_t* ctrl = static_cast<uint32_t*>(h->ws);
+  cudaError_t e = cudaMemsetAsync(ctrl, 0, kCtrlWords * 4, s);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "%s", cudaGetErrorString(e));
+  e = launch_wait_check(ctrl, static_cast<uint64_t>(timeout_us) * 1000ull, s);
+  ++h->launches;
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "%s", cudaGetErrorString(e));
+  return read_back(h, ctrl, s, nullptr);
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// Internal declarations shared by the kernels and the host runtime.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace flce {
+
+// Control block in device memory, one per handle workspace (uint32 words).
+enum CtrlWord : int {
+  kCtrlError = 0,    // first error recorded by a kernel (flce_status numbering)
+  kCtrlNValid = 1,   // number of non-ignored tokens
+  kCtrlLoss = 2,     // fp32 bits of the mean loss
+  kCtrlWords = 16
+};
+
+// Tile shape of the tcgen05 GEMMs: 128 x 256 output tile per CTA, 64-deep
+// k-blocks (one 128-byte swizzle row of bf16), 4-stage TMA pipeline.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kVocabTile = kBN;   // vocab columns per log-sum-exp partial
+
+// Epilogues of the tcgen05 GEMM
+enum Epilogue : int {
+  kEpiLse = 0,       // online max / sum-exp + target gather (+ bf16 logits store)
+  kEpiBf16 = 1,      // bf16 store
+  kEpiF32 = 2,       // fp32 store or reduce-add (3-D map: col, row, split)
+  kEpiDlogits = 3    // (exp(z - lse) - onehot) / n_valid, bf16 store
+};
+
+// The kernel instantiations the runtime launches
+enum UmmaKind : int {
+  kUmmaLogits = 0,     // A = x_c (K-major), B = W (K-major), kEpiLse
+  kUmmaDlogits = 1,    // A = x_c, B = W, kEpiDlogits
+  kUmmaDxBf16 = 2,     // A = dlogits (K-major), B = W (MN-major), kEpiBf16
+  kUmmaDxF32 = 3,      // same operands, fp32 split partials
+  kUmmaDw = 4,         // A = dlogitsᵀ (MN-major), B = x_c (MN-major), kEpiF32
+  kUmmaCheckKK = 5,    // both K-major, fp32 out (tests)
+  kUmmaCheckMK = 6     // A MN-major, B K-major, fp32 out (tests)
+};
+
+struct UmmaArgs {
+  int32_t num_m, num_n, num_s;   // output tiles along M, N and splits of K
+  int32_t kb_total;              // 64-deep k-blocks over the whole K
+  int32_t kb_per_split;          // k-blocks per split
+  int32_t raster;                // 0: m fastest; 1: n fastest (then the other, then s)
+  int32_t rows;                  // valid output rows (M extent)
+  int32_t cols;                  // valid output columns (N extent; V for the logits GEMM)
+  int32_t vocab_tiles;           // log-sum-exp partials per token
+  int32_t reduce_add;            // kEpiF32: 1 = add into the output instead of storing
+  int32_t store_logits;          // kEpiLse: 1 = also store bf16 logits
+  int32_t pad0;
+  int64_t ignore_index;
+  const int64_t* targets;        // targets of this chunk's tokens
+  float2* partials;              // [rows][vocab_tiles] (running max, sum of exp)
+  float* zt;                     // [rows] fp32 target logit
+  const float* lse;              // [rows] log-sum-exp (kEpiDlogits)
+  uint32_t* ctrl;                // control block
+  uint64_t timeout_ns;           // limit of every mbarrier wait
+};
+
+// flce_umma.cu
+int umma_smem_bytes();
+cudaError_t launch_umma(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                        const UmmaArgs& args, int grid, cudaStream_t s);
+cudaError_t launch_wait_check(uint32_t* ctrl, uint64_t timeout_ns, cudaStream_t s);
+
+// flce_rows.cu
+cudaError_t launch_count_valid(const int64_t* t, int64_t N, int64_t V, int64_t ignore_index,
+                               uint32_t* ctrl, cudaStream_t s);
+cudaError_t launch_lse_combine(const float2* partials, int vocab_tiles, const float* zt,
+                               const int64_t* t_chunk, int rows, int64_t ignore_index, float* lse,
+                               float* token_loss_chunk, cudaStream_t s);
+cudaError_t launch_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int rows, int64_t V,
+                                const float2* partials, int vocab_tiles, const float* lse,
+                                const int64_t* t_chunk, int64_t ignore_index,
+                                const uint32_t* ctrl, cudaStream_t s);
+cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, const float* lse,
+                               const int64_t* t_chunk, int64_t ignore_index,
+                               const uint32_t* ctrl, cudaStream_t s);
+cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_stride, int rows,
+                             int64_t H, __nv_bfloat16* dx, cudaStream_t s);
+cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* ctrl,
+                                 cudaStream_t s);
+
+// flce_simt.cu (fp32 path)
+cudaError_t launch_simt_gemm_f32(const float* A, int64_t sam, int64_t sak, const float* B,
+                                 int64_t sbk, int64_t sbn, float* C, int64_t ldc, int64_t M,
+                                 int64_t N, int64_t K, int accumulate, cudaStream_t s);
+cudaError_t launch_simt_tile_stats(const float* logits, int64_t ldv, int rows, int64_t V,
+                                   int vocab_tiles, const int64_t* t_chunk, int64_t ignore_index,
+                                   float2* partials, float* zt, cudaStream_t s);
+
+}  // namespace flce

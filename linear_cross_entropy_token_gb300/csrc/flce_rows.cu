@@ -1,0 +1,243 @@
+// Row-wise kernels of fused linear cross-entropy: the n_valid count and
+// target range check, the cross-tile log-sum-exp combine, the in-place
+// dlogits pass, the dx split reduction and the loss reduction.
+//
+// The formulas are those of the Unsloth page ("Unsloth 심층 아키텍처 …",
+// section "스트리밍 청크 기반 Fast CrossEntropy 손실 커널"): per token
+// L = -z_y + log sum_j exp(z_j) and dL/dz_j = softmax(z)_j - 1(j = y), with the
+// sum kept as a running max m and l = sum exp(z - m) per vocab tile. The
+// dlogits pass overwrites the chunk's logits buffer in place, as step 2 of
+// the FLCE page does ("Fused Linear Cross-Entropy: LLM 학습 logits 메모리 병목
+// 없애기", section "FLCE의 핵심 아이디어"). All reductions run in a fixed
+// order, so a call is bit-for-bit repeatable.
+#include <cuda_bf16.h>
+
+#include "flce_internal.h"
+#include "ptx.cuh"
+
+namespace flce {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// n_valid = #{i : t_i != ignore_index}; any other target outside [0, V)
+// records FLCE_ERR_BAD_TARGET. One block; fixed-order integer sum.
+__global__ void count_valid_kernel(const int64_t* __restrict__ t, int64_t N, int64_t V,
+                                   int64_t ignore_index, uint32_t* ctrl) {
+  __shared__ uint32_t warp_cnt[32];
+  uint32_t cnt = 0;
+  bool bad = false;
+  for (int64_t i = threadIdx.x; i < N; i += blockDim.x) {
+    const int64_t v = t[i];
+    if (v == ignore_index) continue;
+    if (v < 0 || v >= V) bad = true;
+    ++cnt;
+  }
+  if (bad) atomicCAS(ctrl + kCtrlError, 0u, kErrBadTarget);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if ((threadIdx.x & 31) == 0) warp_cnt[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    uint32_t c = threadIdx.x < (blockDim.x >> 5) ? warp_cnt[threadIdx.x] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (threadIdx.x == 0) ctrl[kCtrlNValid] = c;
+  }
+}
+
+// One warp per token row: lse = M + log sum_s l_s exp(m_s - M) over the vocab
+// tiles' (m_s, l_s); token loss = lse - z_t (0 for an ignored token).
+__global__ void lse_combine_kernel(const float2* __restrict__ partials, int vocab_tiles,
+                                   const float* __restrict__ zt, const int64_t* __restrict__ t,
+                                   int rows, int64_t ignore_index, float* __restrict__ lse,
+                                   float* __restrict__ token_loss) {
+  const int warps = blockDim.x >> 5;
+  const int r = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const float2* p = partials + static_cast<size_t>(r) * vocab_tiles;
+  float M = -INFINITY;
+  for (int s = lane; s < vocab_tiles; s += 32) M = fmaxf(M, p[s].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float S = 0.f;
+  const float Ml = M * kLog2e;
+  for (int s = lane; s < vocab_tiles; s += 32) {
+    const float2 q = p[s];
+    S += q.y * ex2_approx(fmaf(q.x, kLog2e, -Ml));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  if (lane == 0) {
+    const float l = M + logf(S);
+    lse[r] = l;
+    const int64_t tg = t[r];
+    token_loss[r] = (tg == ignore_index) ? 0.f : (l - zt[r]);
+  }
+}
+
+// dlogits in place over a bf16 chunk buffer: 8 columns (16 bytes) per
+// thread; blockIdx.y = token row. The buffer holds y = z - m_s, the logits
+// shifted by their vocab tile's max m_s (partials[.].x), so
+// softmax = exp(y + m_s - lse). Ignored rows and padding columns get 0.
+__global__ void dlogits_bf16_kernel(__nv_bfloat16* __restrict__ buf, int64_t ldv, int64_t V,
+                                    const float2* __restrict__ partials, int vocab_tiles,
+                                    const float* __restrict__ lse, const int64_t* __restrict__ t,
+                                    int64_t ignore_index, const uint32_t* __restrict__ ctrl) {
+  const int r = blockIdx.y;
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
+  if (c0 >= ldv) return;
+  const int64_t tg = t[r];
+  const uint32_t nv = ctrl[kCtrlNValid];
+  const bool valid = tg != ignore_index;
+  const float scale = (valid && nv > 0) ? 1.0f / static_cast<float>(nv) : 0.f;
+  const int tile = static_cast<int>(c0 / kVocabTile);  // 8 columns never straddle a tile
+  const float ll = (lse[r] - partials[static_cast<size_t>(r) * vocab_tiles + tile].x) * kLog2e;
+  uint4* ptr = reinterpret_cast<uint4*>(buf + static_cast<size_t>(r) * ldv + c0);
+  uint4 v = *ptr;
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w[q]);
+    float2 f = __bfloat1622float2(h);
+    const int64_t j0 = c0 + 2 * q;
+    float d0 = ex2_approx(fmaf(f.x, kLog2e, -ll));
+    float d1 = ex2_approx(fmaf(f.y, kLog2e, -ll));
+    if (j0 == tg) d0 -= 1.f;
+    if (j0 + 1 == tg) d1 -= 1.f;
+    d0 = (j0 < V) ? d0 * scale : 0.f;
+    d1 = (j0 + 1 < V) ? d1 * scale : 0.f;
+    h = __floats2bfloat162_rn(d0, d1);
+    w[q] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// fp32 version: 4 columns per thread
+__global__ void dlogits_f32_kernel(float* __restrict__ buf, int64_t ldv, int64_t V,
+                                   const float* __restrict__ lse, const int64_t* __restrict__ t,
+                                   int64_t ignore_index, const uint32_t* __restrict__ ctrl) {
+  const int r = blockIdx.y;
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (c0 >= ldv) return;
+  const int64_t tg = t[r];
+  const uint32_t nv = ctrl[kCtrlNValid];
+  const bool valid = tg != ignore_index;
+  const float scale = (valid && nv > 0) ? 1.0f / static_cast<float>(nv) : 0.f;
+  const float l = lse[r];
+  float4* ptr = reinterpret_cast<float4*>(buf + static_cast<size_t>(r) * ldv + c0);
+  float4 v = *ptr;
+  float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int64_t j = c0 + q;
+    float d = expf(f[q] - l);
+    if (j == tg) d -= 1.f;
+    f[q] = (j < V) ? d * scale : 0.f;
+  }
+  *ptr = make_float4(f[0], f[1], f[2], f[3]);
+}
+
+// dx rows = sum over splits of the fp32 partials, in split order, to bf16
+__global__ void dx_reduce_kernel(const float* __restrict__ part, int splits, int64_t split_stride,
+                                 int64_t total, __nv_bfloat16* __restrict__ dx) {
+  const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i >= total) return;
+  float4 acc = *reinterpret_cast<const float4*>(part + i);
+  for (int s = 1; s < splits; ++s) {
+    const float4 v = *reinterpret_cast<const float4*>(part + s * split_stride + i);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 o;
+  o.x = *reinterpret_cast<uint32_t*>(&lo);
+  o.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(dx + i) = o;
+}
+
+// loss = (sum of token losses) / n_valid, the sum in float64 and fixed order
+__global__ void loss_finalize_kernel(const float* __restrict__ token_loss, int64_t N,
+                                     uint32_t* ctrl) {
+  __shared__ double part[1024];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < N; i += blockDim.x) s += static_cast<double>(token_loss[i]);
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = blockDim.x >> 1; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const uint32_t nv = ctrl[kCtrlNValid];
+    const float loss = nv > 0 ? static_cast<float>(part[0] / static_cast<double>(nv)) : 0.f;
+    ctrl[kCtrlLoss] = __float_as_uint(loss);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_count_valid(const int64_t* t, int64_t N, int64_t V, int64_t ignore_index,
+                               uint32_t* ctrl, cudaStream_t s) {
+  count_valid_kernel<<<1, 1024, 0, s>>>(t, N, V, ignore_index, ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_combine(const float2* partials, int vocab_tiles, const float* zt,
+                               const int64_t* t_chunk, int rows, int64_t ignore_index, float* lse,
+                               float* token_loss_chunk, cudaStream_t s) {
+  const int warps = 8;
+  lse_combine_kernel<<<(rows + warps - 1) / warps, warps * 32, 0, s>>>(
+      partials, vocab_tiles, zt, t_chunk, rows, ignore_index, lse, token_loss_chunk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int rows, int64_t V,
+                                const float2* partials, int vocab_tiles, const float* lse,
+                                const int64_t* t_chunk, int64_t ignore_index,
+                                const uint32_t* ctrl, cudaStream_t s) {
+  const int threads = 256;
+  const int64_t per_block = threads * 8;
+  dim3 grid(static_cast<unsigned>((ldv + per_block - 1) / per_block), static_cast<unsigned>(rows));
+  dlogits_bf16_kernel<<<grid, threads, 0, s>>>(buf, ldv, V, partials, vocab_tiles, lse, t_chunk,
+                                               ignore_index, ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, const float* lse,
+                               const int64_t* t_chunk, int64_t ignore_index,
+                               const uint32_t* ctrl, cudaStream_t s) {
+  const int threads = 256;
+  const int64_t per_block = threads * 4;
+  dim3 grid(static_cast<unsigned>((ldv + per_block - 1) / per_block), static_cast<unsigned>(rows));
+  dlogits_f32_kernel<<<grid, threads, 0, s>>>(buf, ldv, V, lse, t_chunk, ignore_index, ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_stride, int rows,
+                             int64_t H, __nv_bfloat16* dx, cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(rows) * H;  // H % 8 == 0, so total % 4 == 0
+  const int threads = 256;
+  const int64_t blocks = (total / 4 + threads - 1) / threads;
+  dx_reduce_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(partials, splits, split_stride,
+                                                                    total, dx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* ctrl,
+                                 cudaStream_t s) {
+  loss_finalize_kernel<<<1, 1024, 0, s>>>(token_loss, N, ctrl);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

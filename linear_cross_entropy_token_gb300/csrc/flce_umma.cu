@@ -1,0 +1,474 @@
+// Persistent tcgen05 GEMM for sm_103a with the epilogues of fused linear
+// cross-entropy.
+//
+// The three contractions of the FLCE pages' per-chunk schedule ("Fused Linear
+// Cross-Entropy: LLM 학습 logits 메모리 병목 없애기", section "FLCE의 핵심
+// 아이디어": projection x_c·Wᵀ, dx = dlogits·W, dW += dlogitsᵀ·x_c) all run on
+// this one kernel template:
+//
+//   warp 0      TMA producer: 64-deep k-blocks of A and B into a 4-stage ring
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
+//               (M=128, N=256, K=16, bf16 in, fp32 accumulate) into one of two
+//               256-column accumulators, so the epilogue of tile i overlaps
+//               the main loop of tile i+1
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one token row per
+//               thread), transform, stage 16 KB sub-tiles in 128-byte-swizzled
+//               shared memory and write them out with TMA stores
+//
+// The logits epilogue (kEpiLse) is the on-chip online softmax of the Unsloth
+// page ("Unsloth 심층 아키텍처 …", section "스트리밍 청크 기반 Fast
+// CrossEntropy 손실 커널"): per token row and 256-wide vocab tile it takes
+// the max m and l = sum exp(z - m) from the fp32 accumulator (two passes over
+// TMEM), picks up the target logit, and optionally stores the tile as bf16
+// logits shifted by m. The row's tiles are combined later by the log-sum-exp
+// combine, the online-softmax step across tiles.
+//
+// Every mbarrier wait is bounded (timeout in UmmaArgs). A wait that runs out
+// records FLCE_ERR_TIMEOUT in the control block; the CTA then waits (bounded)
+// for its own TMA loads and MMAs in flight, frees its TMEM and returns.
+#include <cuda_bf16.h>
+
+#include "flce_internal.h"
+#include "ptx.cuh"
+
+namespace flce {
+namespace {
+
+constexpr int kStages = 4;
+constexpr uint32_t kABytes = kBM * kBK * 2;             // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;             // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;      // 48 KB
+constexpr uint32_t kEpiBytes = 128 * 128;               // 128 rows x 128 bytes
+constexpr uint32_t kNumBars = 2 * kStages + 5;
+constexpr uint32_t kSmemBytes =
+    1024 + kStages * kStageBytes + 2 * kEpiBytes + kNumBars * 8 + 16;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kEpiBar = 1;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct Unit {
+  int m, n, s;
+};
+
+__device__ __forceinline__ Unit unit_coords(const UmmaArgs& a, int u) {
+  Unit r;
+  const int mn = a.num_m * a.num_n;
+  r.s = u / mn;
+  const int w = u - r.s * mn;
+  if (a.raster == 0) {
+    r.m = w % a.num_m;
+    r.n = w / a.num_m;
+  } else {
+    r.n = w % a.num_n;
+    r.m = w / a.num_n;
+  }
+  return r;
+}
+
+// wait bounded by time only (used while draining after an error)
+__device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Row r of a 128-row x 128-byte staging tile, in the 128-byte swizzle that
+// the TMA store expects: 16-byte chunk j of row r sits at chunk j ^ (r % 8).
+__device__ __forceinline__ void stage_row(uint8_t* buf, int r, const uint32_t (&w)[32]) {
+  uint4* rowp = reinterpret_cast<uint4*>(buf + r * 128);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    rowp[j ^ (r & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+
+template <int AMN, int BMN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmO, const UmmaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint8_t* sE = sB + kStages * kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int acc) { return bar0 + 8u * (2 * kStages + acc); };
+  auto tempty_bar = [&](int acc) { return bar0 + 8u * (2 * kStages + 2 + acc); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int acc = 0; acc < 2; ++acc) {
+      mbar_init(tfull_bar(acc), 1);
+      mbar_init(tempty_bar(acc), kEpiThreads);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+    tma_prefetch_map(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_units = a.num_m * a.num_n * a.num_s;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      uint32_t n_issued = 0;
+      bool failed = false;
+      for (int u = blockIdx.x; u < num_units && !failed; u += gridDim.x) {
+        const Unit t = unit_coords(a, u);
+        const int kb0 = t.s * a.kb_per_split;
+        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int stage = n_issued % kStages;
+          const uint32_t phase = (n_issued / kStages) & 1u;
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, a.ctrl, a.timeout_ns)) {
+            failed = true;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          const uint32_t sa = smem_u32(sA + stage * kABytes);
+          const uint32_t sb = smem_u32(sB + stage * kBBytes);
+          const int k0 = kb * kBK;
+          if (AMN == 0) {
+            tma_load_2d(sa, &tmA, fb, k0, t.m * kBM);
+          } else {
+            tma_load_2d(sa, &tmA, fb, t.m * kBM, k0);
+            tma_load_2d(sa + 8192, &tmA, fb, t.m * kBM + 64, k0);
+          }
+          if (BMN == 0) {
+            tma_load_2d(sb, &tmB, fb, k0, t.n * kBN);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_2d(sb + 8192 * j, &tmB, fb, t.n * kBN + 64 * j, k0);
+          }
+          ++n_issued;
+        }
+      }
+      if (failed) {
+        // let the loads already in flight land before the CTA goes away
+        const uint32_t first = n_issued > kStages ? n_issued - kStages : 0;
+        for (uint32_t i = first; i < n_issued; ++i)
+          mbar_drain_wait(full_bar(i % kStages), (i / kStages) & 1u, a.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, AMN, BMN);
+      uint32_t n_consumed = 0;
+      bool issued = false, failed = false;
+      int it = 0;
+      for (int u = blockIdx.x; u < num_units && !failed; u += gridDim.x, ++it) {
+        const Unit t = unit_coords(a, u);
+        const int kb0 = t.s * a.kb_per_split;
+        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, a.ctrl, a.timeout_ns)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int stage = n_consumed % kStages;
+          const uint32_t phase = (n_consumed / kStages) & 1u;
+          if (!mbar_wait_bounded(full_bar(stage), phase, a.ctrl, a.timeout_ns)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(sA + stage * kABytes);
+          const uint32_t sb = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            // K-major: the 16-deep slice starts 32 bytes further along the
+            // swizzled 128-byte row. MN-major: 16 k-rows of 128 bytes further.
+            const uint64_t ad = AMN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                    : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+            const uint64_t bd = BMN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
+                                    : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit(empty_bar(stage));
+          ++n_consumed;
+        }
+        if (failed) break;
+        tc_commit(tfull_bar(acc));
+      }
+      if (failed && issued) {
+        tc_commit(drain_bar);
+        mbar_drain_wait(drain_bar, 0, a.timeout_ns);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wq = warp & 3;               // TMEM lane quarter of this warp
+    const int row = wq * 32 + lane;        // tile row owned by this thread
+    const bool leader = threadIdx.x == 64; // issues the TMA stores
+    uint32_t ebuf = 0;
+    int it = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      const bool ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, a.ctrl, a.timeout_ns);
+      if (named_bar_or(kEpiBar, kEpiThreads, !ok)) break;
+      tc_fence_after();
+      const Unit t = unit_coords(a, u);
+      const int m0 = t.m * kBM;
+      const int n0 = t.n * kBN;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + acc * kBN;
+      const int grow = m0 + row;
+      const bool rvalid = grow < a.rows;
+
+      // stage one 16 KB sub-tile and hand it to the TMA unit
+      auto stage_and_store = [&](const uint32_t (&w)[32], auto&& issue) {
+        uint8_t* buf = sE + ebuf * kEpiBytes;
+        if (leader) bulk_wait_group_read<1>();
+        named_bar_sync(kEpiBar, kEpiThreads);
+        stage_row(buf, row, w);
+        fence_proxy_async_smem();
+        named_bar_sync(kEpiBar, kEpiThreads);
+        if (leader) {
+          issue(smem_u32(buf));
+          bulk_commit_group();
+        }
+        __syncwarp();
+        ebuf ^= 1u;
+      };
+
+      if constexpr (EPI == kEpiLse || EPI == kEpiDlogits) {
+        int64_t tg = -1;
+        if (rvalid) tg = a.targets[grow];
+        const bool tvalid = rvalid && tg != a.ignore_index;
+        const int tcol = (tvalid && tg >= n0 && tg < n0 + kBN) ? static_cast<int>(tg - n0) : -1;
+        float tmax = -INFINITY, tsum = 0.f, zt = 0.f;
+        float scale = 0.f, lse_l2 = 0.f;
+        if constexpr (EPI == kEpiDlogits) {
+          const uint32_t nv = a.ctrl[kCtrlNValid];
+          scale = (tvalid && nv > 0) ? 1.0f / static_cast<float>(nv) : 0.f;
+          lse_l2 = rvalid ? a.lse[grow] * kLog2e : 0.f;
+        }
+        if constexpr (EPI == kEpiLse) {
+          // pass 1 over the accumulator: the tile's row max and the target logit
+#pragma unroll 1
+          for (int g = 0; g < kBN / 32; ++g) {
+            const int ncv = a.cols - (n0 + g * 32);
+            if (ncv <= 0) break;  // uniform across the epilogue threads
+            uint32_t r0[32];
+            tmem_ld_32x32b_x32(tbase + g * 32, r0);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < ncv) tmax = fmaxf(tmax, __uint_as_float(r0[i]));
+            if (tcol >= g * 32 && tcol < g * 32 + 32) {
+              const int k = tcol - g * 32;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i == k) zt = __uint_as_float(r0[i]);
+            }
+          }
+        }
+        // last 64-column group holding valid columns (uniform)
+        const int last_g = min(kBN / 64 - 1, (a.cols - n0 - 1) / 64);
+#pragma unroll 1
+        for (int g = 0; g <= last_g; ++g) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(tbase + g * 64, r0);
+          tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
+          tmem_ld_wait();
+          if (g == last_g) {
+            tc_fence_before();
+            mbar_arrive(tempty_bar(acc));
+          }
+          const int c0 = n0 + g * 64;
+          const int ncv = a.cols - c0;  // valid columns in this group, >= 1 (uniform)
+          if constexpr (EPI == kEpiLse) {
+            // pass 2: sum of exp(z - tmax), and the logits stored shifted by
+            // the tile max, y = z - tmax, so that the largest entries are
+            // stored near 0 where bf16 is most precise
+            const float ml = tmax * kLog2e;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r0[i]), kLog2e, -ml));
+              if (i + 32 < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r1[i]), kLog2e, -ml));
+            }
+            if (a.store_logits) {
+              uint32_t w[32];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]) - tmax, __uint_as_float(r0[2 * i + 1]) - tmax);
+                w[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]) - tmax,
+                                        __uint_as_float(r1[2 * i + 1]) - tmax);
+              }
+              stage_and_store(w, [&](uint32_t src) { tma_store_2d(&tmO, src, c0, m0); });
+            }
+          } else {
+            // dlogits = (exp(z - lse) - onehot) * scale, written over the logits buffer
+            const int k = (tcol >= g * 64 && tcol < g * 64 + 64) ? tcol - g * 64 : -1;
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float v[4] = {__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]),
+                            __uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])};
+              const int ci[4] = {2 * i, 2 * i + 1, 32 + 2 * i, 33 + 2 * i};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                float p = ex2_approx(fmaf(v[q], kLog2e, -lse_l2));
+                if (ci[q] == k) p -= 1.0f;
+                v[q] = p * scale;
+              }
+              w[i] = pack_bf16x2(v[0], v[1]);
+              w[16 + i] = pack_bf16x2(v[2], v[3]);
+            }
+            stage_and_store(w, [&](uint32_t src) { tma_store_2d(&tmO, src, c0, m0); });
+          }
+        }
+        if constexpr (EPI == kEpiLse) {
+          if (rvalid) {
+            a.partials[static_cast<size_t>(grow) * a.vocab_tiles + t.n] = make_float2(tmax, tsum);
+            if (tcol >= 0) a.zt[grow] = zt;
+          }
+        }
+      } else if constexpr (EPI == kEpiBf16) {
+#pragma unroll 1
+        for (int g = 0; g < kBN / 64; ++g) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(tbase + g * 64, r0);
+          tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
+          tmem_ld_wait();
+          if (g == kBN / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(tempty_bar(acc));
+          }
+          const int c0 = n0 + g * 64;
+          if (c0 >= a.cols) continue;
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+            w[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+          }
+          stage_and_store(w, [&](uint32_t src) { tma_store_2d(&tmO, src, c0, m0); });
+        }
+      } else {  // kEpiF32
+#pragma unroll 1
+        for (int g = 0; g < kBN / 32; ++g) {
+          uint32_t r0[32];
+          tmem_ld_32x32b_x32(tbase + g * 32, r0);
+          tmem_ld_wait();
+          if (g == kBN / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(tempty_bar(acc));
+          }
+          const int c0 = n0 + g * 32;
+          if (c0 >= a.cols) continue;
+          if (a.reduce_add)
+            stage_and_store(r0, [&](uint32_t src) { tma_reduce_add_3d(&tmO, src, c0, m0, t.s); });
+          else
+            stage_and_store(r0, [&](uint32_t src) { tma_store_3d(&tmO, src, c0, m0, t.s); });
+        }
+      }
+    }
+    if (leader) bulk_wait_group<0>();
+  }
+
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// One bounded wait on a barrier that nothing completes: checks that a wait
+// which runs out reports FLCE_ERR_TIMEOUT and returns.
+__global__ void wait_check_kernel(uint32_t* ctrl, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // phase 0 never completes: nobody arrives
+    mbar_wait_bounded(smem_u32(&bar), 0u, ctrl + kCtrlError, timeout_ns);
+  }
+  __syncthreads();
+}
+
+template <int AMN, int BMN, int EPI>
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+                       const UmmaArgs& args, int grid, cudaStream_t s) {
+  auto kern = umma_gemm_kernel<AMN, BMN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, kSmemBytes, s>>>(ta, tb, to, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int umma_smem_bytes() { return static_cast<int>(kSmemBytes); }
+
+cudaError_t launch_umma(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                        const UmmaArgs& args, int grid, cudaStream_t s) {
+  // the epilogue's error word lives at ctrl[kCtrlError]; the kernels read
+  // and write it through args.ctrl
+  switch (kind) {
+    case kUmmaLogits: return launch_one<0, 0, kEpiLse>(a, b, o, args, grid, s);
+    case kUmmaDlogits: return launch_one<0, 0, kEpiDlogits>(a, b, o, args, grid, s);
+    case kUmmaDxBf16: return launch_one<0, 1, kEpiBf16>(a, b, o, args, grid, s);
+    case kUmmaDxF32: return launch_one<0, 1, kEpiF32>(a, b, o, args, grid, s);
+    case kUmmaDw: return launch_one<1, 1, kEpiF32>(a, b, o, args, grid, s);
+    case kUmmaCheckKK: return launch_one<0, 0, kEpiF32>(a, b, o, args, grid, s);
+    case kUmmaCheckMK: return launch_one<1, 0, kEpiF32>(a, b, o, args, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_wait_check(uint32_t* ctrl, uint64_t timeout_ns, cudaStream_t s) {
+  wait_check_kernel<<<1, 32, 0, s>>>(ctrl, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

@@ -1,0 +1,124 @@
+"""The C-ABI library: it loads, exports every function include/flce.h declares,
+and its host-only logic (the token-chunk planner) does what it states. No
+compute call runs here."""
+import ctypes
+import os
+
+import pytest
+
+from linear_cross_entropy_token_gb300 import build as flce_build
+from linear_cross_entropy_token_gb300 import flce
+
+
+@pytest.fixture(scope="module")
+def lib():
+    flce_build.build()
+    return flce.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = flce.header_functions()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(lib, n), f"libflce.so does not export {n}"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.flce_abi_version() == 1
+    assert lib.flce_status_string(0) == b"FLCE_OK"
+    assert lib.flce_status_string(4) == b"FLCE_ERR_BAD_TARGET"
+    assert lib.flce_kernel_name(1) == b"gemm_logits_lse"
+    assert lib.flce_kernel_name(99) == b"?"
+    for k, name in enumerate(flce.KERNEL_KINDS):
+        assert lib.flce_kernel_name(k).decode() == name
+
+
+def test_library_is_built_for_sm103a_only():
+    """build() compiles one -gencode, for compute capability 10.3."""
+    assert flce_build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+@pytest.mark.skipif(os.environ.get("CUDA_VISIBLE_DEVICES") is None and
+                    __import__("torch").cuda.is_available(), reason="a GPU is present")
+def test_create_without_gpu_is_unsupported(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    cfg = flce.make_config("bf16", 0)
+    h = ctypes.c_void_p()
+    st = lib.flce_create(ctypes.byref(h), ctypes.byref(cfg))
+    assert st == 2 and not h.value   # FLCE_ERR_UNSUPPORTED, no handle
+    with pytest.raises(flce.FlceError):
+        flce.FLCE("bf16", 0)
+
+
+def test_null_handle_calls_fail_cleanly(lib):
+    loss = ctypes.c_float()
+    assert lib.flce_forward_backward(None, None, None, None, 1, 8, 8, -100, 0, ctypes.byref(loss),
+                                     None, None, None) == 1
+    assert lib.flce_launch_count(None) == 0
+    assert lib.flce_last_error(None) == b"null handle"
+    lib.flce_destroy(None)
+
+
+# ---------------------------------------------------------------- planner
+
+GiB = 1 << 30
+
+
+def test_plan_llama3_default_budget():
+    p = flce.plan(16384, 4096, 128256, "bf16")
+    assert p["chunk"] == 4096 and p["num_chunks"] == 4
+    assert p["vocab_tiles"] == 501 and p["ldv"] == 128256
+    assert p["logits_bytes"] == 4096 * 128256 * 2
+    assert p["workspace_bytes"] <= int(1.25 * GiB)
+    assert p["dx_splits"] == 2          # 512 dx tiles on 152 SMs: 2 splits fill the waves
+
+
+def test_plan_long_context_stays_O_CV():
+    p = flce.plan(131072, 4096, 128256, "bf16")
+    full_logits = 131072 * 128256 * 2
+    assert p["num_chunks"] * p["chunk"] >= 131072
+    assert p["workspace_bytes"] <= int(1.25 * GiB) < full_logits / 20
+    assert p["chunk"] % 128 == 0
+
+
+def test_plan_explicit_chunk_and_budget():
+    p = flce.plan(256, 128, 4096, "fp32", chunk=64)
+    assert (p["chunk"], p["num_chunks"], p["dx_splits"]) == (64, 4, 1)
+    assert p["logits_bytes"] == 64 * 4096 * 4
+    p = flce.plan(16384, 4096, 151936, "bf16", chunk=8192, hbm_budget_bytes=4 * GiB)
+    assert p["chunk"] == 8192 and p["num_chunks"] == 2
+    with pytest.raises(flce.FlceError) as e:
+        flce.plan(16384, 4096, 151936, "bf16", chunk=8192)   # 2.5 GB > default 1.25 GiB
+    assert e.value.status_name == "FLCE_ERR_BUDGET"
+    with pytest.raises(flce.FlceError) as e:
+        flce.plan(16384, 4096, 151936, "bf16", hbm_budget_bytes=1 << 20)
+    assert e.value.status_name == "FLCE_ERR_BUDGET"
+
+
+def test_plan_small_and_ragged():
+    p = flce.plan(2048, 1024, 32000, "bf16")
+    assert p["chunk"] == 2048 and p["num_chunks"] == 1
+    p = flce.plan(1000, 64, 4099, "bf16", chunk=300)
+    assert (p["chunk"], p["num_chunks"], p["ldv"], p["vocab_tiles"]) == (300, 4, 4160, 17)
+    p = flce.plan(50, 64, 100, "bf16")
+    assert p["chunk"] == 50 and p["num_chunks"] == 1
+    p = flce.plan(0, 64, 100, "bf16")
+    assert p["chunk"] == 0 and p["num_chunks"] == 0
+
+
+def test_plan_balances_chunks():
+    for N in (5000, 16384, 40000, 131072):
+        p = flce.plan(N, 4096, 128256, "bf16")
+        last = N - (p["num_chunks"] - 1) * p["chunk"]
+        assert 0 < last <= p["chunk"]
+        # no chunk is more than one 128-token tile longer than an even split
+        assert p["chunk"] - N / p["num_chunks"] < 128
+
+
+def test_plan_rejects_bad_sizes():
+    for args in ((-1, 8, 8), (8, 0, 8), (8, 8, 0)):
+        with pytest.raises(flce.FlceError) as e:
+            flce.plan(*args)
+        assert e.value.status_name == "FLCE_ERR_INVALID_ARG"

@@ -1,0 +1,52 @@
+"""The tcgen05 GEMM core alone, for each operand majorness, against the float64
+product of the same bf16 operands; and the bounded device wait."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def handle():
+    from linear_cross_entropy_token_gb300 import FLCE
+    h = FLCE("bf16", 0)
+    yield h
+    h.close()
+
+
+SHAPES = [(128, 256, 64), (256, 512, 192), (200, 296, 136), (384, 768, 1024), (64, 40, 8)]
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)],
+                         ids=["A_K-B_K", "A_K-B_MN", "A_MN-B_MN", "A_MN-B_K"])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemm_core(handle, a_mn, b_mn, M, N, K):
+    g = torch.Generator().manual_seed(M * 7 + N * 3 + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)   # logical A (M x K)
+    B = torch.randn(N, K, generator=g).to(torch.bfloat16)   # logical B (N x K)
+    ref = (A.double() @ B.double().T).numpy()
+    Ad = (A.T.contiguous() if a_mn else A).cuda()
+    Bd = (B.T.contiguous() if b_mn else B).cuda()
+    C = handle.check_gemm(Ad, Bd, bool(a_mn), bool(b_mn), M, N, K).double().cpu().numpy()
+    err = np.linalg.norm(C - ref) / np.linalg.norm(ref)
+    if err > 1e-5:
+        # diagnostics for a layout mistake: compare against likely confusions
+        alt = {"transposed_ref": np.linalg.norm(C - (A.double() @ B.double().T).numpy().T[:M, :N])
+               if M == N else None,
+               "frac_close": float(np.mean(np.isclose(C, ref, rtol=1e-3, atol=1e-2))),
+               "C[0,:4]": C[0, :4].tolist(), "ref[0,:4]": ref[0, :4].tolist(),
+               "C[1,:4]": C[1, :4].tolist(), "ref[1,:4]": ref[1, :4].tolist()}
+        pytest.fail(f"relative error {err:.3e}; {alt}")
+
+
+def test_bounded_wait_reports_timeout(handle):
+    """A device-side wait on a barrier nothing completes gives up after its
+    limit, reports FLCE_ERR_TIMEOUT, and leaves the context usable."""
+    st = handle.check_wait_timeout(2000)   # 2 ms
+    assert st == 5
+    # the context still works afterwards
+    A = torch.ones(128, 64, dtype=torch.bfloat16, device="cuda")
+    B = torch.ones(256, 64, dtype=torch.bfloat16, device="cuda")
+    C = handle.check_gemm(A, B, False, False, 128, 256, 64)
+    assert torch.all(C == 64.0)

@@ -1,0 +1,204 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, element
+by element, on the seeded workloads, at sizes the oracle finishes in seconds
+that still span several tiles and ragged tails, plus the edge cases."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from flce_testing import assert_parity, device_inputs, rel_fro, run, to_np64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bf16():
+    from linear_cross_entropy_token_gb300 import FLCE
+    h = FLCE("bf16", 0, hbm_budget_bytes=4 << 30)
+    yield h
+    h.close()
+
+
+@pytest.fixture(scope="module")
+def bf16_recompute():
+    from linear_cross_entropy_token_gb300 import FLCE
+    h = FLCE("bf16", 0, dlogits_mode="recompute")
+    yield h
+    h.close()
+
+
+@pytest.fixture(scope="module")
+def fp32():
+    from linear_cross_entropy_token_gb300 import FLCE
+    h = FLCE("fp32", 0)
+    yield h
+    h.close()
+
+
+def _oracle(w, chunk=None):
+    return oracle.flce_reference(w.x_f64(), w.W_f64(), w.t, w.ignore_index, chunk=chunk)
+
+
+def test_tiny_fp32_config(fp32):
+    w = workloads.make("tiny_fp32")
+    res = run(fp32, w, chunk=w.spec.chunk)
+    assert res["plan"]["chunk"] == 64 and res["plan"]["num_chunks"] == 4
+    assert_parity(res, _oracle(w), "fp32", token_rtol=1e-5)
+
+
+def test_small_bf16_config(bf16):
+    w = workloads.make("small_bf16")
+    res = run(bf16, w)
+    assert res["plan"]["num_chunks"] == 1
+    assert_parity(res, _oracle(w), "bf16", token_rtol=1e-3)
+
+
+def test_small_bf16_config_recompute(bf16_recompute):
+    w = workloads.make("small_bf16")
+    res = run(bf16_recompute, w)
+    assert_parity(res, _oracle(w), "bf16", token_rtol=1e-3)
+
+
+@pytest.mark.parametrize("N,H,V,chunk,ign", [
+    (1000, 256, 4099, 300, 0.1),     # odd V: last vocab tile holds 3 columns; N % C != 0, C % 128 != 0
+    (512, 512, 50257, 0, 0.05),      # GPT-2-sized vocabulary
+    (256, 128, 4096, 64, 0.0),       # C < 128 in bf16
+    (777, 136, 1000, 256, 0.2),      # H not a multiple of 64 (K tail), V < one 1024-column span
+    (130, 64, 300, 0, 0.0),          # everything smaller than one tile along some axis
+])
+def test_ragged_shapes(bf16, N, H, V, chunk, ign):
+    w = workloads.generate(workloads.custom(N, H, V, "bf16", ignore_frac=ign, seed=N + V))
+    res = run(bf16, w, chunk=chunk)
+    assert_parity(res, _oracle(w), "bf16", token_rtol=1e-3)
+
+
+@pytest.mark.parametrize("N,H,V,chunk", [(1000, 256, 4099, 300), (256, 128, 4096, 64)])
+def test_ragged_shapes_recompute(bf16_recompute, N, H, V, chunk):
+    w = workloads.generate(workloads.custom(N, H, V, "bf16", ignore_frac=0.1, seed=5))
+    assert_parity(run(bf16_recompute, w, chunk=chunk), _oracle(w), "bf16", token_rtol=1e-3)
+
+
+@pytest.mark.parametrize("N,H,V,chunk", [(300, 100, 999, 128), (64, 7, 33, 0)])
+def test_fp32_ragged(fp32, N, H, V, chunk):
+    w = workloads.generate(workloads.custom(N, H, V, "fp32", ignore_frac=0.1, seed=9))
+    assert_parity(run(fp32, w, chunk=chunk), _oracle(w), "fp32", token_rtol=1e-5)
+
+
+def test_chunk_sizes_agree(bf16):
+    """Chunking is exact: every C gives the oracle's result."""
+    w = workloads.generate(workloads.custom(1536, 256, 8192, "bf16", ignore_frac=0.05, seed=2))
+    ref = _oracle(w)
+    for c in (128, 384, 512, 1536, 0):
+        assert_parity(run(bf16, w, chunk=c), ref, "bf16", token_rtol=1e-3)
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_all_tokens_ignored(bf16, fp32):
+    for h, dt in ((bf16, "bf16"), (fp32, "fp32")):
+        w = workloads.generate(workloads.custom(300, 64, 500, dt, seed=3))
+        w.t[:] = -100
+        res = run(h, w, chunk=128)
+        assert res["loss"] == 0.0
+        assert np.all(res["dx"] == 0.0) and np.all(res["dW"] == 0.0)
+        assert np.all(res["token_loss"] == 0.0)
+
+
+def test_empty_batch(bf16):
+    W = torch.randn(100, 64, device="cuda").to(torch.bfloat16)
+    x = torch.empty(0, 64, device="cuda", dtype=torch.bfloat16)
+    t = torch.empty(0, device="cuda", dtype=torch.int64)
+    dW = torch.full((100, 64), 7.0, device="cuda")
+    loss, dx, dW = bf16.forward_backward(x, W, t, dW=dW)
+    assert loss == 0.0 and dx.shape == (0, 64) and torch.all(dW == 0)
+
+
+def test_zero_weight_closed_form(bf16):
+    """W = 0: every logit is 0, loss = ln V, dx = 0 exactly,
+    dW_j = (1/n_v)(sum_valid x_i / V - sum_{valid, t_i = j} x_i)."""
+    w = workloads.generate(workloads.custom(700, 128, 3000, "bf16", ignore_frac=0.1, seed=4))
+    w.W[:] = 0
+    res = run(bf16, w, chunk=256)
+    assert abs(res["loss"] - math.log(3000)) <= 2e-6 * math.log(3000)
+    assert np.all(res["dx"] == 0.0)
+    x = w.x_f64()
+    valid = w.t != -100
+    nv = valid.sum()
+    dW = np.tile(x[valid].sum(0) / 3000, (3000, 1))
+    np.subtract.at(dW, w.t[valid], x[valid])
+    dW /= nv
+    assert rel_fro(res["dW"], dW) <= 1e-2
+
+
+def test_bad_target_reports_status(bf16):
+    from linear_cross_entropy_token_gb300 import FlceError
+    w = workloads.generate(workloads.custom(200, 64, 500, "bf16", seed=6))
+    for bad in (500, -5):
+        w.t[17] = bad
+        x, W, t = device_inputs(w)
+        with pytest.raises(FlceError) as e:
+            bf16.forward_backward(x, W, t)
+        assert e.value.status_name == "FLCE_ERR_BAD_TARGET"
+
+
+def test_other_ignore_index(bf16):
+    w = workloads.generate(workloads.custom(400, 64, 700, "bf16", seed=7))
+    w.t[::5] = 3                     # class 3 marks the ignored tokens
+    res = run(bf16, w, chunk=128, ignore_index=3)
+    ref = oracle.flce_reference(w.x_f64(), w.W_f64(), w.t, ignore_index=3)
+    assert_parity(res, ref, "bf16", token_rtol=1e-3)
+
+
+def test_large_logits_stability(bf16):
+    """W -> W + 1·uᵀ shifts every logit of token i by x_i·u (|z| ~ 100..200,
+    beyond exp's fp32 range): loss and gradients stay finite and match the
+    oracle on the same (rounded) inputs."""
+    w = workloads.generate(workloads.custom(512, 128, 2000, "bf16", ignore_frac=0.05, seed=8))
+    u = np.float32(4.0) * np.sign(np.random.default_rng(0).standard_normal(128)).astype(np.float32)
+    Wf = workloads.bf16_bits_to_f32(w.W) + u[None, :]
+    workloads.round_f32_to_bf16_bits(Wf.astype(np.float32), w.W)
+    ref = _oracle(w)
+    assert np.abs(w.x_f64() @ w.W_f64()[:1].T).max() > 90
+    res = run(bf16, w, chunk=256)
+    assert np.isfinite(res["loss"])
+    assert_parity(res, ref, "bf16", token_rtol=1e-3)
+
+
+def test_repeatable_bit_for_bit(bf16):
+    w = workloads.generate(workloads.custom(1024, 256, 5000, "bf16", ignore_frac=0.1, seed=10))
+    a = run(bf16, w, chunk=384)
+    b = run(bf16, w, chunk=384)
+    assert a["loss"] == b["loss"]
+    assert np.array_equal(a["dx"], b["dx"]) and np.array_equal(a["dW"], b["dW"])
+
+
+def test_host_buffer_entry_point(bf16):
+    w = workloads.generate(workloads.custom(600, 128, 3000, "bf16", ignore_frac=0.1, seed=11))
+    xh = torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Wh = torch.from_numpy(w.W.view(np.int16)).view(torch.bfloat16).pin_memory()
+    th = torch.from_numpy(w.t).pin_memory()
+    loss, dx, dW = bf16.forward_backward_host(xh, Wh, th, chunk=256)
+    res = {"loss": loss, "dx": to_np64(dx), "dW": to_np64(dW)}
+    assert_parity(res, _oracle(w), "bf16")
+
+
+def test_caller_workspace(bf16):
+    from linear_cross_entropy_token_gb300 import FLCE, FlceError, plan
+    w = workloads.generate(workloads.custom(500, 64, 1000, "bf16", seed=12))
+    p = plan(500, 64, 1000, "bf16", chunk=256)
+    h = FLCE("bf16", 0)
+    try:
+        buf = torch.empty(p["workspace_bytes"] + 4096, dtype=torch.uint8, device="cuda")
+        off = (-buf.data_ptr()) % 1024
+        h.set_workspace(buf[off:off + p["workspace_bytes"]])
+        assert_parity(run(h, w, chunk=256), _oracle(w), "bf16")
+        small = buf[off:off + 1024]
+        h.set_workspace(small)
+        with pytest.raises(FlceError) as e:
+            run(h, w, chunk=256)
+        assert e.value.status_name == "FLCE_ERR_BUDGET"
+    finally:
+        h.close()
