@@ -39,7 +39,7 @@ HBM_BOUND = {"dlogits_inplace", "lse_combine", "dx_split_reduce", "count_valid",
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=40)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="llama3_bf16")

@@ -90,7 +90,7 @@ Layout make_layout(int64_t N, int64_t H, int64_t C, int64_t ldv, int64_t vt, int
   L.zt = take(static_cast<uint64_t>(C) * 4);
   L.lse = take(static_cast<uint64_t>(C) * 4);
   L.token_loss = take(static_cast<uint64_t>(std::max<int64_t>(N, 1)) * 4);
-  L.dxpart = take(splits > 1 ? static_cast<uint64_t>(splits) * C * H * 4 : 0);
+  L.dxpart = take(static_cast<uint64_t>(splits) * C * H * 4);  // bf16 path: fp32 dx partials
   L.total = off;
   return L;
 }
@@ -135,7 +135,7 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   std::memset(out, 0, sizeof(*out));
   out->ldv = static_cast<int64_t>(align_up(static_cast<uint64_t>(V), 64));
   out->vocab_tiles = cdiv(V, kVocabTile);
-  auto splits_for = [&](int64_t C) { return bf16 ? pick_dx_splits(C, H, V, num_sms) : 1; };
+  auto splits_for = [&](int64_t C) { return bf16 ? pick_dx_splits(C, H, V, num_sms) : 0; };
   auto ws = [&](int64_t C) {
     return make_layout(N, H, C, out->ldv, out->vocab_tiles, splits_for(C), esize).total;
   };
@@ -171,8 +171,9 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   }
   out->chunk = C;
   out->num_chunks = C ? cdiv(N, C) : 0;
-  out->dx_splits = C ? splits_for(C) : 1;
-  out->workspace_bytes = make_layout(N, H, C, out->ldv, out->vocab_tiles, out->dx_splits, esize).total;
+  out->dx_splits = std::max<int64_t>(1, C ? splits_for(C) : 1);
+  out->workspace_bytes =
+      make_layout(N, H, C, out->ldv, out->vocab_tiles, C ? splits_for(C) : 0, esize).total;
   out->logits_bytes = static_cast<uint64_t>(C) * out->ldv * esize;
   return FLCE_OK;
 }
@@ -369,7 +370,7 @@ flce_status read_back(flce_handle_t h, uint32_t* ctrl_dev, cudaStream_t s, float
 flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t* t, int64_t N,
                    int64_t H, int64_t V, int64_t ignore_index, int64_t chunk, float* loss, void* dx,
                    float* dW, cudaStream_t s) {
-  if (!x || !W || !t || !loss || !dW || (N > 0 && !dx))
+  if (!W || !loss || !dW || (N > 0 && (!x || !t || !dx)))
     return fail(h, FLCE_ERR_INVALID_ARG, "null pointer argument");
   const bool bf16 = h->cfg.dtype == FLCE_DTYPE_BF16;
   if (bf16) {
@@ -383,7 +384,8 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
   if (st != FLCE_OK) return fail(h, st, "%s", why.c_str());
   st = ensure_workspace(h, p.workspace_bytes);
   if (st != FLCE_OK) return st;
-  const Layout L = make_layout(N, H, p.chunk, p.ldv, p.vocab_tiles, p.dx_splits, bf16 ? 2 : 4);
+  const Layout L =
+      make_layout(N, H, p.chunk, p.ldv, p.vocab_tiles, bf16 ? p.dx_splits : 0, bf16 ? 2 : 4);
   uint8_t* ws = static_cast<uint8_t*>(h->ws);
   uint32_t* ctrl = reinterpret_cast<uint32_t*>(ws + L.ctrl);
   float2* partials = reinterpret_cast<float2*>(ws + L.partials);
@@ -508,19 +510,16 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       b.cols = static_cast<int>(H);
       b.reduce_add = 0;
       units = b.num_m * b.num_n * b.num_s;
-      if (S == 1) {
-        if (!map_bf16_2d(&mDx, dxb + off * H, H, rows, H * 2, 64, 128, &why))
-          return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
-        FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, 2 * dr * dV + 2 * dV * dH + 2 * dr * dH,
-                    launch_umma(kUmmaDxBf16, mZ_k, mW_mn, mDx, b, std::min(units, sms), s));
-      } else {
-        if (!map_f32_3d(&mDx, dxpart, H, rows, S, H * 4, static_cast<uint64_t>(C) * H * 4, &why))
-          return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
-        FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH,
-                    launch_umma(kUmmaDxF32, mZ_k, mW_mn, mDx, b, std::min(units, sms), s));
-        FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4.0 * S * dr * dH + 2 * dr * dH,
-                    launch_dx_reduce(dxpart, S, C * H, rows, H, dxb + off * H, s));
-      }
+      // fp32 partials of softmax·W / n_valid per split; the reduction subtracts
+      // W[t_i] / n_valid in fp32, rounds dx to bf16 once, and completes the
+      // dlogits rows (-1 / n_valid at the target) for the dW GEMM
+      if (!map_f32_3d(&mDx, dxpart, H, rows, S, H * 4, static_cast<uint64_t>(C) * H * 4, &why))
+        return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
+      FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH,
+                  launch_umma(kUmmaDxF32, mZ_k, mW_mn, mDx, b, std::min(units, sms), s));
+      FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4.0 * S * dr * dH + 4 * dr * dH,
+                  launch_dx_reduce(dxpart, S, C * H, rows, H, static_cast<const __nv_bfloat16*>(W), V,
+                                   t + off, ignore_index, ctrl, logits, ldv, dxb + off * H, s));
       // 4. dW (+)= dlogitsᵀ · x_chunk, fp32 (stored on the first chunk, added after)
       UmmaArgs d = a;
       d.num_m = static_cast<int>(cdiv(V, kBM));

@@ -81,7 +81,9 @@ cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, con
                                const int64_t* t_chunk, int64_t ignore_index,
                                const uint32_t* ctrl, cudaStream_t s);
 cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_stride, int rows,
-                             int64_t H, __nv_bfloat16* dx, cudaStream_t s);
+                             int64_t H, const __nv_bfloat16* W, int64_t V, const int64_t* t_chunk,
+                             int64_t ignore_index, const uint32_t* ctrl, __nv_bfloat16* buf,
+                             int64_t ldv, __nv_bfloat16* dx, cudaStream_t s);
 cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* ctrl,
                                  cudaStream_t s);
 

@@ -342,20 +342,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               stage_and_store(w, [&](uint32_t src) { tma_store_2d(&tmO, src, c0, m0); });
             }
           } else {
-            // dlogits = (exp(z - lse) - onehot) * scale, written over the logits buffer
-            const int k = (tcol >= g * 64 && tcol < g * 64 + 64) ? tcol - g * 64 : -1;
+            // softmax / n_valid = exp(z - lse) * scale, written over the logits
+            // buffer; the dx reduction adds the -onehot / n_valid term
             uint32_t w[32];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               float v[4] = {__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]),
                             __uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])};
-              const int ci[4] = {2 * i, 2 * i + 1, 32 + 2 * i, 33 + 2 * i};
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                float p = ex2_approx(fmaf(v[q], kLog2e, -lse_l2));
-                if (ci[q] == k) p -= 1.0f;
-                v[q] = p * scale;
-              }
+              for (int q = 0; q < 4; ++q) v[q] = ex2_approx(fmaf(v[q], kLog2e, -lse_l2)) * scale;
               w[i] = pack_bf16x2(v[0], v[1]);
               w[16 + i] = pack_bf16x2(v[2], v[3]);
             }

@@ -69,6 +69,11 @@ CONFIGS = {
                              Fraction(1, 20)),
     "long_bf16": ConfigSpec("long_bf16", 131072, 4096, 128256, "bf16", "uniform",
                             Fraction(0)),
+    # one 4096-token chunk of the Llama-3-shaped batch against a 32768-entry
+    # slice of the vocabulary: the same kernels at a size a profiler replays
+    # quickly (W is 268 MB, above the 129 MB L2)
+    "one_chunk_bf16": ConfigSpec("one_chunk_bf16", 4096, 4096, 32768, "bf16", "zipf",
+                                 Fraction(1, 20)),
 }
 
 # chunk sizes swept on the Qwen3-shaped config
