@@ -61,6 +61,15 @@ class OracleResult:
 
 # ---------------------------------------------------------------- the steps
 
+def _values(a) -> np.ndarray:
+    """Inputs as float64 values; integer arrays (such as raw bf16 bit
+    patterns) are refused rather than read as numbers."""
+    a = np.asarray(a)
+    if a.dtype.kind in "iub":
+        raise TypeError("the oracle takes real-valued inputs; widen bf16 bit patterns first")
+    return a.astype(np.float64, copy=False)
+
+
 def check_targets(t: np.ndarray, V: int, ignore_index: int) -> None:
     t = np.asarray(t)
     bad = (t != ignore_index) & ((t < 0) | (t >= V))
@@ -129,8 +138,8 @@ def flce_reference(x: np.ndarray, W: np.ndarray, t: np.ndarray,
     dlogitsᵀ·x_chunk into dW; divide loss and gradients by the token count
     (n_valid) at the end. Both orders give the same result up to rounding.
     """
-    x = np.asarray(x, dtype=np.float64)
-    W = np.asarray(W, dtype=np.float64)
+    x = _values(x)
+    W = _values(W)
     t = np.asarray(t, dtype=np.int64)
     N, H = x.shape
     V, H2 = W.shape
@@ -192,11 +201,11 @@ def lse_rows(x: np.ndarray, W: np.ndarray, rows: Sequence[int],
              block: int = 256) -> np.ndarray:
     """log-sum-exp of the logits of the given tokens (float64)."""
     rows = np.asarray(rows, dtype=np.int64)
-    Wd = np.asarray(W, dtype=np.float64)
+    Wd = _values(W)
     out = np.empty(len(rows))
     for s in range(0, len(rows), block):
         r = rows[s:s + block]
-        out[s:s + block] = logsumexp_rows(project(np.asarray(x[r], np.float64), Wd))
+        out[s:s + block] = logsumexp_rows(project(_values(x[r]), Wd))
     return out
 
 
@@ -204,8 +213,8 @@ def token_loss_rows(x, W, t, rows, ignore_index: int = IGNORE_INDEX) -> np.ndarr
     """Per-token loss (0 for ignored tokens) of the given tokens."""
     rows = np.asarray(rows, dtype=np.int64)
     t = np.asarray(t, dtype=np.int64)
-    Wd = np.asarray(W, dtype=np.float64)
-    xr = np.asarray(x[rows], np.float64)
+    Wd = _values(W)
+    xr = _values(x[rows])
     z = project(xr, Wd)
     v = valid_mask(t[rows], ignore_index)
     return token_losses(logsumexp_rows(z), target_logits(z, t[rows], v), v)
@@ -215,8 +224,8 @@ def dx_rows(x, W, t, rows, n_valid: int, ignore_index: int = IGNORE_INDEX) -> np
     """Rows of dx = dlogits·W for the given tokens; needs only their own logits."""
     rows = np.asarray(rows, dtype=np.int64)
     t = np.asarray(t, dtype=np.int64)
-    Wd = np.asarray(W, dtype=np.float64)
-    z = project(np.asarray(x[rows], np.float64), Wd)
+    Wd = _values(W)
+    z = project(_values(x[rows]), Wd)
     v = valid_mask(t[rows], ignore_index)
     if n_valid == 0:
         return np.zeros((len(rows), Wd.shape[1]))
@@ -231,14 +240,14 @@ def dW_rows(x, W, t, vocab_rows, lse_all: np.ndarray, n_valid: int,
     token (lse_all, from lse_rows over all tokens)."""
     J = np.asarray(vocab_rows, dtype=np.int64)
     t = np.asarray(t, dtype=np.int64)
-    WJ = np.asarray(W[J], np.float64)
+    WJ = _values(W[J])
     N = len(t)
     out = np.zeros((len(J), WJ.shape[1]))
     if n_valid == 0:
         return out
     for s in range(0, N, block):
         e = min(N, s + block)
-        xb = np.asarray(x[s:e], np.float64)
+        xb = _values(x[s:e])
         zJ = project(xb, WJ)                                  # (b, |J|)
         g = np.exp(zJ - lse_all[s:e, None])
         tb = t[s:e]

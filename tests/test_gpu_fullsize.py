@@ -41,23 +41,24 @@ class Ref:
 
     def __init__(self, w, full_lse=True):
         self.w = w
+        x = workloads.F64Rows(w.x)
         self.Wd = w.W_f64()
         self.valid = oracle.valid_mask(w.t, w.ignore_index)
         self.n_valid = int(self.valid.sum())
         self.rows = _sample_rows(w)
         self.J = _sample_vocab(w)
-        self.tok = oracle.token_loss_rows(w.x, self.Wd, w.t, self.rows)
-        self.dx = oracle.dx_rows(w.x, self.Wd, w.t, self.rows, self.n_valid)
+        self.tok = oracle.token_loss_rows(x, self.Wd, w.t, self.rows)
+        self.dx = oracle.dx_rows(x, self.Wd, w.t, self.rows, self.n_valid)
         self.lse = None
         if full_lse:
-            self.lse = oracle.lse_rows(w.x, self.Wd, np.arange(w.N), block=512)
+            self.lse = oracle.lse_rows(x, self.Wd, np.arange(w.N), block=512)
             zt = np.zeros(w.N)
             vi = np.flatnonzero(self.valid)
             for s in range(0, len(vi), 4096):
                 r = vi[s:s + 4096]
                 zt[r] = np.einsum("ij,ij->i", w.x_f64(r), self.Wd[w.t[r]])
             self.loss = float(np.sum((self.lse - zt)[self.valid])) / self.n_valid
-            self.dW = oracle.dW_rows(w.x, self.Wd, w.t, self.J, self.lse, self.n_valid)
+            self.dW = oracle.dW_rows(x, self.Wd, w.t, self.J, self.lse, self.n_valid)
 
 
 def _check(handle, w, ref, chunk=0):

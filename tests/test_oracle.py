@@ -241,6 +241,24 @@ def test_sampled_outputs_equal_full_result():
                                atol=1e-14)
 
 
+def test_one_by_one_outputs_on_bf16_rows():
+    """The one-by-one functions take a lazily widened bf16 matrix and refuse
+    raw bit patterns."""
+    w = workloads.generate(workloads.custom(60, 16, 50, "bf16", ignore_frac=0.1, seed=13))
+    r = oracle.flce_reference(w.x_f64(), w.W_f64(), w.t)
+    xr = workloads.F64Rows(w.x)
+    rows = np.array([1, 7, 59])
+    np.testing.assert_allclose(oracle.dx_rows(xr, w.W_f64(), w.t, rows, r.n_valid), r.dx[rows],
+                               atol=1e-14)
+    lse = oracle.lse_rows(xr, w.W_f64(), np.arange(60))
+    np.testing.assert_allclose(oracle.dW_rows(xr, w.W_f64(), w.t, [0, 49], lse, r.n_valid),
+                               r.dW[[0, 49]], atol=1e-14)
+    with pytest.raises(TypeError):
+        oracle.token_loss_rows(w.x, w.W_f64(), w.t, rows)
+    with pytest.raises(TypeError):
+        oracle.flce_reference(w.x, w.W, w.t)
+
+
 # --------------------------------------- planted mistakes fail the pins
 
 def _fd_mismatch(monkeypatch_target, replacement, monkeypatch):

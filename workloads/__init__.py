@@ -121,6 +121,21 @@ def to_f64(a: np.ndarray) -> np.ndarray:
     return a.astype(np.float64)
 
 
+class F64Rows:
+    """Rows of an input matrix (bf16 bits or float32), widened to float64 when
+    indexed, so that a consumer never holds a full-size matrix in float64."""
+
+    def __init__(self, a: np.ndarray):
+        self.a = a
+        self.shape = a.shape
+
+    def __len__(self) -> int:
+        return self.shape[0]
+
+    def __getitem__(self, idx) -> np.ndarray:
+        return to_f64(self.a[idx])
+
+
 def round_f32_to_bf16_bits(f: np.ndarray, out: np.ndarray) -> None:
     """Round float32 values (finite) to bfloat16 bits, nearest-even, into out."""
     b = f.view(np.uint32)
