@@ -15,7 +15,6 @@ Under torchrun each rank runs an independent replica of the workload.
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import os
 import statistics
@@ -84,6 +83,13 @@ def max_over_ranks(ws, value: float, device=None) -> float:
     return float(t.item())
 
 
+def aggregate(ws, tokens_per_rank: int, ms_local: float, device=None):
+    """Whole-job throughput of independent replicas: every rank processed
+    tokens_per_rank tokens; the job took as long as the slowest rank."""
+    ms_max = max_over_ranks(ws, ms_local, device)
+    return ms_max, ws * tokens_per_rank / (ms_max / 1e3)
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -145,14 +151,8 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "linear_cross_entropy_token_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
-    return h.hexdigest()[:16]
+    from linear_cross_entropy_token_gb300.build import source_hash
+    return source_hash()
 
 
 def traffic_for(kernel: str, workload: str, chunk: int):
@@ -276,10 +276,8 @@ def run_ours(args, ws, rank, local):
     ms = ev0.elapsed_time(ev1) / args.steps
     prof = h.profile()
     h.set_profiling(False)
-    ms_max = max_over_ranks(ws, ms, dev if ws > 1 else None)
-
     tokens = N
-    value = ws * tokens / (ms_max / 1e3)
+    ms_max, value = aggregate(ws, tokens, ms, dev if ws > 1 else None)
     flops = 6.0 * N * H * V
     tflops = flops / (ms_max / 1e3) / 1e12
     peaks, peaks_kind = load_peaks()
@@ -321,8 +319,8 @@ def run_ours(args, ws, rank, local):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(ws)
-        ems = max_over_ranks(ws, e0.elapsed_time(e1) / args.steps, dev if ws > 1 else None)
-        e2e = {"value": ws * tokens / (ems / 1e3), "unit": UNIT,
+        ems, evalue = aggregate(ws, tokens, e0.elapsed_time(e1) / args.steps, dev if ws > 1 else None)
+        e2e = {"value": evalue, "unit": UNIT,
                "h2d_bytes_per_step": int(x_h.numel() * 2 + W_h.numel() * 2 + t_h.numel() * 8),
                "d2h_bytes_per_step": 4, "ms_per_step": ems,
                "path": "flce_forward_backward_host: pinned host x, W, t copied in; loss read back"}

@@ -130,7 +130,12 @@ def main(argv=None):
         fmt = lambda v: f"{v:.4g}" if isinstance(v, float) else str(v)
         print(_md_table(keys, [[fmt(d.get(k)) for k in keys] for d in res]))
     elif cmd == "traffic":
-        print(json.dumps(traffic(path), indent=1))
+        # optional: --workload NAME --chunk C, recorded with the kernel source hash
+        opts = dict(zip(argv[2::2], argv[3::2]))
+        from .build import source_hash
+        out = {"workload": opts.get("--workload"), "chunk": int(opts.get("--chunk", 0)),
+               "source_hash": source_hash(), "kernels": traffic(path)}
+        print(json.dumps(out, indent=1))
     else:
         print(__doc__)
         return 2
