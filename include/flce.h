@@ -204,6 +204,33 @@ int64_t flce_launch_count(flce_handle_t h);
 /* One-line reason for the handle's last failure ("" if none). */
 const char* flce_last_error(flce_handle_t h);
 
+/* ---- loss without any allocation ------------------------------------------
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot let a library allocate device memory: a framework whose pool
+ * allocator must account for every byte, a runtime on a fixed memory plan
+ * decided ahead of time, or code that must not pay the device-wide
+ * synchronisation that cudaFree implies.
+ *
+ * Computes the mean loss and the per-token losses of x·Wᵀ (bf16 x and W, as
+ * flce_forward_backward, same layout rules) without dx or dW, and without a
+ * handle: it calls no cudaMalloc, cudaFree or allocating library routine. Its
+ * scratch is one file-scope device array of 64 MiB, which every GPU that loads
+ * the library holds until the process exits. That bounds V: one 128-token
+ * chunk needs 128 x ceil(V/256) x 8 bytes of it, so V up to about 16.7 million.
+ * Larger V returns INVALID_ARG.
+ *   x, W, t      device inputs as for flce_forward_backward (current device)
+ *   loss         host, receives the fp32 mean loss
+ *   token_loss   device, N fp32 outputs (0 for ignored tokens)
+ * The first call on a device looks up the device address of the scratch
+ * array (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture. Every call on a device shares the one
+ * array, so calls that overlap on the GPU (other streams, other threads)
+ * race: run them one after another. Synchronises the stream before
+ * returning. Errors: INVALID_ARG, BAD_TARGET, TIMEOUT, CUDA. */
+flce_status flce_loss_static(const void* x, const void* W, const int64_t* t, int64_t N,
+                             int64_t H, int64_t V, int64_t ignore_index, float* loss,
+                             float* token_loss, void* stream);
+
 /* ---- checks of single parts (used by the tests) ------------------------- */
 
 /* The tcgen05 GEMM core alone: C[M x N] (fp32, row-major, device) = A·B over

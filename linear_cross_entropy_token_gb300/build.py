@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libflce.so")
-SOURCES = ["flce_api.cu", "flce_umma.cu", "flce_rows.cu", "flce_simt.cu"]
+SOURCES = ["flce_api.cu", "flce_umma.cu", "flce_rows.cu", "flce_simt.cu", "flce_static.cu"]
 HEADERS = ["ptx.cuh", "flce_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

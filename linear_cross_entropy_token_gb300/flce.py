@@ -88,6 +88,8 @@ def load() -> ctypes.CDLL:
         "flce_last_error": (ctypes.c_char_p, [vp]),
         "flce_check_gemm": (i32, [vp, i32, i32, vp, vp, vp, i64, i64, i64, vp]),
         "flce_check_wait_timeout": (i32, [vp, u32, vp]),
+        "flce_loss_static": (i32, [vp, vp, vp, i64, i64, i64, i64, ctypes.POINTER(ctypes.c_float),
+                                   vp, vp]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(lib, name)
@@ -252,6 +254,27 @@ class FLCE:
         import torch
         return int(self.lib.flce_check_wait_timeout(self.h, timeout_us,
                                                     _stream_ptr(torch.device("cuda", self.device))))
+
+
+def loss_static(x, W, t, ignore_index: int = -100, token_loss=None):
+    """Mean loss and per-token losses (no dx, dW) through flce_loss_static,
+    which allocates no device memory: for callers whose device memory must
+    all come from their own allocator. Returns (loss, token_loss)."""
+    import torch
+    lib = load()
+    N, H = x.shape
+    V = W.shape[0]
+    if x.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or t.dtype != torch.int64:
+        raise ValueError("x and W must be bf16, t int64")
+    if token_loss is None:
+        token_loss = torch.empty(N, dtype=torch.float32, device=x.device)
+    loss = ctypes.c_float(0.0)
+    with torch.cuda.device(x.device):
+        st = lib.flce_loss_static(x.data_ptr(), W.data_ptr(), t.data_ptr(), N, H, V, ignore_index,
+                                  ctypes.byref(loss), token_loss.data_ptr(), _stream_ptr(x.device))
+    if st != FLCE_OK:
+        raise FlceError(st, "flce_loss_static")
+    return loss.value, token_loss
 
 
 _handles = {}
