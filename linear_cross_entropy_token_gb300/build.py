@@ -32,13 +32,16 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def source_hash() -> str:
-    """Short hash of the CUDA sources (identifies the kernels a profile of
-    them describes)."""
+GEMM_SOURCES = ("flce_umma.cu", "ptx.cuh", "flce_internal.h")
+
+
+def source_hash(names=GEMM_SOURCES) -> str:
+    """Short hash of CUDA sources (by default those of the tcgen05 GEMM
+    kernels), identifying the kernels a profile of them describes."""
     import hashlib
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")):
+    for name in sorted(names):
+        if os.path.exists(os.path.join(CSRC, name)):
             with open(os.path.join(CSRC, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
