@@ -74,12 +74,21 @@ enum { FLCE_DTYPE_BF16 = 0, FLCE_DTYPE_FP32 = 1 };
  *  AUTO:      INPLACE, the faster of the two on GB300 by measurement. */
 enum { FLCE_DLOGITS_AUTO = 0, FLCE_DLOGITS_INPLACE = 1, FLCE_DLOGITS_RECOMPUTE = 2 };
 
+/* Tile shape of the tcgen05 GEMMs (bf16 only).
+ *  SINGLE: one CTA per 128 x 256 output tile (tcgen05 cta_group::1).
+ *  PAIR:   a cluster of two CTAs on two SMs per 256 x 256 tile
+ *          (tcgen05 cta_group::2): each CTA loads half of the B operand.
+ *  AUTO:   SINGLE. */
+enum { FLCE_CTA_AUTO = 0, FLCE_CTA_SINGLE = 1, FLCE_CTA_PAIR = 2 };
+
 typedef struct flce_config {
     int32_t dtype;               /* FLCE_DTYPE_*                                       */
     int32_t device;              /* CUDA device ordinal                                */
     uint64_t hbm_budget_bytes;   /* workspace budget for the chunk planner; 0 = 1.25 GiB*/
     int32_t dlogits_mode;        /* FLCE_DLOGITS_*                                     */
     int32_t timeout_ms;          /* limit of every device-side wait; 0 = 2000 ms       */
+    int32_t cta_pair;            /* FLCE_CTA_*                                         */
+    int32_t reserved;            /* must be 0                                          */
 } flce_config;
 
 /* The chunk plan of one call (token-chunk scheduler). */

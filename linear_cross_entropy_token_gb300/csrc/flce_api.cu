@@ -95,16 +95,26 @@ Layout make_layout(int64_t N, int64_t H, int64_t C, int64_t ldv, int64_t vt, int
   return L;
 }
 
-int pick_dx_splits(int64_t C, int64_t H, int64_t V, int num_sms) {
-  const int64_t tiles = cdiv(C, kBM) * cdiv(H, kBN);
+// CTA pairs are the default tile shape (FLCE_CTA_AUTO)
+constexpr bool kAutoPair = false;
+
+bool wants_pair(const flce_config* cfg) {
+  return cfg->dtype == FLCE_DTYPE_BF16 &&
+         (cfg->cta_pair == FLCE_CTA_PAIR || (cfg->cta_pair == FLCE_CTA_AUTO && kAutoPair));
+}
+
+// Splits of the dx GEMM's V reduction that fill the machine's waves best:
+// `slots` work units run at once (SMs, or SM pairs), each tile_m x 256.
+int pick_dx_splits(int64_t C, int64_t H, int64_t V, int slots, int tile_m) {
+  const int64_t tiles = cdiv(C, tile_m) * cdiv(H, kBN);
   const int64_t kb = cdiv(V, kBK);
   int best = 1;
   double best_score = -1;
   for (int s = 1; s <= 4; ++s) {
     if (s > 1 && kb / s < 16) break;
     const int64_t units = tiles * s;
-    const int64_t waves = cdiv(units, num_sms);
-    const double eff = static_cast<double>(units) / static_cast<double>(waves * num_sms);
+    const int64_t waves = cdiv(units, slots);
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * slots);
     const double score = eff - 0.01 * (s - 1);
     if (score > best_score + 1e-12) {
       best_score = score;
@@ -135,7 +145,10 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   std::memset(out, 0, sizeof(*out));
   out->ldv = static_cast<int64_t>(align_up(static_cast<uint64_t>(V), 64));
   out->vocab_tiles = cdiv(V, kVocabTile);
-  auto splits_for = [&](int64_t C) { return bf16 ? pick_dx_splits(C, H, V, num_sms) : 0; };
+  const bool pair = wants_pair(cfg);
+  auto splits_for = [&](int64_t C) {
+    return bf16 ? pick_dx_splits(C, H, V, pair ? num_sms / 2 : num_sms, pair ? 2 * kBM : kBM) : 0;
+  };
   auto ws = [&](int64_t C) {
     return make_layout(N, H, C, out->ldv, out->vocab_tiles, splits_for(C), esize).total;
   };
@@ -186,6 +199,8 @@ struct flce_handle_s {
   flce_config cfg{};
   int device = 0;
   int num_sms = 0;
+  int pair_clusters = 0;  // clusters of two the pair kernels fit at once
+  bool use_pair = false;  // GEMMs on CTA pairs (256 x 256 tiles)
   uint64_t timeout_ns = 0;
   std::string err;
   // workspace
@@ -367,6 +382,20 @@ flce_status read_back(flce_handle_t h, uint32_t* ctrl_dev, cudaStream_t s, float
   return FLCE_OK;
 }
 
+// One GEMM on the handle's tile shape; sets num_m from the M extent and the
+// grid from the work units (persistent CTAs, or CTA pairs).
+cudaError_t launch_gemm(flce_handle_t h, int kind, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& o, UmmaArgs args, int64_t M, cudaStream_t s) {
+  if (h->use_pair) {
+    args.num_m = static_cast<int>(cdiv(M, 2 * kBM));
+    const int units = args.num_m * args.num_n * args.num_s;
+    return launch_umma_pair(kind, a, b, o, args, std::min(units, h->pair_clusters), s);
+  }
+  args.num_m = static_cast<int>(cdiv(M, kBM));
+  const int units = args.num_m * args.num_n * args.num_s;
+  return launch_umma(kind, a, b, o, args, std::min(units, h->num_sms), s);
+}
+
 flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t* t, int64_t N,
                    int64_t H, int64_t V, int64_t ignore_index, int64_t chunk, float* loss, void* dx,
                    float* dW, cudaStream_t s) {
@@ -441,11 +470,11 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
     float* dxpart = reinterpret_cast<float*>(ws + L.dxpart);
     const bool recompute = h->cfg.dlogits_mode == FLCE_DLOGITS_RECOMPUTE;
     CUtensorMap mW_k, mW_mn, mX_k, mX_mn, mZ_out, mZ_k, mZ_mn, mDx, mDw;
-    if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, 256, &why) ||
+    // a CTA of a pair loads 128 of the tile's 256 columns of a K-major B
+    if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, h->use_pair ? 128 : 256, &why) ||
         !map_bf16_2d(&mW_mn, W, H, V, H * 2, 64, 64, &why) ||
         !map_f32_3d(&mDw, dW, H, V, 1, H * 4, static_cast<uint64_t>(V) * H * 4, &why))
       return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
-    const int sms = h->num_sms;
     const int kb_h = static_cast<int>(cdiv(H, kBK));
     const int kb_v = static_cast<int>(cdiv(V, kBK));
     for (int64_t c = 0; c < p.num_chunks; ++c) {
@@ -462,7 +491,6 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
 
       // 1. projection with the online max / sum-exp epilogue
       UmmaArgs a{};
-      a.num_m = static_cast<int>(cdiv(rows, kBM));
       a.num_n = vt;
       a.num_s = 1;
       a.kb_total = kb_h;
@@ -479,17 +507,16 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       a.lse = lse;
       a.ctrl = ctrl;
       a.timeout_ns = h->timeout_ns;
-      int units = a.num_m * a.num_n;
       FLCE_LAUNCH(FLCE_K_GEMM_LOGITS, 2 * dr * dH * dV,
                   2 * dr * dH + 2 * dV * dH + (recompute ? 0 : 2 * dr * dV) + 8 * dr * vt + 12 * dr,
-                  launch_umma(kUmmaLogits, mX_k, mW_k, mZ_out, a, std::min(units, sms), s));
+                  launch_gemm(h, kUmmaLogits, mX_k, mW_k, mZ_out, a, rows, s));
       // 2a. cross-tile log-sum-exp and token losses
       FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
                   launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
       // 2b. dlogits = (softmax - onehot) / n_valid over the chunk buffer
       if (recompute) {
         FLCE_LAUNCH(FLCE_K_GEMM_DLOGITS, 2 * dr * dH * dV, 2 * dr * dH + 2 * dV * dH + 2 * dr * dV + 12 * dr,
-                    launch_umma(kUmmaDlogits, mX_k, mW_k, mZ_out, a, std::min(units, sms), s));
+                    launch_gemm(h, kUmmaDlogits, mX_k, mW_k, mZ_out, a, rows, s));
       } else {
         FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 4 * dr * dV,
                     launch_dlogits_bf16(logits, ldv, rows, V, partials, vt, lse, t + off, ignore_index,
@@ -500,7 +527,6 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       const int kbps = (kb_v + S_req - 1) / S_req;
       const int S = (kb_v + kbps - 1) / kbps;
       UmmaArgs b = a;
-      b.num_m = static_cast<int>(cdiv(rows, kBM));
       b.num_n = static_cast<int>(cdiv(H, kBN));
       b.num_s = S;
       b.kb_total = kb_v;
@@ -509,20 +535,18 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       b.rows = rows;
       b.cols = static_cast<int>(H);
       b.reduce_add = 0;
-      units = b.num_m * b.num_n * b.num_s;
       // fp32 partials of softmax·W / n_valid per split; the reduction subtracts
       // W[t_i] / n_valid in fp32, rounds dx to bf16 once, and completes the
       // dlogits rows (-1 / n_valid at the target) for the dW GEMM
       if (!map_f32_3d(&mDx, dxpart, H, rows, S, H * 4, static_cast<uint64_t>(C) * H * 4, &why))
         return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
       FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH,
-                  launch_umma(kUmmaDxF32, mZ_k, mW_mn, mDx, b, std::min(units, sms), s));
+                  launch_gemm(h, kUmmaDxF32, mZ_k, mW_mn, mDx, b, rows, s));
       FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4.0 * S * dr * dH + 4 * dr * dH,
                   launch_dx_reduce(dxpart, S, C * H, rows, H, static_cast<const __nv_bfloat16*>(W), V,
                                    t + off, ignore_index, ctrl, logits, ldv, dxb + off * H, s));
       // 4. dW (+)= dlogitsᵀ · x_chunk, fp32 (stored on the first chunk, added after)
       UmmaArgs d = a;
-      d.num_m = static_cast<int>(cdiv(V, kBM));
       d.num_n = static_cast<int>(cdiv(H, kBN));
       d.num_s = 1;
       d.kb_total = static_cast<int>(cdiv(rows, kBK));
@@ -531,10 +555,9 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       d.rows = static_cast<int>(V);
       d.cols = static_cast<int>(H);
       d.reduce_add = c > 0 ? 1 : 0;
-      units = d.num_m * d.num_n;
       FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dV * dH,
                   2 * dr * dV + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dV * dH,
-                  launch_umma(kUmmaDw, mZ_mn, mX_mn, mDw, d, std::min(units, sms), s));
+                  launch_gemm(h, kUmmaDw, mZ_mn, mX_mn, mDw, d, V, s));
     }
   }
   FLCE_LAUNCH(FLCE_K_LOSS_FINALIZE, 0.0, 4.0 * N, launch_loss_finalize(token_loss, N, ctrl, s));
@@ -605,6 +628,14 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
   h->num_sms = prop.multiProcessorCount;
   h->timeout_ns = static_cast<uint64_t>(cfg->timeout_ms > 0 ? cfg->timeout_ms : 2000) * 1000000ull;
   DeviceGuard g(h->device);
+  if (cfg->dtype == FLCE_DTYPE_BF16) {
+    h->pair_clusters = umma_pair_max_clusters();
+    if (cfg->cta_pair == FLCE_CTA_PAIR && h->pair_clusters <= 0) {
+      delete h;
+      return FLCE_ERR_UNSUPPORTED;
+    }
+    h->use_pair = wants_pair(cfg) && h->pair_clusters > 0;
+  }
   if (cudaMallocHost(&h->host_ctrl, kCtrlWords * 4) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -758,7 +789,7 @@ flce_status flce_check_gemm(flce_handle_t h, int32_t a_mn_major, int32_t b_mn_ma
   bool ok = a_mn_major ? map_bf16_2d(&ma, A, M, K, M * 2, 64, 64, &why)
                        : map_bf16_2d(&ma, A, K, M, K * 2, 64, 128, &why);
   ok = ok && (b_mn_major ? map_bf16_2d(&mb, B, N, K, N * 2, 64, 64, &why)
-                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, 256, &why));
+                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, h->use_pair ? 128 : 256, &why));
   ok = ok && map_f32_3d(&mc, C, N, M, 1, N * 4, static_cast<uint64_t>(M) * N * 4, &why);
   if (!ok) return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
   UmmaArgs a{};
@@ -777,7 +808,7 @@ flce_status flce_check_gemm(flce_handle_t h, int32_t a_mn_major, int32_t b_mn_ma
   const double flops = 2.0 * M * N * K;
   const int kkind = a_mn_major ? FLCE_K_GEMM_DW : (b_mn_major ? FLCE_K_GEMM_DX : FLCE_K_GEMM_LOGITS);
   FLCE_LAUNCH(kkind, flops, 2.0 * (M * K + N * K) + 4.0 * M * N,
-              launch_umma(kind, ma, mb, mc, a, std::min(a.num_m * a.num_n, h->num_sms), s));
+              launch_gemm(h, kind, ma, mb, mc, a, M, s));
   return read_back(h, ctrl, s, nullptr);
 }
 

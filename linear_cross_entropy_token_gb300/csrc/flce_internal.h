@@ -65,6 +65,11 @@ struct UmmaArgs {
 int umma_smem_bytes();
 cudaError_t launch_umma(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                         const UmmaArgs& args, int grid, cudaStream_t s);
+// CTA-pair kernels: 256 x 256 tiles; num_m counts 256-row tiles; B maps of
+// K-major operands use a 64 x 128 box (each CTA loads half of B)
+cudaError_t launch_umma_pair(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                             const UmmaArgs& args, int pairs, cudaStream_t s);
+int umma_pair_max_clusters();
 cudaError_t launch_wait_check(uint32_t* ctrl, uint64_t timeout_ns, cudaStream_t s);
 
 // flce_rows.cu

@@ -1,22 +1,28 @@
-// Persistent tcgen05 GEMM for sm_103a with the epilogues of fused linear
+// Persistent tcgen05 GEMMs for sm_103a with the epilogues of fused linear
 // cross-entropy.
 //
 // The three contractions of the FLCE pages' per-chunk schedule ("Fused Linear
 // Cross-Entropy: LLM 학습 logits 메모리 병목 없애기", section "FLCE의 핵심
-// 아이디어": projection x_c·Wᵀ, dx = dlogits·W, dW += dlogitsᵀ·x_c) all run on
-// this one kernel template:
+// 아이디어": projection x_c·Wᵀ, dx = dlogits·W, dW += dlogitsᵀ·x_c) run on two
+// kernel templates that share their epilogue:
 //
-//   warp 0      TMA producer: 64-deep k-blocks of A and B into a 4-stage ring
-//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
-//               (M=128, N=256, K=16, bf16 in, fp32 accumulate) into one of two
-//               256-column accumulators, so the epilogue of tile i overlaps
-//               the main loop of tile i+1
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (one token row per
-//               thread), transform, stage 16 KB sub-tiles in 128-byte-swizzled
-//               shared memory and write them out with TMA stores
+//   umma_gemm_kernel   one CTA per SM, 128 x 256 output tiles, 4-stage ring
+//                      of 48 KB (A 128x64, B 256x64), tcgen05 cta_group::1
+//   umma_pair_kernel   a cluster of two CTAs on two SMs computes a 256 x 256
+//                      tile with tcgen05 cta_group::2: each CTA holds its 128
+//                      rows of A and its 128 columns of B (6-stage ring of
+//                      32 KB), the even CTA issues the MMAs for both, and
+//                      each CTA's TMEM receives its 128 rows of the result
 //
-// The logits epilogue (kEpiLse) is the on-chip online softmax of the Unsloth
-// page ("Unsloth 심층 아키텍처 …", section "스트리밍 청크 기반 Fast
+// Warp roles (both kernels): warp 0 TMA producer; warp 1 allocates 512 TMEM
+// columns and (one thread) issues the MMAs into one of two 256-column
+// accumulators, so the epilogue of tile i overlaps the main loop of tile i+1;
+// warps 2..5 epilogue: tcgen05.ld the accumulator (one token row per thread),
+// transform, stage 16 KB sub-tiles in 128-byte-swizzled shared memory and
+// write them out with TMA stores.
+//
+// The logits epilogue (kEpiLse) is the on-chip softmax statistics of the
+// Unsloth page ("Unsloth 심층 아키텍처 …", section "스트리밍 청크 기반 Fast
 // CrossEntropy 손실 커널"): per token row and 256-wide vocab tile it takes
 // the max m and l = sum exp(z - m) from the fp32 accumulator (two passes over
 // TMEM), picks up the target logit, and optionally stores the tile as bf16
@@ -34,19 +40,25 @@
 namespace flce {
 namespace {
 
-constexpr int kStages = 4;
-constexpr uint32_t kABytes = kBM * kBK * 2;             // 16 KB
-constexpr uint32_t kBBytes = kBN * kBK * 2;             // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;      // 48 KB
-constexpr uint32_t kEpiBytes = 128 * 128;               // 128 rows x 128 bytes
-constexpr uint32_t kNumBars = 2 * kStages + 5;
+constexpr uint32_t kABytes = kBM * kBK * 2;                // 16 KB: 128 rows of A
+constexpr uint32_t kBBytes = kBN * kBK * 2;                // 32 KB: 256 columns of B
+constexpr uint32_t kBHalfBytes = kBBytes / 2;              // 16 KB: 128 columns of B
+constexpr int kStages = 4;                                 // single-CTA ring
+constexpr int kStagesPair = 6;                             // CTA-pair ring
+constexpr uint32_t kStageBytes = kABytes + kBBytes;        // 48 KB
+constexpr uint32_t kStageBytesPair = kABytes + kBHalfBytes;  // 32 KB per CTA
+constexpr uint32_t kEpiBytes = 128 * 128;                  // 128 rows x 128 bytes
 constexpr uint32_t kSmemBytes =
-    1024 + kStages * kStageBytes + 2 * kEpiBytes + kNumBars * 8 + 16;
+    1024 + kStages * kStageBytes + 2 * kEpiBytes + (2 * kStages + 5) * 8 + 16;
+constexpr uint32_t kSmemBytesPair =
+    1024 + kStagesPair * kStageBytesPair + 2 * kEpiBytes + (2 * kStagesPair + 5) * 8 + 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kEpiBar = 1;
 constexpr float kLog2e = 1.4426950408889634f;
+
+static_assert(kSmemBytes <= 232448 && kSmemBytesPair <= 232448, "shared memory per CTA");
 
 struct Unit {
   int m, n, s;
@@ -96,6 +108,156 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int r, const uint32_t (&
     rowp[j ^ (r & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
 }
 
+// The epilogue of one 128-row x 256-column accumulator tile. Runs on the 128
+// epilogue threads; thread `row` owns one tile row. `release` is called right
+// after the last tcgen05.ld of the tile, handing the accumulator back to the
+// MMA issuer.
+template <int EPI, class Release>
+__device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorMap* tmO, uint8_t* sE,
+                                              uint32_t& ebuf, int row, bool leader, int m0, int n0,
+                                              int n_tile, int s_idx, uint32_t tbase,
+                                              Release&& release) {
+  const int grow = m0 + row;
+  const bool rvalid = grow < a.rows;
+
+  // stage one 16 KB sub-tile and hand it to the TMA unit
+  auto stage_and_store = [&](const uint32_t (&w)[32], auto&& issue) {
+    uint8_t* buf = sE + ebuf * kEpiBytes;
+    if (leader) bulk_wait_group_read<1>();
+    named_bar_sync(kEpiBar, kEpiThreads);
+    stage_row(buf, row, w);
+    fence_proxy_async_smem();
+    named_bar_sync(kEpiBar, kEpiThreads);
+    if (leader) {
+      issue(smem_u32(buf));
+      bulk_commit_group();
+    }
+    __syncwarp();
+    ebuf ^= 1u;
+  };
+
+  if constexpr (EPI == kEpiLse || EPI == kEpiDlogits) {
+    int64_t tg = -1;
+    if (rvalid) tg = a.targets[grow];
+    const bool tvalid = rvalid && tg != a.ignore_index;
+    const int tcol = (tvalid && tg >= n0 && tg < n0 + kBN) ? static_cast<int>(tg - n0) : -1;
+    float tmax = -INFINITY, tsum = 0.f, zt = 0.f;
+    float scale = 0.f, lse_l2 = 0.f;
+    if constexpr (EPI == kEpiDlogits) {
+      const uint32_t nv = a.ctrl[kCtrlNValid];
+      scale = (tvalid && nv > 0) ? 1.0f / static_cast<float>(nv) : 0.f;
+      lse_l2 = rvalid ? a.lse[grow] * kLog2e : 0.f;
+    }
+    if constexpr (EPI == kEpiLse) {
+      // pass 1 over the accumulator: the tile's row max and the target logit
+#pragma unroll 1
+      for (int g = 0; g < kBN / 32; ++g) {
+        const int ncv = a.cols - (n0 + g * 32);
+        if (ncv <= 0) break;  // uniform across the epilogue threads
+        uint32_t r0[32];
+        tmem_ld_32x32b_x32(tbase + g * 32, r0);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < ncv) tmax = fmaxf(tmax, __uint_as_float(r0[i]));
+        if (tcol >= g * 32 && tcol < g * 32 + 32) {
+          const int k = tcol - g * 32;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i == k) zt = __uint_as_float(r0[i]);
+        }
+      }
+    }
+    // last 64-column group holding valid columns (uniform)
+    const int last_g = min(kBN / 64 - 1, (a.cols - n0 - 1) / 64);
+#pragma unroll 1
+    for (int g = 0; g <= last_g; ++g) {
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(tbase + g * 64, r0);
+      tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
+      tmem_ld_wait();
+      if (g == last_g) release();
+      const int c0 = n0 + g * 64;
+      const int ncv = a.cols - c0;  // valid columns in this group, >= 1 (uniform)
+      if constexpr (EPI == kEpiLse) {
+        // pass 2: sum of exp(z - tmax), and the logits stored shifted by the
+        // tile max, y = z - tmax, so that the largest entries are stored near
+        // 0 where bf16 is most precise
+        const float ml = tmax * kLog2e;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r0[i]), kLog2e, -ml));
+          if (i + 32 < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r1[i]), kLog2e, -ml));
+        }
+        if (a.store_logits) {
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]) - tmax, __uint_as_float(r0[2 * i + 1]) - tmax);
+            w[16 + i] =
+                pack_bf16x2(__uint_as_float(r1[2 * i]) - tmax, __uint_as_float(r1[2 * i + 1]) - tmax);
+          }
+          stage_and_store(w, [&](uint32_t src) { tma_store_2d(tmO, src, c0, m0); });
+        }
+      } else {
+        // softmax / n_valid = exp(z - lse) * scale, written over the logits
+        // buffer; the dx reduction adds the -onehot / n_valid term
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float v[4] = {__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]),
+                        __uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = ex2_approx(fmaf(v[q], kLog2e, -lse_l2)) * scale;
+          w[i] = pack_bf16x2(v[0], v[1]);
+          w[16 + i] = pack_bf16x2(v[2], v[3]);
+        }
+        stage_and_store(w, [&](uint32_t src) { tma_store_2d(tmO, src, c0, m0); });
+      }
+    }
+    if constexpr (EPI == kEpiLse) {
+      if (rvalid) {
+        a.partials[static_cast<size_t>(grow) * a.vocab_tiles + n_tile] = make_float2(tmax, tsum);
+        if (tcol >= 0) a.zt[grow] = zt;
+      }
+    }
+  } else if constexpr (EPI == kEpiBf16) {
+#pragma unroll 1
+    for (int g = 0; g < kBN / 64; ++g) {
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(tbase + g * 64, r0);
+      tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
+      tmem_ld_wait();
+      if (g == kBN / 64 - 1) release();
+      const int c0 = n0 + g * 64;
+      if (c0 >= a.cols) continue;
+      uint32_t w[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+        w[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+      }
+      stage_and_store(w, [&](uint32_t src) { tma_store_2d(tmO, src, c0, m0); });
+    }
+  } else {  // kEpiF32
+#pragma unroll 1
+    for (int g = 0; g < kBN / 32; ++g) {
+      uint32_t r0[32];
+      tmem_ld_32x32b_x32(tbase + g * 32, r0);
+      tmem_ld_wait();
+      if (g == kBN / 32 - 1) release();
+      const int c0 = n0 + g * 32;
+      if (c0 >= a.cols) continue;
+      if (a.reduce_add)
+        stage_and_store(r0, [&](uint32_t src) { tma_reduce_add_3d(tmO, src, c0, m0, s_idx); });
+      else
+        stage_and_store(r0, [&](uint32_t src) { tma_store_3d(tmO, src, c0, m0, s_idx); });
+    }
+  }
+}
+
+// ===================================================== single-CTA kernel
+
 template <int AMN, int BMN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -107,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + kStages * kABytes;
   uint8_t* sE = sB + kStages * kBBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -253,155 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_bar_or(kEpiBar, kEpiThreads, !ok)) break;
       tc_fence_after();
       const Unit t = unit_coords(a, u);
-      const int m0 = t.m * kBM;
-      const int n0 = t.n * kBN;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + acc * kBN;
-      const int grow = m0 + row;
-      const bool rvalid = grow < a.rows;
-
-      // stage one 16 KB sub-tile and hand it to the TMA unit
-      auto stage_and_store = [&](const uint32_t (&w)[32], auto&& issue) {
-        uint8_t* buf = sE + ebuf * kEpiBytes;
-        if (leader) bulk_wait_group_read<1>();
-        named_bar_sync(kEpiBar, kEpiThreads);
-        stage_row(buf, row, w);
-        fence_proxy_async_smem();
-        named_bar_sync(kEpiBar, kEpiThreads);
-        if (leader) {
-          issue(smem_u32(buf));
-          bulk_commit_group();
-        }
-        __syncwarp();
-        ebuf ^= 1u;
-      };
-
-      if constexpr (EPI == kEpiLse || EPI == kEpiDlogits) {
-        int64_t tg = -1;
-        if (rvalid) tg = a.targets[grow];
-        const bool tvalid = rvalid && tg != a.ignore_index;
-        const int tcol = (tvalid && tg >= n0 && tg < n0 + kBN) ? static_cast<int>(tg - n0) : -1;
-        float tmax = -INFINITY, tsum = 0.f, zt = 0.f;
-        float scale = 0.f, lse_l2 = 0.f;
-        if constexpr (EPI == kEpiDlogits) {
-          const uint32_t nv = a.ctrl[kCtrlNValid];
-          scale = (tvalid && nv > 0) ? 1.0f / static_cast<float>(nv) : 0.f;
-          lse_l2 = rvalid ? a.lse[grow] * kLog2e : 0.f;
-        }
-        if constexpr (EPI == kEpiLse) {
-          // pass 1 over the accumulator: the tile's row max and the target logit
-#pragma unroll 1
-          for (int g = 0; g < kBN / 32; ++g) {
-            const int ncv = a.cols - (n0 + g * 32);
-            if (ncv <= 0) break;  // uniform across the epilogue threads
-            uint32_t r0[32];
-            tmem_ld_32x32b_x32(tbase + g * 32, r0);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < ncv) tmax = fmaxf(tmax, __uint_as_float(r0[i]));
-            if (tcol >= g * 32 && tcol < g * 32 + 32) {
-              const int k = tcol - g * 32;
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i == k) zt = __uint_as_float(r0[i]);
-            }
-          }
-        }
-        // last 64-column group holding valid columns (uniform)
-        const int last_g = min(kBN / 64 - 1, (a.cols - n0 - 1) / 64);
-#pragma unroll 1
-        for (int g = 0; g <= last_g; ++g) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(tbase + g * 64, r0);
-          tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
-          tmem_ld_wait();
-          if (g == last_g) {
-            tc_fence_before();
-            mbar_arrive(tempty_bar(acc));
-          }
-          const int c0 = n0 + g * 64;
-          const int ncv = a.cols - c0;  // valid columns in this group, >= 1 (uniform)
-          if constexpr (EPI == kEpiLse) {
-            // pass 2: sum of exp(z - tmax), and the logits stored shifted by
-            // the tile max, y = z - tmax, so that the largest entries are
-            // stored near 0 where bf16 is most precise
-            const float ml = tmax * kLog2e;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (i < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r0[i]), kLog2e, -ml));
-              if (i + 32 < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r1[i]), kLog2e, -ml));
-            }
-            if (a.store_logits) {
-              uint32_t w[32];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]) - tmax, __uint_as_float(r0[2 * i + 1]) - tmax);
-                w[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]) - tmax,
-                                        __uint_as_float(r1[2 * i + 1]) - tmax);
-              }
-              stage_and_store(w, [&](uint32_t src) { tma_store_2d(&tmO, src, c0, m0); });
-            }
-          } else {
-            // softmax / n_valid = exp(z - lse) * scale, written over the logits
-            // buffer; the dx reduction adds the -onehot / n_valid term
-            uint32_t w[32];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float v[4] = {__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]),
-                            __uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])};
-#pragma unroll
-              for (int q = 0; q < 4; ++q) v[q] = ex2_approx(fmaf(v[q], kLog2e, -lse_l2)) * scale;
-              w[i] = pack_bf16x2(v[0], v[1]);
-              w[16 + i] = pack_bf16x2(v[2], v[3]);
-            }
-            stage_and_store(w, [&](uint32_t src) { tma_store_2d(&tmO, src, c0, m0); });
-          }
-        }
-        if constexpr (EPI == kEpiLse) {
-          if (rvalid) {
-            a.partials[static_cast<size_t>(grow) * a.vocab_tiles + t.n] = make_float2(tmax, tsum);
-            if (tcol >= 0) a.zt[grow] = zt;
-          }
-        }
-      } else if constexpr (EPI == kEpiBf16) {
-#pragma unroll 1
-        for (int g = 0; g < kBN / 64; ++g) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_32x32b_x32(tbase + g * 64, r0);
-          tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
-          tmem_ld_wait();
-          if (g == kBN / 64 - 1) {
-            tc_fence_before();
-            mbar_arrive(tempty_bar(acc));
-          }
-          const int c0 = n0 + g * 64;
-          if (c0 >= a.cols) continue;
-          uint32_t w[32];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
-            w[16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
-          }
-          stage_and_store(w, [&](uint32_t src) { tma_store_2d(&tmO, src, c0, m0); });
-        }
-      } else {  // kEpiF32
-#pragma unroll 1
-        for (int g = 0; g < kBN / 32; ++g) {
-          uint32_t r0[32];
-          tmem_ld_32x32b_x32(tbase + g * 32, r0);
-          tmem_ld_wait();
-          if (g == kBN / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(tempty_bar(acc));
-          }
-          const int c0 = n0 + g * 32;
-          if (c0 >= a.cols) continue;
-          if (a.reduce_add)
-            stage_and_store(r0, [&](uint32_t src) { tma_reduce_add_3d(&tmO, src, c0, m0, t.s); });
-          else
-            stage_and_store(r0, [&](uint32_t src) { tma_store_3d(&tmO, src, c0, m0, t.s); });
-        }
-      }
+      epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, t.m * kBM, t.n * kBN, t.n, t.s, tbase, [&] {
+        tc_fence_before();
+        mbar_arrive(tempty_bar(acc));
+      });
     }
     if (leader) bulk_wait_group<0>();
   }
@@ -411,6 +429,190 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ======================================================= CTA-pair kernel
+
+template <int AMN, int BMN, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    umma_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmO, const UmmaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStagesPair * kABytes;
+  uint8_t* sE = sB + kStagesPair * kBHalfBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesPair + 5);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStagesPair + s); };
+  auto tfull_bar = [&](int acc) { return bar0 + 8u * (2 * kStagesPair + acc); };
+  auto tempty_bar = [&](int acc) { return bar0 + 8u * (2 * kStagesPair + 2 + acc); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStagesPair + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0: the CTA that issues the MMAs
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(num_clusters_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesPair; ++s) {
+      mbar_init(full_bar(s), 1);     // used in CTA 0 only: both CTAs' loads land here
+      mbar_init(empty_bar(s), 1);    // each CTA's own, released by the pair's MMA commit
+    }
+    for (int acc = 0; acc < 2; ++acc) {
+      mbar_init(tfull_bar(acc), 1);
+      mbar_init(tempty_bar(acc), 2 * kEpiThreads);  // used in CTA 0: both epilogues arrive
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+    tma_prefetch_map(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_units = a.num_m * a.num_n * a.num_s;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      uint32_t n_issued = 0;
+      bool failed = false;
+      for (int u = pair; u < num_units && !failed; u += npairs) {
+        const Unit t = unit_coords(a, u);
+        const int kb0 = t.s * a.kb_per_split;
+        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+        const int mA = t.m * 2 * kBM + static_cast<int>(rank) * kBM;   // this CTA's rows of A
+        const int nB = t.n * kBN + static_cast<int>(rank) * (kBN / 2);  // this CTA's columns of B
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int stage = n_issued % kStagesPair;
+          const uint32_t phase = (n_issued / kStagesPair) & 1u;
+          if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, a.ctrl, a.timeout_ns)) {
+            failed = true;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytesPair);
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          const uint32_t sa = smem_u32(sA + stage * kABytes);
+          const uint32_t sb = smem_u32(sB + stage * kBHalfBytes);
+          const int k0 = kb * kBK;
+          if (AMN == 0) {
+            tma_load_2d_pair(sa, &tmA, fb, k0, mA);
+          } else {
+            tma_load_2d_pair(sa, &tmA, fb, mA, k0);
+            tma_load_2d_pair(sa + 8192, &tmA, fb, mA + 64, k0);
+          }
+          if (BMN == 0) {
+            tma_load_2d_pair(sb, &tmB, fb, k0, nB);
+          } else {
+            tma_load_2d_pair(sb, &tmB, fb, nB, k0);
+            tma_load_2d_pair(sb + 8192, &tmB, fb, nB + 64, k0);
+          }
+          ++n_issued;
+        }
+      }
+      if (failed && rank == 0) {
+        const uint32_t first = n_issued > kStagesPair ? n_issued - kStagesPair : 0;
+        for (uint32_t i = first; i < n_issued; ++i)
+          mbar_drain_wait(full_bar(i % kStagesPair), (i / kStagesPair) & 1u, a.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------- MMA issuer (CTA 0 of the pair)
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, AMN, BMN);
+      uint32_t n_consumed = 0;
+      bool issued = false, failed = false;
+      int it = 0;
+      for (int u = pair; u < num_units && !failed; u += npairs, ++it) {
+        const Unit t = unit_coords(a, u);
+        const int kb0 = t.s * a.kb_per_split;
+        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait_bounded_cluster(tempty_bar(acc), acc_phase ^ 1u, a.ctrl, a.timeout_ns)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int stage = n_consumed % kStagesPair;
+          const uint32_t phase = (n_consumed / kStagesPair) & 1u;
+          if (!mbar_wait_bounded_cluster(full_bar(stage), phase, a.ctrl, a.timeout_ns)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(sA + stage * kABytes);
+          const uint32_t sb = smem_u32(sB + stage * kBHalfBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = AMN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                    : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+            const uint64_t bd = BMN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
+                                    : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
+            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit_pair_multicast(empty_bar(stage), 0x3);
+          ++n_consumed;
+        }
+        if (failed) break;
+        tc_commit_pair_multicast(tfull_bar(acc), 0x3);
+      }
+      if (failed && issued) {
+        tc_commit_pair(drain_bar);
+        mbar_drain_wait(drain_bar, 0, a.timeout_ns);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const bool leader = threadIdx.x == 64;
+    uint32_t ebuf = 0;
+    int it = 0;
+    for (int u = pair; u < num_units; u += npairs, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      const bool ok = mbar_wait_bounded_cluster(tfull_bar(acc), acc_phase, a.ctrl, a.timeout_ns);
+      if (named_bar_or(kEpiBar, kEpiThreads, !ok)) break;
+      tc_fence_after();
+      const Unit t = unit_coords(a, u);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + acc * kBN;
+      const int m0 = t.m * 2 * kBM + static_cast<int>(rank) * kBM;
+      epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, m0, t.n * kBN, t.n, t.s, tbase, [&] {
+        tc_fence_before();
+        if (rank == 0)
+          mbar_arrive(tempty_bar(acc));
+        else
+          mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+      });
+    }
+    if (leader) bulk_wait_group<0>();
+  }
+
+  __syncwarp();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair's MMAs may touch its memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -441,14 +643,24 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
   return cudaGetLastError();
 }
 
+// grid = 2 x pairs (a multiple of the cluster size)
+template <int AMN, int BMN, int EPI>
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+                        const UmmaArgs& args, int pairs, cudaStream_t s) {
+  auto kern = umma_pair_kernel<AMN, BMN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytesPair));
+  if (e != cudaSuccess) return e;
+  kern<<<2 * pairs, kThreads, kSmemBytesPair, s>>>(ta, tb, to, args);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-int umma_smem_bytes() { return static_cast<int>(kSmemBytes); }
+int umma_smem_bytes() { return static_cast<int>(kSmemBytes > kSmemBytesPair ? kSmemBytes : kSmemBytesPair); }
 
 cudaError_t launch_umma(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                         const UmmaArgs& args, int grid, cudaStream_t s) {
-  // the epilogue's error word lives at ctrl[kCtrlError]; the kernels read
-  // and write it through args.ctrl
   switch (kind) {
     case kUmmaLogits: return launch_one<0, 0, kEpiLse>(a, b, o, args, grid, s);
     case kUmmaDlogits: return launch_one<0, 0, kEpiDlogits>(a, b, o, args, grid, s);
@@ -459,6 +671,46 @@ cudaError_t launch_umma(int kind, const CUtensorMap& a, const CUtensorMap& b, co
     case kUmmaCheckMK: return launch_one<1, 0, kEpiF32>(a, b, o, args, grid, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_umma_pair(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                             const UmmaArgs& args, int pairs, cudaStream_t s) {
+  switch (kind) {
+    case kUmmaLogits: return launch_pair<0, 0, kEpiLse>(a, b, o, args, pairs, s);
+    case kUmmaDlogits: return launch_pair<0, 0, kEpiDlogits>(a, b, o, args, pairs, s);
+    case kUmmaDxF32: return launch_pair<0, 1, kEpiF32>(a, b, o, args, pairs, s);
+    case kUmmaDw: return launch_pair<1, 1, kEpiF32>(a, b, o, args, pairs, s);
+    case kUmmaCheckKK: return launch_pair<0, 0, kEpiF32>(a, b, o, args, pairs, s);
+    case kUmmaCheckMK: return launch_pair<1, 0, kEpiF32>(a, b, o, args, pairs, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Clusters of two that fit on the device at once for the pair kernels
+int umma_pair_max_clusters() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytesPair;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  auto kern = umma_pair_kernel<1, 1, kEpiF32>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytesPair)) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 cudaError_t launch_wait_check(uint32_t* ctrl, uint64_t timeout_ns, cudaStream_t s) {

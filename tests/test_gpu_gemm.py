@@ -1,5 +1,6 @@
-"""The tcgen05 GEMM core alone, for each operand majorness, against the float64
-product of the same bf16 operands; and the bounded device wait."""
+"""The tcgen05 GEMM core alone, for each operand majorness and both tile
+shapes (one CTA per 128 x 256 tile; a CTA pair per 256 x 256 tile), against
+the float64 product of the same bf16 operands; and the bounded device wait."""
 import numpy as np
 import pytest
 import torch
@@ -7,15 +8,16 @@ import torch
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def handle():
+@pytest.fixture(scope="module", params=["single", "pair"])
+def handle(request):
     from linear_cross_entropy_token_gb300 import FLCE
-    h = FLCE("bf16", 0)
+    h = FLCE("bf16", 0, cta=request.param)
     yield h
     h.close()
 
 
-SHAPES = [(128, 256, 64), (256, 512, 192), (200, 296, 136), (384, 768, 1024), (64, 40, 8)]
+SHAPES = [(128, 256, 64), (256, 512, 192), (200, 296, 136), (384, 768, 1024), (64, 40, 8),
+          (520, 264, 320)]
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)],
@@ -31,13 +33,13 @@ def test_gemm_core(handle, a_mn, b_mn, M, N, K):
     C = handle.check_gemm(Ad, Bd, bool(a_mn), bool(b_mn), M, N, K).double().cpu().numpy()
     err = np.linalg.norm(C - ref) / np.linalg.norm(ref)
     if err > 1e-5:
-        # diagnostics for a layout mistake: compare against likely confusions
-        alt = {"transposed_ref": np.linalg.norm(C - (A.double() @ B.double().T).numpy().T[:M, :N])
-               if M == N else None,
-               "frac_close": float(np.mean(np.isclose(C, ref, rtol=1e-3, atol=1e-2))),
-               "C[0,:4]": C[0, :4].tolist(), "ref[0,:4]": ref[0, :4].tolist(),
-               "C[1,:4]": C[1, :4].tolist(), "ref[1,:4]": ref[1, :4].tolist()}
-        pytest.fail(f"relative error {err:.3e}; {alt}")
+        # where the product is wrong tells a layout mistake apart
+        bad = ~np.isclose(C, ref, rtol=1e-3, atol=1e-2)
+        rows = np.flatnonzero(bad.any(axis=1))
+        cols = np.flatnonzero(bad.any(axis=0))
+        pytest.fail(f"relative error {err:.3e}; wrong rows {rows[:8]}..{rows[-4:]} "
+                    f"({len(rows)}), wrong cols {cols[:8]}..{cols[-4:]} ({len(cols)}); "
+                    f"C[0,:4]={C[0, :4]}, ref[0,:4]={ref[0, :4]}")
 
 
 def test_bounded_wait_reports_timeout(handle):

@@ -62,6 +62,37 @@ def test_small_bf16_config_recompute(bf16_recompute):
     assert_parity(res, _oracle(w), "bf16", token_rtol=1e-3)
 
 
+@pytest.fixture(scope="module", params=["inplace", "recompute"])
+def bf16_pair(request):
+    from linear_cross_entropy_token_gb300 import FLCE
+    h = FLCE("bf16", 0, hbm_budget_bytes=4 << 30, dlogits_mode=request.param, cta="pair")
+    yield h
+    h.close()
+
+
+@pytest.mark.parametrize("N,H,V,chunk,ign", [
+    (2048, 1024, 32000, 0, 0.1),     # the small bf16 config's shape
+    (1000, 256, 4099, 300, 0.1),     # odd V, N % C != 0, C % 256 != 0
+    (256, 128, 4096, 64, 0.0),       # C < 128: the pair's second CTA holds no rows
+    (777, 136, 1000, 384, 0.2),      # K tail, ragged 256-row pair tiles
+    (1536, 256, 8192, 512, 0.05),
+])
+def test_cta_pair_tiles(bf16_pair, N, H, V, chunk, ign):
+    """The same parity on 256 x 256 tiles computed by CTA pairs."""
+    w = workloads.generate(workloads.custom(N, H, V, "bf16", ignore_frac=ign, seed=N + 3 * V))
+    assert_parity(run(bf16_pair, w, chunk=chunk), _oracle(w), "bf16", token_rtol=1e-3)
+
+
+def test_cta_pair_matches_single(bf16, bf16_pair):
+    """Both tile shapes accumulate each output in the same k order: results
+    agree to rounding of the fp32 accumulation order within a k-block."""
+    w = workloads.generate(workloads.custom(1024, 512, 6000, "bf16", ignore_frac=0.1, seed=31))
+    a = run(bf16, w, chunk=512)
+    b = run(bf16_pair, w, chunk=512)
+    assert abs(a["loss"] - b["loss"]) <= 1e-5 * abs(a["loss"])
+    assert rel_fro(b["dW"], a["dW"]) <= 1e-2 and rel_fro(b["dx"], a["dx"]) <= 1e-2
+
+
 @pytest.mark.parametrize("N,H,V,chunk,ign", [
     (1000, 256, 4099, 300, 0.1),     # odd V: last vocab tile holds 3 columns; N % C != 0, C % 128 != 0
     (512, 512, 50257, 0, 0.05),      # GPT-2-sized vocabulary
