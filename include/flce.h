@@ -100,6 +100,7 @@ typedef struct flce_plan {
     int64_t dx_splits;           /* split of the V reduction of the dx GEMM            */
     uint64_t workspace_bytes;    /* device bytes one call needs                        */
     uint64_t logits_bytes;       /* of which the C x ldv logits / dlogits buffer       */
+    int64_t tile_m;              /* rows of a GEMM output tile: 128 (one CTA) or 256 (CTA pair) */
 } flce_plan;
 
 /* Kernel kinds, for the per-kernel timing of flce_profile_read(). */

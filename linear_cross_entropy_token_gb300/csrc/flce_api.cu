@@ -188,6 +188,7 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   out->workspace_bytes =
       make_layout(N, H, C, out->ldv, out->vocab_tiles, C ? splits_for(C) : 0, esize).total;
   out->logits_bytes = static_cast<uint64_t>(C) * out->ldv * esize;
+  out->tile_m = pair ? 2 * kBM : kBM;
   return FLCE_OK;
 }
 
@@ -635,6 +636,8 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
       return FLCE_ERR_UNSUPPORTED;
     }
     h->use_pair = wants_pair(cfg) && h->pair_clusters > 0;
+    // the handle's plans follow the tile shape it actually runs
+    h->cfg.cta_pair = h->use_pair ? FLCE_CTA_PAIR : FLCE_CTA_SINGLE;
   }
   if (cudaMallocHost(&h->host_ctrl, kCtrlWords * 4) != cudaSuccess) {
     cudaGetLastError();

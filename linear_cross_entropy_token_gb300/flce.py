@@ -45,7 +45,7 @@ class Plan(ctypes.Structure):
     _fields_ = [("chunk", ctypes.c_int64), ("num_chunks", ctypes.c_int64),
                 ("vocab_tiles", ctypes.c_int64), ("ldv", ctypes.c_int64),
                 ("dx_splits", ctypes.c_int64), ("workspace_bytes", ctypes.c_uint64),
-                ("logits_bytes", ctypes.c_uint64)]
+                ("logits_bytes", ctypes.c_uint64), ("tile_m", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
