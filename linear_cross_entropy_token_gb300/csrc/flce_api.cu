@@ -96,7 +96,7 @@ Layout make_layout(int64_t N, int64_t H, int64_t C, int64_t ldv, int64_t vt, int
 }
 
 // CTA pairs are the default tile shape (FLCE_CTA_AUTO)
-constexpr bool kAutoPair = false;
+constexpr bool kAutoPair = true;
 
 bool wants_pair(const flce_config* cfg) {
   return cfg->dtype == FLCE_DTYPE_BF16 &&
