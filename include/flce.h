@@ -117,7 +117,8 @@ enum {
     FLCE_K_LOSS_FINALIZE = 8,    /* fixed-order sum of token losses / n_valid          */
     FLCE_K_SIMT_GEMM = 9,        /* fp32 path: CUDA-core GEMMs                         */
     FLCE_K_SIMT_TILE_STATS = 10, /* fp32 path: per-vocab-tile max/sum-exp              */
-    FLCE_K_NUM_KINDS = 11
+    FLCE_K_GEMM_DX_DW = 11,      /* CTA pairs: the dx and dW GEMMs of a chunk in one launch */
+    FLCE_K_NUM_KINDS = 12
 };
 
 typedef struct flce_kernel_profile {

@@ -71,7 +71,8 @@ struct Profiler {
 // ------------------------------------------------------------- workspace
 
 struct Layout {
-  uint64_t ctrl = 0, logits = 0, partials = 0, zt = 0, lse = 0, token_loss = 0, dxpart = 0;
+  uint64_t ctrl = 0, logits = 0, partials = 0, zt = 0, lse = 0, dcorr = 0, token_loss = 0,
+           dxpart = 0;
   uint64_t total = 0;
 };
 
@@ -89,6 +90,7 @@ Layout make_layout(int64_t N, int64_t H, int64_t C, int64_t ldv, int64_t vt, int
   L.partials = take(static_cast<uint64_t>(C) * vt * 8);
   L.zt = take(static_cast<uint64_t>(C) * 4);
   L.lse = take(static_cast<uint64_t>(C) * 4);
+  L.dcorr = take(static_cast<uint64_t>(C) * 4);
   L.token_loss = take(static_cast<uint64_t>(std::max<int64_t>(N, 1)) * 4);
   L.dxpart = take(static_cast<uint64_t>(splits) * C * H * 4);  // bf16 path: fp32 dx partials
   L.total = off;
@@ -421,6 +423,7 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
   float2* partials = reinterpret_cast<float2*>(ws + L.partials);
   float* zt = reinterpret_cast<float*>(ws + L.zt);
   float* lse = reinterpret_cast<float*>(ws + L.lse);
+  float* dcorr = reinterpret_cast<float*>(ws + L.dcorr);
   float* token_loss = reinterpret_cast<float*>(ws + L.token_loss);
   h->last_plan = p;
   h->last_N = N;
@@ -506,6 +509,7 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       a.partials = partials;
       a.zt = zt;
       a.lse = lse;
+      a.dcorr = dcorr;
       a.ctrl = ctrl;
       a.timeout_ns = h->timeout_ns;
       FLCE_LAUNCH(FLCE_K_GEMM_LOGITS, 2 * dr * dH * dV,
@@ -521,7 +525,7 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       } else {
         FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 4 * dr * dV,
                     launch_dlogits_bf16(logits, ldv, rows, V, partials, vt, lse, t + off, ignore_index,
-                                        ctrl, s));
+                                        ctrl, dcorr, s));
       }
       // 3. dx_chunk = dlogits · W
       const int S_req = static_cast<int>(p.dx_splits);
@@ -536,16 +540,11 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       b.rows = rows;
       b.cols = static_cast<int>(H);
       b.reduce_add = 0;
-      // fp32 partials of softmax·W / n_valid per split; the reduction subtracts
-      // W[t_i] / n_valid in fp32, rounds dx to bf16 once, and completes the
-      // dlogits rows (-1 / n_valid at the target) for the dW GEMM
+      // fp32 partials of dlogits·W per split; the reduction adds them in split
+      // order, adds dcorr·W[t_i] (the target entry's bf16 rounding error) and
+      // rounds dx to bf16 once
       if (!map_f32_3d(&mDx, dxpart, H, rows, S, H * 4, static_cast<uint64_t>(C) * H * 4, &why))
         return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
-      FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH,
-                  launch_gemm(h, kUmmaDxF32, mZ_k, mW_mn, mDx, b, rows, s));
-      FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4.0 * S * dr * dH + 4 * dr * dH,
-                  launch_dx_reduce(dxpart, S, C * H, rows, H, static_cast<const __nv_bfloat16*>(W), V,
-                                   t + off, ignore_index, ctrl, logits, ldv, dxb + off * H, s));
       // 4. dW (+)= dlogitsᵀ · x_chunk, fp32 (stored on the first chunk, added after)
       UmmaArgs d = a;
       d.num_n = static_cast<int>(cdiv(H, kBN));
@@ -556,9 +555,36 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       d.rows = static_cast<int>(V);
       d.cols = static_cast<int>(H);
       d.reduce_add = c > 0 ? 1 : 0;
-      FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dV * dH,
-                  2 * dr * dV + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dV * dH,
-                  launch_gemm(h, kUmmaDw, mZ_mn, mX_mn, mDw, d, V, s));
+      const double dx_bytes = 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH;
+      const double dw_bytes = 2 * dr * dV + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dV * dH;
+      if (h->use_pair) {
+        // both read the finished dlogits buffer: one launch, dx units first
+        DualMaps maps;
+        maps.a[0] = mZ_k;
+        maps.b[0] = mW_mn;
+        maps.o[0] = mDx;
+        maps.a[1] = mZ_mn;
+        maps.b[1] = mX_mn;
+        maps.o[1] = mDw;
+        DualArgs da;
+        da.p[0] = b;
+        da.p[1] = d;
+        da.p[0].num_m = static_cast<int>(cdiv(rows, 2 * kBM));
+        da.p[1].num_m = static_cast<int>(cdiv(V, 2 * kBM));
+        da.units0 = da.p[0].num_m * da.p[0].num_n * da.p[0].num_s;
+        da.pad = 0;
+        const int units = da.units0 + da.p[1].num_m * da.p[1].num_n;
+        FLCE_LAUNCH(FLCE_K_GEMM_DX_DW, 4 * dr * dV * dH, dx_bytes + dw_bytes,
+                    launch_umma_pair_dual(maps, da, std::min(units, h->pair_clusters), s));
+      } else {
+        FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, dx_bytes,
+                    launch_gemm(h, kUmmaDxF32, mZ_k, mW_mn, mDx, b, rows, s));
+        FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dV * dH, dw_bytes,
+                    launch_gemm(h, kUmmaDw, mZ_mn, mX_mn, mDw, d, V, s));
+      }
+      FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4.0 * S * dr * dH + 4 * dr * dH,
+                  launch_dx_reduce(dxpart, S, C * H, rows, H, static_cast<const __nv_bfloat16*>(W), V,
+                                   t + off, ignore_index, ctrl, dcorr, dxb + off * H, s));
     }
   }
   FLCE_LAUNCH(FLCE_K_LOSS_FINALIZE, 0.0, 4.0 * N, launch_loss_finalize(token_loss, N, ctrl, s));
@@ -599,6 +625,7 @@ const char* flce_kernel_name(int32_t kind) {
     case FLCE_K_LOSS_FINALIZE: return "loss_finalize";
     case FLCE_K_SIMT_GEMM: return "simt_gemm_f32";
     case FLCE_K_SIMT_TILE_STATS: return "simt_tile_stats_f32";
+    case FLCE_K_GEMM_DX_DW: return "gemm_dx_dw";
     default: return "?";
   }
 }

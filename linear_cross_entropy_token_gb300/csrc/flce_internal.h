@@ -57,6 +57,7 @@ struct UmmaArgs {
   float2* partials;              // [rows][vocab_tiles] (running max, sum of exp)
   float* zt;                     // [rows] fp32 target logit
   const float* lse;              // [rows] log-sum-exp (kEpiDlogits)
+  float* dcorr;                  // [rows] rounding error of the target entry (kEpiDlogits)
   uint32_t* ctrl;                // control block
   uint64_t timeout_ns;           // limit of every mbarrier wait
 };
@@ -70,6 +71,20 @@ cudaError_t launch_umma(int kind, const CUtensorMap& a, const CUtensorMap& b, co
 cudaError_t launch_umma_pair(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                              const UmmaArgs& args, int pairs, cudaStream_t s);
 int umma_pair_max_clusters();
+
+// The dx and dW GEMMs of one chunk in one CTA-pair launch: problem 0 = dx
+// (A K-major), problem 1 = dW (A MN-major); B MN-major, fp32 epilogue in both.
+// The dx units come first in the schedule.
+struct DualMaps {
+  CUtensorMap a[2], b[2], o[2];
+};
+struct DualArgs {
+  UmmaArgs p[2];
+  int32_t units0;  // work units of problem 0
+  int32_t pad;
+};
+cudaError_t launch_umma_pair_dual(const DualMaps& maps, const DualArgs& args, int pairs,
+                                  cudaStream_t s);
 cudaError_t launch_wait_check(uint32_t* ctrl, uint64_t timeout_ns, cudaStream_t s);
 
 // flce_rows.cu
@@ -81,14 +96,14 @@ cudaError_t launch_lse_combine(const float2* partials, int vocab_tiles, const fl
 cudaError_t launch_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int rows, int64_t V,
                                 const float2* partials, int vocab_tiles, const float* lse,
                                 const int64_t* t_chunk, int64_t ignore_index,
-                                const uint32_t* ctrl, cudaStream_t s);
+                                const uint32_t* ctrl, float* dcorr, cudaStream_t s);
 cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, const float* lse,
                                const int64_t* t_chunk, int64_t ignore_index,
                                const uint32_t* ctrl, cudaStream_t s);
 cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_stride, int rows,
                              int64_t H, const __nv_bfloat16* W, int64_t V, const int64_t* t_chunk,
-                             int64_t ignore_index, const uint32_t* ctrl, __nv_bfloat16* buf,
-                             int64_t ldv, __nv_bfloat16* dx, cudaStream_t s);
+                             int64_t ignore_index, const uint32_t* ctrl, const float* dcorr,
+                             __nv_bfloat16* dx, cudaStream_t s);
 cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* ctrl,
                                  cudaStream_t s);
 

@@ -83,44 +83,62 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partials, int voca
   }
 }
 
-// dlogits in place over a bf16 chunk buffer: 8 columns (16 bytes) per
-// thread; blockIdx.y = token row. The buffer holds y = z - m_s, the logits
-// shifted by their vocab tile's max m_s (partials[.].x), so
-// softmax = exp(y + m_s - lse). This pass writes softmax / n_valid; the
-// -onehot / n_valid term is added by the dx reduction (exactly, in fp32, as
-// -W[t_i] / n_valid for dx, and into the buffer before the dW GEMM), because a
-// bf16 (softmax - 1) / n_valid at the target column carries a 2^-9 relative
-// error that dx = dlogits·W would multiply by the common part of W's rows.
-// Ignored rows and padding columns get 0.
-__global__ void dlogits_bf16_kernel(__nv_bfloat16* __restrict__ buf, int64_t ldv, int64_t V,
-                                    const float2* __restrict__ partials, int vocab_tiles,
-                                    const float* __restrict__ lse, const int64_t* __restrict__ t,
-                                    int64_t ignore_index, const uint32_t* __restrict__ ctrl) {
+// dlogits in place over a bf16 chunk buffer: d = (softmax - onehot) / n_valid.
+// The buffer holds y = z - m_s, the logits shifted by their vocab tile's max
+// m_s (partials[.].x), so softmax = exp(y + m_s - lse). One block covers 8192
+// columns of one token row (blockIdx.y); each thread loads its four 16-byte
+// vectors before computing, to keep more bytes in flight.
+//
+// The target column's entry, about -1/n_valid, is stored in bf16 with a 2^-9
+// relative error; dx = dlogits·W would multiply that error by the part of W
+// common to all rows. Its exact fp32 rounding error goes to dcorr[row] so the
+// dx reduction can add dcorr·W[t] back. Ignored rows and padding columns get 0.
+constexpr int kDlogitsVecs = 4;
+
+__global__ void __launch_bounds__(256) dlogits_bf16_kernel(
+    __nv_bfloat16* __restrict__ buf, int64_t ldv, int64_t V, const float2* __restrict__ partials,
+    int vocab_tiles, const float* __restrict__ lse, const int64_t* __restrict__ t,
+    int64_t ignore_index, const uint32_t* __restrict__ ctrl, float* __restrict__ dcorr) {
   const int r = blockIdx.y;
-  const int64_t c0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
-  if (c0 >= ldv) return;
   const int64_t tg = t[r];
   const uint32_t nv = ctrl[kCtrlNValid];
   const bool valid = tg != ignore_index;
   const float scale = (valid && nv > 0) ? 1.0f / static_cast<float>(nv) : 0.f;
-  const int tile = static_cast<int>(c0 / kVocabTile);  // 8 columns never straddle a tile
-  const float ll = (lse[r] - partials[static_cast<size_t>(r) * vocab_tiles + tile].x) * kLog2e;
-  uint4* ptr = reinterpret_cast<uint4*>(buf + static_cast<size_t>(r) * ldv + c0);
-  uint4 v = *ptr;
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const float l = lse[r];
+  const float2* prow = partials + static_cast<size_t>(r) * vocab_tiles;
+  __nv_bfloat16* row = buf + static_cast<size_t>(r) * ldv;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * (blockDim.x * 8 * kDlogitsVecs);
+  uint4 v[kDlogitsVecs];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w[q]);
-    float2 f = __bfloat1622float2(h);
-    const int64_t j0 = c0 + 2 * q;
-    float d0 = ex2_approx(fmaf(f.x, kLog2e, -ll));
-    float d1 = ex2_approx(fmaf(f.y, kLog2e, -ll));
-    d0 = (j0 < V) ? d0 * scale : 0.f;
-    d1 = (j0 + 1 < V) ? d1 * scale : 0.f;
-    h = __floats2bfloat162_rn(d0, d1);
-    w[q] = *reinterpret_cast<uint32_t*>(&h);
+  for (int i = 0; i < kDlogitsVecs; ++i) {
+    const int64_t c0 = base + (static_cast<int64_t>(i) * blockDim.x + threadIdx.x) * 8;
+    if (c0 < ldv) v[i] = *reinterpret_cast<const uint4*>(row + c0);
   }
-  *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+  for (int i = 0; i < kDlogitsVecs; ++i) {
+    const int64_t c0 = base + (static_cast<int64_t>(i) * blockDim.x + threadIdx.x) * 8;
+    if (c0 >= ldv) continue;
+    // 8 columns never straddle a vocab tile
+    const float ll = (l - prow[c0 / kVocabTile].x) * kLog2e;
+    uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w[q]);
+      const float2 f = __bfloat1622float2(h);
+      const int64_t j0 = c0 + 2 * q;
+      float d0 = ex2_approx(fmaf(f.x, kLog2e, -ll));
+      float d1 = ex2_approx(fmaf(f.y, kLog2e, -ll));
+      if (j0 == tg) d0 -= 1.f;
+      if (j0 + 1 == tg) d1 -= 1.f;
+      d0 = (j0 < V) ? d0 * scale : 0.f;
+      d1 = (j0 + 1 < V) ? d1 * scale : 0.f;
+      h = __floats2bfloat162_rn(d0, d1);
+      if (j0 == tg) dcorr[r] = d0 - __low2float(h);
+      if (j0 + 1 == tg) dcorr[r] = d1 - __high2float(h);
+      w[q] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(row + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 // fp32 version: 4 columns per thread
@@ -148,51 +166,46 @@ __global__ void dlogits_f32_kernel(float* __restrict__ buf, int64_t ldv, int64_t
   *ptr = make_float4(f[0], f[1], f[2], f[3]);
 }
 
-// dx row i = (sum over splits of the fp32 partials of softmax·W / n_valid,
-// in split order) - W[t_i] / n_valid, rounded once to bf16. blockIdx.y =
-// token row, 4 columns per thread. Thread 0 of the row's first block then
-// completes the dlogits row for the dW GEMM: d[i][t_i] -= 1 / n_valid.
+// dx row i = sum over splits of the fp32 partials of dlogits·W (in split
+// order) + dcorr[i]·W[t_i], rounded once to bf16. dcorr[i] is the fp32
+// rounding error of the bf16 dlogits entry at the target column, so the sum
+// is dx as if that entry, the largest of the row, had been stored exactly.
+// blockIdx.y = token row, 4 columns per thread.
 __global__ void dx_reduce_kernel(const float* __restrict__ part, int splits, int64_t split_stride,
                                  int64_t H, const __nv_bfloat16* __restrict__ W, int64_t V,
                                  const int64_t* __restrict__ t, int64_t ignore_index,
-                                 const uint32_t* __restrict__ ctrl, __nv_bfloat16* __restrict__ buf,
-                                 int64_t ldv, __nv_bfloat16* __restrict__ dx) {
+                                 const uint32_t* __restrict__ ctrl, const float* __restrict__ dcorr,
+                                 __nv_bfloat16* __restrict__ dx) {
   const int r = blockIdx.y;
   const int64_t h = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (h >= H) return;
   const int64_t tg = t[r];
-  const uint32_t nv = ctrl[kCtrlNValid];
-  const bool onehot = tg != ignore_index && tg >= 0 && tg < V && nv > 0;
-  const float scale = onehot ? 1.0f / static_cast<float>(nv) : 0.f;
-  if (h < H) {
-    const int64_t i = static_cast<int64_t>(r) * H + h;
-    float4 acc = *reinterpret_cast<const float4*>(part + i);
-    for (int s = 1; s < splits; ++s) {
-      const float4 v = *reinterpret_cast<const float4*>(part + s * split_stride + i);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    if (onehot) {
-      const uint2 wv = *reinterpret_cast<const uint2*>(W + tg * H + h);
-      const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.x));
-      const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.y));
-      acc.x = fmaf(-w01.x, scale, acc.x);
-      acc.y = fmaf(-w01.y, scale, acc.y);
-      acc.z = fmaf(-w23.x, scale, acc.z);
-      acc.w = fmaf(-w23.y, scale, acc.w);
-    }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 o;
-    o.x = *reinterpret_cast<uint32_t*>(&lo);
-    o.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dx + i) = o;
+  const bool corr = tg != ignore_index && tg >= 0 && tg < V && ctrl[kCtrlNValid] > 0;
+  const int64_t i = static_cast<int64_t>(r) * H + h;
+  float4 acc = *reinterpret_cast<const float4*>(part + i);
+  for (int s = 1; s < splits; ++s) {
+    const float4 v = *reinterpret_cast<const float4*>(part + s * split_stride + i);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
   }
-  if (onehot && blockIdx.x == 0 && threadIdx.x == 0) {
-    __nv_bfloat16* p = buf + static_cast<size_t>(r) * ldv + tg;
-    *p = __float2bfloat16_rn(__bfloat162float(*p) - scale);
+  if (corr) {
+    const float c = dcorr[r];
+    const uint2 wv = *reinterpret_cast<const uint2*>(W + tg * H + h);
+    const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.x));
+    const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.y));
+    acc.x = fmaf(w01.x, c, acc.x);
+    acc.y = fmaf(w01.y, c, acc.y);
+    acc.z = fmaf(w23.x, c, acc.z);
+    acc.w = fmaf(w23.y, c, acc.w);
   }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 o;
+  o.x = *reinterpret_cast<uint32_t*>(&lo);
+  o.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(dx + i) = o;
 }
 
 // loss = (sum of token losses) / n_valid, the sum in float64 and fixed order
@@ -234,12 +247,12 @@ cudaError_t launch_lse_combine(const float2* partials, int vocab_tiles, const fl
 cudaError_t launch_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int rows, int64_t V,
                                 const float2* partials, int vocab_tiles, const float* lse,
                                 const int64_t* t_chunk, int64_t ignore_index,
-                                const uint32_t* ctrl, cudaStream_t s) {
+                                const uint32_t* ctrl, float* dcorr, cudaStream_t s) {
   const int threads = 256;
-  const int64_t per_block = threads * 8;
+  const int64_t per_block = threads * 8 * kDlogitsVecs;
   dim3 grid(static_cast<unsigned>((ldv + per_block - 1) / per_block), static_cast<unsigned>(rows));
   dlogits_bf16_kernel<<<grid, threads, 0, s>>>(buf, ldv, V, partials, vocab_tiles, lse, t_chunk,
-                                               ignore_index, ctrl);
+                                               ignore_index, ctrl, dcorr);
   return cudaGetLastError();
 }
 
@@ -255,12 +268,12 @@ cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, con
 
 cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_stride, int rows,
                              int64_t H, const __nv_bfloat16* W, int64_t V, const int64_t* t_chunk,
-                             int64_t ignore_index, const uint32_t* ctrl, __nv_bfloat16* buf,
-                             int64_t ldv, __nv_bfloat16* dx, cudaStream_t s) {
+                             int64_t ignore_index, const uint32_t* ctrl, const float* dcorr,
+                             __nv_bfloat16* dx, cudaStream_t s) {
   const int threads = 128;  // H % 8 == 0: 4 columns per thread, no partial vectors
   dim3 grid(static_cast<unsigned>((H / 4 + threads - 1) / threads), static_cast<unsigned>(rows));
   dx_reduce_kernel<<<grid, threads, 0, s>>>(partials, splits, split_stride, H, W, V, t_chunk,
-                                            ignore_index, ctrl, buf, ldv, dx);
+                                            ignore_index, ctrl, dcorr, dx);
   return cudaGetLastError();
 }
 

@@ -200,17 +200,32 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
           stage_and_store(w, [&](uint32_t src) { tma_store_2d(tmO, src, c0, m0); });
         }
       } else {
-        // softmax / n_valid = exp(z - lse) * scale, written over the logits
-        // buffer; the dx reduction adds the -onehot / n_valid term
+        // d = (exp(z - lse) - onehot) * scale over the logits buffer; the
+        // fp32 rounding error of the target entry goes to dcorr for the dx
+        // reduction
+        const int k = (tcol >= g * 64 && tcol < g * 64 + 64) ? tcol - g * 64 : -1;
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float v[4] = {__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]),
                         __uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])};
+          const int ci[4] = {2 * i, 2 * i + 1, 32 + 2 * i, 33 + 2 * i};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) v[q] = ex2_approx(fmaf(v[q], kLog2e, -lse_l2)) * scale;
+          for (int q = 0; q < 4; ++q) {
+            float p = ex2_approx(fmaf(v[q], kLog2e, -lse_l2));
+            if (ci[q] == k) p -= 1.0f;
+            v[q] = p * scale;
+          }
           w[i] = pack_bf16x2(v[0], v[1]);
           w[16 + i] = pack_bf16x2(v[2], v[3]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (ci[q] == k) {
+              const uint32_t word = q < 2 ? w[i] : w[16 + i];
+              const uint32_t bits = (q & 1) ? (word >> 16) : (word & 0xFFFFu);
+              a.dcorr[grow] = v[q] - __uint_as_float(bits << 16);
+            }
+          }
         }
         stage_and_store(w, [&](uint32_t src) { tma_store_2d(tmO, src, c0, m0); });
       }
@@ -616,6 +631,217 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// ============================================ dx and dW GEMMs in one launch
+//
+// Both backward contractions of a chunk read the finished dlogits buffer
+// and write fp32 (dx split partials; dW stored or added), so they can share
+// one persistent launch: the dx work units come first in the static
+// schedule, then the many short dW units fill every pair's remaining time.
+// Problem 0 is dx (A = dlogits, K-major), problem 1 is dW (A = dlogitsᵀ,
+// MN-major); B (W, x_c) is MN-major in both.
+
+template <int AMN>
+__device__ __forceinline__ void load_a_pair(uint32_t sa, const CUtensorMap* m, uint32_t fb, int k0,
+                                            int mA) {
+  if (AMN == 0) {
+    tma_load_2d_pair(sa, m, fb, k0, mA);
+  } else {
+    tma_load_2d_pair(sa, m, fb, mA, k0);
+    tma_load_2d_pair(sa + 8192, m, fb, mA + 64, k0);
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    umma_pair_dual_kernel(const __grid_constant__ DualMaps maps, const __grid_constant__ DualArgs d) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStagesPair * kABytes;
+  uint8_t* sE = sB + kStagesPair * kBHalfBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesPair + 5);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStagesPair + s); };
+  auto tfull_bar = [&](int acc) { return bar0 + 8u * (2 * kStagesPair + acc); };
+  auto tempty_bar = [&](int acc) { return bar0 + 8u * (2 * kStagesPair + 2 + acc); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStagesPair + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(num_clusters_x());
+  uint32_t* ctrl = d.p[0].ctrl;
+  const uint64_t timeout_ns = d.p[0].timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesPair; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int acc = 0; acc < 2; ++acc) {
+      mbar_init(tfull_bar(acc), 1);
+      mbar_init(tempty_bar(acc), 2 * kEpiThreads);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    for (int q = 0; q < 2; ++q) {
+      tma_prefetch_map(&maps.a[q]);
+      tma_prefetch_map(&maps.b[q]);
+      tma_prefetch_map(&maps.o[q]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int units1 = d.p[1].num_m * d.p[1].num_n * d.p[1].num_s;
+  const int num_units = d.units0 + units1;
+  // problem and its own unit index for a unit of the combined schedule
+  auto locate = [&](int u, int& q, Unit& t) {
+    q = u >= d.units0 ? 1 : 0;
+    t = unit_coords(d.p[q], q ? u - d.units0 : u);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t n_issued = 0;
+      bool failed = false;
+      for (int u = pair; u < num_units && !failed; u += npairs) {
+        int q;
+        Unit t;
+        locate(u, q, t);
+        const UmmaArgs& a = d.p[q];
+        const int kb0 = t.s * a.kb_per_split;
+        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+        const int mA = t.m * 2 * kBM + static_cast<int>(rank) * kBM;
+        const int nB = t.n * kBN + static_cast<int>(rank) * (kBN / 2);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int stage = n_issued % kStagesPair;
+          const uint32_t phase = (n_issued / kStagesPair) & 1u;
+          if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, ctrl, timeout_ns)) {
+            failed = true;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytesPair);
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          const uint32_t sa = smem_u32(sA + stage * kABytes);
+          const uint32_t sb = smem_u32(sB + stage * kBHalfBytes);
+          const int k0 = kb * kBK;
+          if (q == 0)
+            load_a_pair<0>(sa, &maps.a[0], fb, k0, mA);
+          else
+            load_a_pair<1>(sa, &maps.a[1], fb, k0, mA);
+          tma_load_2d_pair(sb, &maps.b[q], fb, nB, k0);
+          tma_load_2d_pair(sb + 8192, &maps.b[q], fb, nB + 64, k0);
+          ++n_issued;
+        }
+      }
+      if (failed && rank == 0) {
+        const uint32_t first = n_issued > kStagesPair ? n_issued - kStagesPair : 0;
+        for (uint32_t i = first; i < n_issued; ++i)
+          mbar_drain_wait(full_bar(i % kStagesPair), (i / kStagesPair) & 1u, timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc_k = idesc_bf16_f32(2 * kBM, kBN, 0, 1);
+      constexpr uint32_t idesc_mn = idesc_bf16_f32(2 * kBM, kBN, 1, 1);
+      uint32_t n_consumed = 0;
+      bool issued = false, failed = false;
+      int it = 0;
+      for (int u = pair; u < num_units && !failed; u += npairs, ++it) {
+        int q;
+        Unit t;
+        locate(u, q, t);
+        const UmmaArgs& a = d.p[q];
+        const int kb0 = t.s * a.kb_per_split;
+        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait_bounded_cluster(tempty_bar(acc), acc_phase ^ 1u, ctrl, timeout_ns)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        const uint32_t idesc = q ? idesc_mn : idesc_k;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int stage = n_consumed % kStagesPair;
+          const uint32_t phase = (n_consumed / kStagesPair) & 1u;
+          if (!mbar_wait_bounded_cluster(full_bar(stage), phase, ctrl, timeout_ns)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(sA + stage * kABytes);
+          const uint32_t sb = smem_u32(sB + stage * kBHalfBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = q ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                  : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+            const uint64_t bd = smem_desc_sw128(sb + 2048u * k, 8192u, 1024u);
+            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit_pair_multicast(empty_bar(stage), 0x3);
+          ++n_consumed;
+        }
+        if (failed) break;
+        tc_commit_pair_multicast(tfull_bar(acc), 0x3);
+      }
+      if (failed && issued) {
+        tc_commit_pair(drain_bar);
+        mbar_drain_wait(drain_bar, 0, timeout_ns);
+      }
+    }
+  } else {
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const bool leader = threadIdx.x == 64;
+    uint32_t ebuf = 0;
+    int it = 0;
+    for (int u = pair; u < num_units; u += npairs, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      const bool ok = mbar_wait_bounded_cluster(tfull_bar(acc), acc_phase, ctrl, timeout_ns);
+      if (named_bar_or(kEpiBar, kEpiThreads, !ok)) break;
+      tc_fence_after();
+      int q;
+      Unit t;
+      locate(u, q, t);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + acc * kBN;
+      const int m0 = t.m * 2 * kBM + static_cast<int>(rank) * kBM;
+      epilogue_tile<kEpiF32>(d.p[q], &maps.o[q], sE, ebuf, row, leader, m0, t.n * kBN, t.n, t.s, tbase,
+                             [&] {
+                               tc_fence_before();
+                               if (rank == 0)
+                                 mbar_arrive(tempty_bar(acc));
+                               else
+                                 mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+                             });
+    }
+    if (leader) bulk_wait_group<0>();
+  }
+
+  __syncwarp();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 // One bounded wait on a barrier that nothing completes: checks that a wait
 // which runs out reports FLCE_ERR_TIMEOUT and returns.
 __global__ void wait_check_kernel(uint32_t* ctrl, uint64_t timeout_ns) {
@@ -684,6 +910,15 @@ cudaError_t launch_umma_pair(int kind, const CUtensorMap& a, const CUtensorMap& 
     case kUmmaCheckMK: return launch_pair<1, 0, kEpiF32>(a, b, o, args, pairs, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_umma_pair_dual(const DualMaps& maps, const DualArgs& args, int pairs,
+                                  cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(umma_pair_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytesPair));
+  if (e != cudaSuccess) return e;
+  umma_pair_dual_kernel<<<2 * pairs, kThreads, kSmemBytesPair, s>>>(maps, args);
+  return cudaGetLastError();
 }
 
 // Clusters of two that fit on the device at once for the pair kernels

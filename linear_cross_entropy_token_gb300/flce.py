@@ -24,7 +24,7 @@ DLOGITS = {"auto": 0, "inplace": 1, "recompute": 2}
 CTA = {"auto": 0, "single": 1, "pair": 2}
 KERNEL_KINDS = ["count_valid", "gemm_logits_lse", "lse_combine", "dlogits_inplace",
                 "gemm_dlogits_recompute", "gemm_dx", "dx_split_reduce", "gemm_dw",
-                "loss_finalize", "simt_gemm_f32", "simt_tile_stats_f32"]
+                "loss_finalize", "simt_gemm_f32", "simt_tile_stats_f32", "gemm_dx_dw"]
 
 
 class FlceError(RuntimeError):

@@ -14,10 +14,12 @@ from flce_testing import assert_parity, device_inputs, rel_fro, run, to_np64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def bf16():
+@pytest.fixture(scope="module", params=["single", "pair"])
+def bf16(request):
+    """Both GEMM tile shapes: one CTA per 128 x 256 tile, and CTA pairs per
+    256 x 256 tile (with dx and dW in one launch)."""
     from linear_cross_entropy_token_gb300 import FLCE
-    h = FLCE("bf16", 0, hbm_budget_bytes=4 << 30)
+    h = FLCE("bf16", 0, hbm_budget_bytes=4 << 30, cta=request.param)
     yield h
     h.close()
 
@@ -83,11 +85,16 @@ def test_cta_pair_tiles(bf16_pair, N, H, V, chunk, ign):
     assert_parity(run(bf16_pair, w, chunk=chunk), _oracle(w), "bf16", token_rtol=1e-3)
 
 
-def test_cta_pair_matches_single(bf16, bf16_pair):
+def test_cta_pair_matches_single(bf16_pair):
     """Both tile shapes accumulate each output in the same k order: results
     agree to rounding of the fp32 accumulation order within a k-block."""
+    from linear_cross_entropy_token_gb300 import FLCE
     w = workloads.generate(workloads.custom(1024, 512, 6000, "bf16", ignore_frac=0.1, seed=31))
-    a = run(bf16, w, chunk=512)
+    single = FLCE("bf16", 0, cta="single")
+    try:
+        a = run(single, w, chunk=512)
+    finally:
+        single.close()
     b = run(bf16_pair, w, chunk=512)
     assert abs(a["loss"] - b["loss"]) <= 1e-5 * abs(a["loss"])
     assert rel_fro(b["dW"], a["dW"]) <= 1e-2 and rel_fro(b["dx"], a["dx"]) <= 1e-2
