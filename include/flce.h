@@ -89,8 +89,16 @@ typedef struct flce_config {
     int32_t dlogits_mode;        /* FLCE_DLOGITS_*                                     */
     int32_t timeout_ms;          /* limit of every device-side wait; 0 = 2000 ms       */
     int32_t cta_pair;            /* FLCE_CTA_*                                         */
-    int32_t reserved;            /* must be 0                                          */
+    int32_t backward_launch;     /* FLCE_BACKWARD_*                                    */
 } flce_config;
+
+/* How the dx and dW GEMMs of a chunk are launched (CTA pairs only).
+ *  SEPARATE:   one launch each.
+ *  ONE_LAUNCH: one launch; its work units (dx first, then dW) are handed out
+ *              dynamically, so the short dW units fill the time the long dx
+ *              units leave idle at the end.
+ *  AUTO:       ONE_LAUNCH. */
+enum { FLCE_BACKWARD_AUTO = 0, FLCE_BACKWARD_SEPARATE = 1, FLCE_BACKWARD_ONE_LAUNCH = 2 };
 
 /* The chunk plan of one call (token-chunk scheduler). */
 typedef struct flce_plan {

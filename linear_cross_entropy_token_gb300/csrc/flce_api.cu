@@ -557,8 +557,9 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       d.reduce_add = c > 0 ? 1 : 0;
       const double dx_bytes = 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH;
       const double dw_bytes = 2 * dr * dV + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dV * dH;
-      if (h->use_pair) {
-        // both read the finished dlogits buffer: one launch, dx units first
+      if (h->use_pair && h->cfg.backward_launch != FLCE_BACKWARD_SEPARATE) {
+        // both read the finished dlogits buffer: one launch, dx units first,
+        // handed out from a counter in the control block
         DualMaps maps;
         maps.a[0] = mZ_k;
         maps.b[0] = mW_mn;
@@ -573,6 +574,9 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
         da.p[1].num_m = static_cast<int>(cdiv(V, 2 * kBM));
         da.units0 = da.p[0].num_m * da.p[0].num_n * da.p[0].num_s;
         da.pad = 0;
+        da.sched_ctr = reinterpret_cast<int32_t*>(ctrl + kCtrlSched);
+        e = cudaMemsetAsync(da.sched_ctr, 0, 4, s);
+        if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
         const int units = da.units0 + da.p[1].num_m * da.p[1].num_n;
         FLCE_LAUNCH(FLCE_K_GEMM_DX_DW, 4 * dr * dV * dH, dx_bytes + dw_bytes,
                     launch_umma_pair_dual(maps, da, std::min(units, h->pair_clusters), s));

@@ -12,6 +12,7 @@ enum CtrlWord : int {
   kCtrlError = 0,    // first error recorded by a kernel (flce_status numbering)
   kCtrlNValid = 1,   // number of non-ignored tokens
   kCtrlLoss = 2,     // fp32 bits of the mean loss
+  kCtrlSched = 3,    // work-unit counter of a dynamically scheduled launch
   kCtrlWords = 16
 };
 
@@ -80,8 +81,9 @@ struct DualMaps {
 };
 struct DualArgs {
   UmmaArgs p[2];
-  int32_t units0;  // work units of problem 0
+  int32_t units0;       // work units of problem 0
   int32_t pad;
+  int32_t* sched_ctr;   // next unit to hand out; zero before each launch
 };
 cudaError_t launch_umma_pair_dual(const DualMaps& maps, const DualArgs& args, int pairs,
                                   cudaStream_t s);

@@ -635,10 +635,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 //
 // Both backward contractions of a chunk read the finished dlogits buffer
 // and write fp32 (dx split partials; dW stored or added), so they can share
-// one persistent launch: the dx work units come first in the static
-// schedule, then the many short dW units fill every pair's remaining time.
-// Problem 0 is dx (A = dlogits, K-major), problem 1 is dW (A = dlogitsᵀ,
-// MN-major); B (W, x_c) is MN-major in both.
+// one persistent launch. Problem 0 is dx (A = dlogits, K-major), problem 1 is
+// dW (A = dlogitsᵀ, MN-major); B (W, x_c) is MN-major in both.
+//
+// The units differ in length (a dx unit runs ~1000 k-blocks, a dW unit 64),
+// so they are handed out dynamically: the even CTA's producer claims the next
+// unit from a global counter (dx units first) and publishes its index in a
+// 4-deep ring in shared memory, to its own MMA issuer and epilogue and, over
+// distributed shared memory, to the odd CTA's producer and epilogue. Each of
+// those four consumers releases the slot on an mbarrier of the even CTA. A
+// pair that finished early simply claims more of the short units.
+constexpr int kSchedDepth = 4;
+constexpr uint32_t kSmemBytesDual = kSmemBytesPair + 2 * kSchedDepth * 8 + kSchedDepth * 4 + 16;
+static_assert(kSmemBytesDual <= 232448, "shared memory per CTA");
 
 template <int AMN>
 __device__ __forceinline__ void load_a_pair(uint32_t sa, const CUtensorMap* m, uint32_t fb, int k0,
@@ -660,7 +669,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + kStagesPair * kABytes;
   uint8_t* sE = sB + kStagesPair * kBHalfBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesPair + 5);
+  uint64_t* sbars = bars + 2 * kStagesPair + 5;  // unit ring: full[kSchedDepth], empty[kSchedDepth]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbars + 2 * kSchedDepth);
+  int32_t* sched_u = reinterpret_cast<int32_t*>(tmem_slot + 1);
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -668,12 +679,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int acc) { return bar0 + 8u * (2 * kStagesPair + acc); };
   auto tempty_bar = [&](int acc) { return bar0 + 8u * (2 * kStagesPair + 2 + acc); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kStagesPair + 4);
+  const uint32_t sbar0 = smem_u32(sbars);
+  auto sfull_bar = [&](int i) { return sbar0 + 8u * i; };
+  auto sempty_bar = [&](int i) { return sbar0 + 8u * (kSchedDepth + i); };
+  const uint32_t su0 = smem_u32(sched_u);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
-  const int pair = static_cast<int>(cluster_id_x());
-  const int npairs = static_cast<int>(num_clusters_x());
   uint32_t* ctrl = d.p[0].ctrl;
   const uint64_t timeout_ns = d.p[0].timeout_ns;
 
@@ -687,6 +700,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(acc), 2 * kEpiThreads);
     }
     mbar_init(drain_bar, 1);
+    for (int i = 0; i < kSchedDepth; ++i) {
+      mbar_init(sfull_bar(i), 1);   // the even CTA's producer publishes
+      mbar_init(sempty_bar(i), 4);  // even MMA, even epilogue, odd producer, odd epilogue
+    }
     fence_mbar_init();
     fence_proxy_async_smem();
     for (int q = 0; q < 2; ++q) {
@@ -711,12 +728,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     q = u >= d.units0 ? 1 : 0;
     t = unit_coords(d.p[q], q ? u - d.units0 : u);
   };
+  // consumers: the unit of step i (-1 = no more), then release the slot.
+  // Returns false if the wait ran out.
+  auto next_unit = [&](int i, int& u, bool release) {
+    const int slot = i % kSchedDepth;
+    if (!mbar_wait_bounded_cluster(sfull_bar(slot), (i / kSchedDepth) & 1u, ctrl, timeout_ns))
+      return false;
+    u = ld_shared_s32(su0 + 4u * slot);
+    if (release) {
+      if (rank == 0)
+        mbar_arrive(sempty_bar(slot));
+      else
+        mbar_arrive_cluster(mapa_shared(sempty_bar(slot), 0));
+    }
+    return true;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t n_issued = 0;
       bool failed = false;
-      for (int u = pair; u < num_units && !failed; u += npairs) {
+      for (int i = 0; !failed; ++i) {
+        int u;
+        if (rank == 0) {
+          // claim the next unit and publish it to both CTAs
+          const int slot = i % kSchedDepth;
+          if (!mbar_wait_bounded_cluster(sempty_bar(slot), ((i / kSchedDepth) & 1u) ^ 1u, ctrl,
+                                         timeout_ns)) {
+            failed = true;
+            break;
+          }
+          u = atomicAdd(d.sched_ctr, 1);
+          if (u >= num_units) u = -1;
+          sched_u[slot] = u;
+          st_shared_cluster_u32(mapa_shared(su0 + 4u * slot, 1), static_cast<uint32_t>(u));
+          mbar_arrive(sfull_bar(slot));
+          mbar_arrive_cluster(mapa_shared(sfull_bar(slot), 1));
+        } else if (!next_unit(i, u, true)) {
+          failed = true;
+          break;
+        }
+        if (u < 0) break;
         int q;
         Unit t;
         locate(u, q, t);
@@ -758,8 +810,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_mn = idesc_bf16_f32(2 * kBM, kBN, 1, 1);
       uint32_t n_consumed = 0;
       bool issued = false, failed = false;
-      int it = 0;
-      for (int u = pair; u < num_units && !failed; u += npairs, ++it) {
+      for (int it = 0; !failed; ++it) {
+        int u;
+        if (!next_unit(it, u, true)) {
+          failed = true;
+          break;
+        }
+        if (u < 0) break;
         int q;
         Unit t;
         locate(u, q, t);
@@ -809,8 +866,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int row = wq * 32 + lane;
     const bool leader = threadIdx.x == 64;
     uint32_t ebuf = 0;
-    int it = 0;
-    for (int u = pair; u < num_units; u += npairs, ++it) {
+    for (int it = 0;; ++it) {
+      int u = -1;
+      const bool got = next_unit(it, u, false);
+      // all 128 threads have read the slot (or given up) before one releases it
+      if (named_bar_or(kEpiBar, kEpiThreads, !got)) break;
+      if (leader) {
+        const int slot = it % kSchedDepth;
+        if (rank == 0)
+          mbar_arrive(sempty_bar(slot));
+        else
+          mbar_arrive_cluster(mapa_shared(sempty_bar(slot), 0));
+      }
+      if (u < 0) break;
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       const bool ok = mbar_wait_bounded_cluster(tfull_bar(acc), acc_phase, ctrl, timeout_ns);
@@ -915,9 +983,9 @@ cudaError_t launch_umma_pair(int kind, const CUtensorMap& a, const CUtensorMap& 
 cudaError_t launch_umma_pair_dual(const DualMaps& maps, const DualArgs& args, int pairs,
                                   cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(umma_pair_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytesPair));
+                                       static_cast<int>(kSmemBytesDual));
   if (e != cudaSuccess) return e;
-  umma_pair_dual_kernel<<<2 * pairs, kThreads, kSmemBytesPair, s>>>(maps, args);
+  umma_pair_dual_kernel<<<2 * pairs, kThreads, kSmemBytesDual, s>>>(maps, args);
   return cudaGetLastError();
 }
 

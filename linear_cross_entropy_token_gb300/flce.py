@@ -22,6 +22,7 @@ STATUS = {0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3:
 DTYPE_BF16, DTYPE_FP32 = 0, 1
 DLOGITS = {"auto": 0, "inplace": 1, "recompute": 2}
 CTA = {"auto": 0, "single": 1, "pair": 2}
+BACKWARD = {"auto": 0, "separate": 1, "one_launch": 2}
 KERNEL_KINDS = ["count_valid", "gemm_logits_lse", "lse_combine", "dlogits_inplace",
                 "gemm_dlogits_recompute", "gemm_dx", "dx_split_reduce", "gemm_dw",
                 "loss_finalize", "simt_gemm_f32", "simt_tile_stats_f32", "gemm_dx_dw"]
@@ -38,7 +39,7 @@ class Config(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("hbm_budget_bytes", ctypes.c_uint64), ("dlogits_mode", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_int32), ("cta_pair", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("backward_launch", ctypes.c_int32)]
 
 
 class Plan(ctypes.Structure):
@@ -109,9 +110,10 @@ def header_functions() -> list:
 
 
 def make_config(dtype: str = "bf16", device: int = 0, hbm_budget_bytes: int = 0,
-                dlogits_mode: str = "auto", timeout_ms: int = 0, cta: str = "auto") -> Config:
+                dlogits_mode: str = "auto", timeout_ms: int = 0, cta: str = "auto",
+                backward: str = "auto") -> Config:
     return Config(DTYPE_BF16 if dtype == "bf16" else DTYPE_FP32, device, hbm_budget_bytes,
-                  DLOGITS[dlogits_mode], timeout_ms, CTA[cta], 0)
+                  DLOGITS[dlogits_mode], timeout_ms, CTA[cta], BACKWARD[backward])
 
 
 def plan(N: int, H: int, V: int, dtype: str = "bf16", chunk: int = 0, hbm_budget_bytes: int = 0,
@@ -135,11 +137,13 @@ class FLCE:
     """One library handle on one device, for one input dtype ("bf16" or "fp32")."""
 
     def __init__(self, dtype: str = "bf16", device: int = 0, hbm_budget_bytes: int = 0,
-                 dlogits_mode: str = "auto", timeout_ms: int = 0, cta: str = "auto"):
+                 dlogits_mode: str = "auto", timeout_ms: int = 0, cta: str = "auto",
+                 backward: str = "auto"):
         self.lib = load()
         self.dtype = dtype
         self.device = device
-        self.cfg = make_config(dtype, device, hbm_budget_bytes, dlogits_mode, timeout_ms, cta)
+        self.cfg = make_config(dtype, device, hbm_budget_bytes, dlogits_mode, timeout_ms, cta,
+                               backward)
         h = ctypes.c_void_p()
         st = self.lib.flce_create(ctypes.byref(h), ctypes.byref(self.cfg))
         if st != FLCE_OK:
