@@ -557,7 +557,7 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
       d.reduce_add = c > 0 ? 1 : 0;
       const double dx_bytes = 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH;
       const double dw_bytes = 2 * dr * dV + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dV * dH;
-      if (h->use_pair && h->cfg.backward_launch != FLCE_BACKWARD_SEPARATE) {
+      if (h->use_pair && h->cfg.backward_launch == FLCE_BACKWARD_ONE_LAUNCH) {
         // both read the finished dlogits buffer: one launch, dx units first,
         // handed out from a counter in the control block
         DualMaps maps;

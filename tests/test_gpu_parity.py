@@ -14,7 +14,7 @@ from flce_testing import assert_parity, device_inputs, rel_fro, run, to_np64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=["single", "pair", "pair-separate"])
+@pytest.fixture(scope="module", params=["single", "pair", "pair-one_launch"])
 def bf16(request):
     """Both GEMM tile shapes: one CTA per 128 x 256 tile, and CTA pairs per
     256 x 256 tile, with the dx and dW GEMMs in one dynamically scheduled
@@ -22,7 +22,7 @@ def bf16(request):
     from linear_cross_entropy_token_gb300 import FLCE
     cta, _, sep = request.param.partition("-")
     h = FLCE("bf16", 0, hbm_budget_bytes=4 << 30, cta=cta,
-             backward="separate" if sep else "auto")
+             backward=sep or "auto")
     yield h
     h.close()
 
