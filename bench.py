@@ -45,8 +45,11 @@ def parse():
     p.add_argument("--chunk", type=int, default=0)
     p.add_argument("--budget-gib", type=float, default=0.0)
     p.add_argument("--dlogits", choices=["auto", "inplace", "recompute"], default="auto")
-    p.add_argument("--cta", choices=["auto", "single", "pair"], default="auto",
-                   help="GEMM tile shape: one CTA per 128x256 tile, or CTA pairs per 256x256")
+    p.add_argument("--cta", choices=["auto", "single", "pair", "quad"], default="auto",
+                   help="GEMM tile shape: one CTA per 128x256 tile, CTA pairs per 256x256, "
+                        "or two pairs sharing B per 512x256")
+    p.add_argument("--backward", choices=["auto", "separate", "one_launch"], default="auto",
+                   help="dx and dW GEMMs of a chunk in two launches or one (CTA pairs)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -245,7 +248,8 @@ def run_ours(args, ws, rank, local):
     dx = torch.empty_like(x)
     dW = torch.empty((V, H), dtype=torch.float32, device=dev)
     budget = int(args.budget_gib * (1 << 30))
-    h = FLCE("bf16", local, hbm_budget_bytes=budget, dlogits_mode=args.dlogits, cta=args.cta)
+    h = FLCE("bf16", local, hbm_budget_bytes=budget, dlogits_mode=args.dlogits, cta=args.cta,
+             backward=args.backward)
     stream = torch.cuda.current_stream(dev)
 
     free0, _ = torch.cuda.mem_get_info(dev)
@@ -345,7 +349,9 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": args.config, "N": N, "H": H, "V": V, "chunk": plan["chunk"],
                    "num_chunks": plan["num_chunks"], "dx_splits": plan["dx_splits"],
                    "dlogits": "recompute" if args.dlogits == "recompute" else "inplace",
-                   "gemm_tiles": "256x256, CTA pairs" if plan["tile_m"] == 256 else "128x256, one CTA",
+                   "gemm_tiles": {128: "128x256, one CTA", 256: "256x256, CTA pairs",
+                                  512: "512x256, two CTA pairs sharing B"}[plan["tile_m"]],
+                   "backward_gemms": "one launch" if args.backward == "one_launch" else "two launches",
                    "targets": w.spec.targets, "ignore_frac": float(w.spec.ignore_frac),
                    "l2": "inputs larger than L2 (W is 1.05 GB bf16; the chunk buffer 1.05 GB)",
                    "parallelism": "replicas" if ws > 1 else "single"},

@@ -80,7 +80,11 @@ enum { FLCE_DLOGITS_AUTO = 0, FLCE_DLOGITS_INPLACE = 1, FLCE_DLOGITS_RECOMPUTE =
  *          (tcgen05 cta_group::2): each CTA loads half of the B operand.
  *  AUTO:   PAIR (measured faster on GB300: 34.1 vs 36.9 ms for the 16384-token,
  *          128256-vocabulary step), SINGLE where pairs cannot be scheduled. */
-enum { FLCE_CTA_AUTO = 0, FLCE_CTA_SINGLE = 1, FLCE_CTA_PAIR = 2 };
+enum { FLCE_CTA_AUTO = 0, FLCE_CTA_SINGLE = 1, FLCE_CTA_PAIR = 2, FLCE_CTA_QUAD = 3 };
+/*  QUAD:   clusters of two CTA pairs on consecutive 256-row blocks of the same
+ *          256 columns (512 x 256 tiles); the pairs share B through TMA
+ *          multicast, so a CTA fetches a quarter of the B tile instead of a
+ *          half. */
 
 typedef struct flce_config {
     int32_t dtype;               /* FLCE_DTYPE_*                                       */

@@ -97,13 +97,17 @@ Layout make_layout(int64_t N, int64_t H, int64_t C, int64_t ldv, int64_t vt, int
   return L;
 }
 
-// CTA pairs are the default tile shape (FLCE_CTA_AUTO)
-constexpr bool kAutoPair = true;
+// Tile shape that FLCE_CTA_AUTO resolves to
+constexpr int kAutoCta = FLCE_CTA_PAIR;
 
-bool wants_pair(const flce_config* cfg) {
-  return cfg->dtype == FLCE_DTYPE_BF16 &&
-         (cfg->cta_pair == FLCE_CTA_PAIR || (cfg->cta_pair == FLCE_CTA_AUTO && kAutoPair));
+// CTAs per GEMM work unit: 1 (single), 2 (pair) or 4 (two pairs sharing B)
+int cta_group_size(const flce_config* cfg) {
+  if (cfg->dtype != FLCE_DTYPE_BF16) return 1;
+  const int mode = cfg->cta_pair == FLCE_CTA_AUTO ? kAutoCta : cfg->cta_pair;
+  return mode == FLCE_CTA_QUAD ? 4 : mode == FLCE_CTA_PAIR ? 2 : 1;
 }
+
+bool wants_pair(const flce_config* cfg) { return cta_group_size(cfg) == 2; }
 
 // Splits of the dx GEMM's V reduction that fill the machine's waves best:
 // `slots` work units run at once (SMs, or SM pairs), each tile_m x 256.
@@ -147,9 +151,9 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   std::memset(out, 0, sizeof(*out));
   out->ldv = static_cast<int64_t>(align_up(static_cast<uint64_t>(V), 64));
   out->vocab_tiles = cdiv(V, kVocabTile);
-  const bool pair = wants_pair(cfg);
+  const int group = cta_group_size(cfg);
   auto splits_for = [&](int64_t C) {
-    return bf16 ? pick_dx_splits(C, H, V, pair ? num_sms / 2 : num_sms, pair ? 2 * kBM : kBM) : 0;
+    return bf16 ? pick_dx_splits(C, H, V, num_sms / group, group * kBM) : 0;
   };
   auto ws = [&](int64_t C) {
     return make_layout(N, H, C, out->ldv, out->vocab_tiles, splits_for(C), esize).total;
@@ -190,7 +194,7 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   out->workspace_bytes =
       make_layout(N, H, C, out->ldv, out->vocab_tiles, C ? splits_for(C) : 0, esize).total;
   out->logits_bytes = static_cast<uint64_t>(C) * out->ldv * esize;
-  out->tile_m = pair ? 2 * kBM : kBM;
+  out->tile_m = group * kBM;
   return FLCE_OK;
 }
 
@@ -204,6 +208,8 @@ struct flce_handle_s {
   int num_sms = 0;
   int pair_clusters = 0;  // clusters of two the pair kernels fit at once
   bool use_pair = false;  // GEMMs on CTA pairs (256 x 256 tiles)
+  int quad_clusters = 0;  // clusters of four the quad kernels fit at once
+  bool use_quad = false;  // GEMMs on two pairs sharing B (512 x 256 tiles)
   uint64_t timeout_ns = 0;
   std::string err;
   // workspace
@@ -389,6 +395,11 @@ flce_status read_back(flce_handle_t h, uint32_t* ctrl_dev, cudaStream_t s, float
 // grid from the work units (persistent CTAs, or CTA pairs).
 cudaError_t launch_gemm(flce_handle_t h, int kind, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& o, UmmaArgs args, int64_t M, cudaStream_t s) {
+  if (h->use_quad) {
+    args.num_m = static_cast<int>(cdiv(M, 4 * kBM));
+    const int units = args.num_m * args.num_n * args.num_s;
+    return launch_umma_quad(kind, a, b, o, args, std::min(units, h->quad_clusters), s);
+  }
   if (h->use_pair) {
     args.num_m = static_cast<int>(cdiv(M, 2 * kBM));
     const int units = args.num_m * args.num_n * args.num_s;
@@ -475,7 +486,7 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
     const bool recompute = h->cfg.dlogits_mode == FLCE_DLOGITS_RECOMPUTE;
     CUtensorMap mW_k, mW_mn, mX_k, mX_mn, mZ_out, mZ_k, mZ_mn, mDx, mDw;
     // a CTA of a pair loads 128 of the tile's 256 columns of a K-major B
-    if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, h->use_pair ? 128 : 256, &why) ||
+    if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, h->use_quad ? 64 : h->use_pair ? 128 : 256, &why) ||
         !map_bf16_2d(&mW_mn, W, H, V, H * 2, 64, 64, &why) ||
         !map_f32_3d(&mDw, dW, H, V, 1, H * 4, static_cast<uint64_t>(V) * H * 4, &why))
       return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
@@ -661,14 +672,24 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
   h->timeout_ns = static_cast<uint64_t>(cfg->timeout_ms > 0 ? cfg->timeout_ms : 2000) * 1000000ull;
   DeviceGuard g(h->device);
   if (cfg->dtype == FLCE_DTYPE_BF16) {
-    h->pair_clusters = umma_pair_max_clusters();
-    if (cfg->cta_pair == FLCE_CTA_PAIR && h->pair_clusters <= 0) {
-      delete h;
-      return FLCE_ERR_UNSUPPORTED;
+    const int group = cta_group_size(cfg);
+    if (group == 4) {
+      h->quad_clusters = umma_quad_max_clusters();
+      if (h->quad_clusters <= 0) {
+        delete h;
+        return FLCE_ERR_UNSUPPORTED;
+      }
+      h->use_quad = true;
+    } else if (group == 2) {
+      h->pair_clusters = umma_pair_max_clusters();
+      if (cfg->cta_pair == FLCE_CTA_PAIR && h->pair_clusters <= 0) {
+        delete h;
+        return FLCE_ERR_UNSUPPORTED;
+      }
+      h->use_pair = h->pair_clusters > 0;
     }
-    h->use_pair = wants_pair(cfg) && h->pair_clusters > 0;
     // the handle's plans follow the tile shape it actually runs
-    h->cfg.cta_pair = h->use_pair ? FLCE_CTA_PAIR : FLCE_CTA_SINGLE;
+    h->cfg.cta_pair = h->use_quad ? FLCE_CTA_QUAD : h->use_pair ? FLCE_CTA_PAIR : FLCE_CTA_SINGLE;
   }
   if (cudaMallocHost(&h->host_ctrl, kCtrlWords * 4) != cudaSuccess) {
     cudaGetLastError();
@@ -823,7 +844,7 @@ flce_status flce_check_gemm(flce_handle_t h, int32_t a_mn_major, int32_t b_mn_ma
   bool ok = a_mn_major ? map_bf16_2d(&ma, A, M, K, M * 2, 64, 64, &why)
                        : map_bf16_2d(&ma, A, K, M, K * 2, 64, 128, &why);
   ok = ok && (b_mn_major ? map_bf16_2d(&mb, B, N, K, N * 2, 64, 64, &why)
-                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, h->use_pair ? 128 : 256, &why));
+                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, h->use_quad ? 64 : h->use_pair ? 128 : 256, &why));
   ok = ok && map_f32_3d(&mc, C, N, M, 1, N * 4, static_cast<uint64_t>(M) * N * 4, &why);
   if (!ok) return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
   UmmaArgs a{};

@@ -72,6 +72,11 @@ cudaError_t launch_umma(int kind, const CUtensorMap& a, const CUtensorMap& b, co
 cudaError_t launch_umma_pair(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                              const UmmaArgs& args, int pairs, cudaStream_t s);
 int umma_pair_max_clusters();
+// Two CTA pairs per cluster sharing B through multicast: 512 x 256 tiles;
+// num_m counts 512-row tiles; B maps of K-major operands use a 64 x 64 box
+cudaError_t launch_umma_quad(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                             const UmmaArgs& args, int quads, cudaStream_t s);
+int umma_quad_max_clusters();
 
 // The dx and dW GEMMs of one chunk in one CTA-pair launch: problem 0 = dx
 // (A K-major), problem 1 = dW (A MN-major); B MN-major, fp32 epilogue in both.

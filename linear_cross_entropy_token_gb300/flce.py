@@ -21,7 +21,7 @@ STATUS = {0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3:
           4: "FLCE_ERR_BAD_TARGET", 5: "FLCE_ERR_TIMEOUT", 6: "FLCE_ERR_CUDA"}
 DTYPE_BF16, DTYPE_FP32 = 0, 1
 DLOGITS = {"auto": 0, "inplace": 1, "recompute": 2}
-CTA = {"auto": 0, "single": 1, "pair": 2}
+CTA = {"auto": 0, "single": 1, "pair": 2, "quad": 3}
 BACKWARD = {"auto": 0, "separate": 1, "one_launch": 2}
 KERNEL_KINDS = ["count_valid", "gemm_logits_lse", "lse_combine", "dlogits_inplace",
                 "gemm_dlogits_recompute", "gemm_dx", "dx_split_reduce", "gemm_dw",

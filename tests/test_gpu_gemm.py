@@ -8,7 +8,7 @@ import torch
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=["single", "pair"])
+@pytest.fixture(scope="module", params=["single", "pair", "quad"])
 def handle(request):
     from linear_cross_entropy_token_gb300 import FLCE
     h = FLCE("bf16", 0, cta=request.param)
