@@ -170,6 +170,12 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg);
  * Waits for the handle's outstanding work first. NULL is ignored. */
 void flce_destroy(flce_handle_t h);
 
+/* Workspace bytes flce_forward_backward would need for this call on handle
+ * h: the planned workspace of flce_make_plan with the handle's config and
+ * its device's SM count. Host only. Returns 0 when the call cannot be planned
+ * (NULL handle, bad size, budget too small); flce_last_error then says why. */
+uint64_t flce_workspace_bytes(flce_handle_t h, int64_t N, int64_t H, int64_t V, int64_t chunk);
+
 /* Give the handle caller-owned device memory as its workspace (at least
  * flce_plan.workspace_bytes for the calls that follow; NULL/0 returns to
  * library-allocated workspace). The memory must stay valid until the handle

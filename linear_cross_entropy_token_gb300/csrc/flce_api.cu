@@ -823,6 +823,18 @@ void flce_profile_reset(flce_handle_t h) {
 
 int64_t flce_launch_count(flce_handle_t h) { return h ? h->launches : 0; }
 
+uint64_t flce_workspace_bytes(flce_handle_t h, int64_t N, int64_t H, int64_t V, int64_t chunk) {
+  if (!h) return 0;
+  h->err.clear();
+  flce_plan p;
+  std::string why;
+  if (plan_impl(&h->cfg, N, H, V, chunk, h->num_sms, &p, &why) != FLCE_OK) {
+    h->err = why;
+    return 0;
+  }
+  return p.workspace_bytes;
+}
+
 const char* flce_last_error(flce_handle_t h) { return h ? h->err.c_str() : "null handle"; }
 
 flce_status flce_check_gemm(flce_handle_t h, int32_t a_mn_major, int32_t b_mn_major, const void* A,

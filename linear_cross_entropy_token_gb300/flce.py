@@ -88,6 +88,7 @@ def load() -> ctypes.CDLL:
         "flce_profile_reset": (None, [vp]),
         "flce_kernel_name": (ctypes.c_char_p, [i32]),
         "flce_launch_count": (i64, [vp]),
+        "flce_workspace_bytes": (u64, [vp, i64, i64, i64, i64]),
         "flce_last_error": (ctypes.c_char_p, [vp]),
         "flce_check_gemm": (i32, [vp, i32, i32, vp, vp, vp, i64, i64, i64, vp]),
         "flce_check_wait_timeout": (i32, [vp, u32, vp]),
@@ -223,6 +224,16 @@ class FLCE:
         p = Plan()
         self._check(self.lib.flce_last_plan(self.h, ctypes.byref(p)), "flce_last_plan")
         return p.as_dict()
+
+    def workspace_bytes(self, N: int, H: int, V: int, chunk: int = 0) -> int:
+        """Device workspace a call of these sizes needs on this handle."""
+        n = int(self.lib.flce_workspace_bytes(self.h, N, H, V, chunk))
+        if n == 0:
+            p = Plan()
+            st = self.lib.flce_make_plan(ctypes.byref(self.cfg), N, H, V, chunk, 0, ctypes.byref(p))
+            raise FlceError(st if st != FLCE_OK else 1, "flce_workspace_bytes: " +
+                            self.lib.flce_last_error(self.h).decode())
+        return n
 
     def set_workspace(self, buf) -> None:
         ptr = buf.data_ptr() if buf is not None else None

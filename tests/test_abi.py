@@ -57,6 +57,7 @@ def test_null_handle_calls_fail_cleanly(lib):
     assert lib.flce_forward_backward(None, None, None, None, 1, 8, 8, -100, 0, ctypes.byref(loss),
                                      None, None, None) == 1
     assert lib.flce_launch_count(None) == 0
+    assert lib.flce_workspace_bytes(None, 16, 8, 8, 0) == 0
     assert lib.flce_last_error(None) == b"null handle"
     lib.flce_destroy(None)
 

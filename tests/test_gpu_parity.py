@@ -226,6 +226,24 @@ def test_host_buffer_entry_point(bf16):
     assert_parity(res, _oracle(w), "bf16")
 
 
+def test_workspace_bytes_matches_the_call(bf16):
+    """flce_workspace_bytes on a handle predicts the workspace of the plan the
+    next call runs with, and reports a budget that cannot hold one chunk."""
+    from linear_cross_entropy_token_gb300 import FLCE, FlceError
+    w = workloads.generate(workloads.custom(1000, 256, 4099, "bf16", ignore_frac=0.1, seed=13))
+    for chunk in (0, 300):
+        n = bf16.workspace_bytes(1000, 256, 4099, chunk)
+        run(bf16, w, chunk=chunk)
+        assert n == bf16.last_plan()["workspace_bytes"]
+    tiny = FLCE("bf16", 0, hbm_budget_bytes=1 << 20)
+    try:
+        with pytest.raises(FlceError) as e:
+            tiny.workspace_bytes(16384, 4096, 128256)
+        assert e.value.status_name == "FLCE_ERR_BUDGET"
+    finally:
+        tiny.close()
+
+
 def test_caller_workspace(bf16):
     from linear_cross_entropy_token_gb300 import FLCE, FlceError, plan
     w = workloads.generate(workloads.custom(500, 64, 1000, "bf16", seed=12))
