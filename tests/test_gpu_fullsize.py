@@ -149,3 +149,27 @@ def test_long_context_sampled_and_memory():
         _check(h, w, ref)
     finally:
         h.close()
+
+
+@pytest.mark.parametrize("N,H,V,budget_gib", [
+    # the largest chunk the planner takes (32768 tokens) over a 262k-entry
+    # vocabulary in one chunk: the chunk buffer holds 8.6e9 logits, so every
+    # offset into it needs 64 bits
+    (32768, 512, 262147, 24),
+    # a 16384-wide hidden state: 256 k-blocks per logits tile, 64 hidden
+    # tiles across dx and dW
+    (4096, 16384, 50257, 0),
+])
+def test_maximum_sizes(N, H, V, budget_gib):
+    from linear_cross_entropy_token_gb300 import FLCE
+    w = workloads.generate(workloads.custom(N, H, V, "bf16", targets="zipf", ignore_frac=0.05,
+                                            seed=N + H))
+    ref = Ref(w)
+    h = FLCE("bf16", 0, hbm_budget_bytes=budget_gib * GiB)
+    try:
+        plan = _check(h, w, ref)
+        if budget_gib:
+            assert plan["chunk"] == N and plan["num_chunks"] == 1
+            assert plan["chunk"] * plan["ldv"] > (1 << 33)
+    finally:
+        h.close()
