@@ -6,7 +6,7 @@ cross-entropy of x·Wᵀ over non-ignored tokens with dx and dW, without ever
 holding the N x V logits.
 """
 from .flce import (FLCE, FlceError, KERNEL_KINDS, forward_backward, header_functions, load,
-                   plan)
+                   loss_static, plan)
 
 __all__ = ["FLCE", "FlceError", "KERNEL_KINDS", "forward_backward", "header_functions", "load",
-           "plan"]
+           "loss_static", "plan"]
