@@ -207,7 +207,9 @@ def run_reference(args, ws, rank):
     import workloads
     w = workloads.make(args.config)
     Wd = w.W_f64()
-    _, n, dt, cores = oracle_sample_rate(w, target_s=min(args.cpu_seconds, 6.0))
+    # each step a sample sized so that warm-up plus timed steps take ~90 s
+    per_step = max(0.2, min(args.cpu_seconds, 6.0, 90.0 / max(1, args.steps + args.warmup)))
+    _, n, dt, cores = oracle_sample_rate(w, target_s=per_step)
     xs = w.x_f64(np.arange(n))
     ts = w.t[:n]
     for _ in range(args.warmup):
