@@ -89,6 +89,11 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partials, int voca
 // columns of one token row (blockIdx.y); each thread loads its four 16-byte
 // vectors before computing, to keep more bytes in flight.
 //
+// Almost every vector holds neither the target column nor the end of the
+// vocabulary; those take a short path that folds 1/n_valid into the exponent,
+// d = 2^(y·log2 e - (lse - m_s)·log2 e - log2 n_valid). Ignored rows are
+// written as zeros without being read.
+//
 // The target column's entry, about -1/n_valid, is stored in bf16 with a 2^-9
 // relative error; dx = dlogits·W would multiply that error by the part of W
 // common to all rows. Its exact fp32 rounding error goes to dcorr[row] so the
@@ -102,12 +107,21 @@ __global__ void __launch_bounds__(256) dlogits_bf16_kernel(
   const int r = blockIdx.y;
   const int64_t tg = t[r];
   const uint32_t nv = ctrl[kCtrlNValid];
-  const bool valid = tg != ignore_index;
-  const float scale = (valid && nv > 0) ? 1.0f / static_cast<float>(nv) : 0.f;
-  const float l = lse[r];
-  const float2* prow = partials + static_cast<size_t>(r) * vocab_tiles;
+  const bool live = tg != ignore_index && nv > 0;
   __nv_bfloat16* row = buf + static_cast<size_t>(r) * ldv;
   const int64_t base = static_cast<int64_t>(blockIdx.x) * (blockDim.x * 8 * kDlogitsVecs);
+  if (!live) {
+#pragma unroll
+    for (int i = 0; i < kDlogitsVecs; ++i) {
+      const int64_t c0 = base + (static_cast<int64_t>(i) * blockDim.x + threadIdx.x) * 8;
+      if (c0 < ldv) *reinterpret_cast<uint4*>(row + c0) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
+  const float scale = 1.0f / static_cast<float>(nv);
+  const float lg_nv = __log2f(static_cast<float>(nv));
+  const float l = lse[r];
+  const float2* prow = partials + static_cast<size_t>(r) * vocab_tiles;
   uint4 v[kDlogitsVecs];
 #pragma unroll
   for (int i = 0; i < kDlogitsVecs; ++i) {
@@ -121,21 +135,33 @@ __global__ void __launch_bounds__(256) dlogits_bf16_kernel(
     // 8 columns never straddle a vocab tile
     const float ll = (l - prow[c0 / kVocabTile].x) * kLog2e;
     uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    if (c0 + 8 <= V && (tg < c0 || tg >= c0 + 8)) {
+      const float nl = ll + lg_nv;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w[q]);
-      const float2 f = __bfloat1622float2(h);
-      const int64_t j0 = c0 + 2 * q;
-      float d0 = ex2_approx(fmaf(f.x, kLog2e, -ll));
-      float d1 = ex2_approx(fmaf(f.y, kLog2e, -ll));
-      if (j0 == tg) d0 -= 1.f;
-      if (j0 + 1 == tg) d1 -= 1.f;
-      d0 = (j0 < V) ? d0 * scale : 0.f;
-      d1 = (j0 + 1 < V) ? d1 * scale : 0.f;
-      h = __floats2bfloat162_rn(d0, d1);
-      if (j0 == tg) dcorr[r] = d0 - __low2float(h);
-      if (j0 + 1 == tg) dcorr[r] = d1 - __high2float(h);
-      w[q] = *reinterpret_cast<uint32_t*>(&h);
+      for (int q = 0; q < 4; ++q) {
+        const float f0 = __uint_as_float(w[q] << 16);
+        const float f1 = __uint_as_float(w[q] & 0xFFFF0000u);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(ex2_approx(fmaf(f0, kLog2e, -nl)),
+                                                       ex2_approx(fmaf(f1, kLog2e, -nl)));
+        w[q] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w[q]);
+        const float2 f = __bfloat1622float2(h);
+        const int64_t j0 = c0 + 2 * q;
+        float d0 = ex2_approx(fmaf(f.x, kLog2e, -ll));
+        float d1 = ex2_approx(fmaf(f.y, kLog2e, -ll));
+        if (j0 == tg) d0 -= 1.f;
+        if (j0 + 1 == tg) d1 -= 1.f;
+        d0 = (j0 < V) ? d0 * scale : 0.f;
+        d1 = (j0 + 1 < V) ? d1 * scale : 0.f;
+        h = __floats2bfloat162_rn(d0, d1);
+        if (j0 == tg) dcorr[r] = d0 - __low2float(h);
+        if (j0 + 1 == tg) dcorr[r] = d1 - __high2float(h);
+        w[q] = *reinterpret_cast<uint32_t*>(&h);
+      }
     }
     *reinterpret_cast<uint4*>(row + c0) = make_uint4(w[0], w[1], w[2], w[3]);
   }
