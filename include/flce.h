@@ -30,7 +30,10 @@
  *   - Status codes, never exceptions or aborts. On failure, flce_last_error()
  *     gives a one-line reason.
  *   - Device pointers are CUDA device addresses on the handle's device,
- *     contiguous row-major, 16-byte aligned. Host pointers are ordinary host
+ *     contiguous row-major, 16-byte aligned. The checks (INVALID_ARG when
+ *     they fail): bf16 x, W, dx, dW 16-byte aligned; fp32 ones 4-byte; t
+ *     8-byte. Sizes cannot be checked against the buffers: the caller
+ *     passes buffers of the stated shapes. Host pointers are ordinary host
  *     memory (page-locked memory makes the copies asynchronous).
  *   - "stream" is a cudaStream_t passed as void*; NULL is the legacy default
  *     stream. All device work of a call is ordered on that stream.

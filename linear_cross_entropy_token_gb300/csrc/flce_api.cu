@@ -416,10 +416,15 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
   if (!W || !loss || !dW || (N > 0 && (!x || !t || !dx)))
     return fail(h, FLCE_ERR_INVALID_ARG, "null pointer argument");
   const bool bf16 = h->cfg.dtype == FLCE_DTYPE_BF16;
+  if (N > 0 && (reinterpret_cast<uintptr_t>(t) & 7u))
+    return fail(h, FLCE_ERR_INVALID_ARG, "t must be 8-byte aligned");
   if (bf16) {
     if (H % 8 != 0) return fail(h, FLCE_ERR_INVALID_ARG, "bf16 needs H %% 8 == 0 (H = %lld)", (long long)H);
     if (!aligned16(x) || !aligned16(W) || !aligned16(dW) || (N > 0 && !aligned16(dx)))
       return fail(h, FLCE_ERR_INVALID_ARG, "x, W, dx and dW must be 16-byte aligned");
+  } else if ((reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(dW) |
+              (N > 0 ? reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(dx) : 0)) & 3u) {
+    return fail(h, FLCE_ERR_INVALID_ARG, "x, W, dx and dW must be 4-byte aligned");
   }
   flce_plan p;
   std::string why;

@@ -96,6 +96,8 @@ extern "C" flce_status flce_loss_static(const void* x, const void* W, const int6
   if (N < 0 || H < 8 || V < 1 || H % 8 != 0 || N > (1ll << 31) - 1 || V > (1ll << 31) - 1)
     return FLCE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(W)) & 15u) return FLCE_ERR_INVALID_ARG;
+  if (N > 0 && ((reinterpret_cast<uintptr_t>(t) & 7u) || (reinterpret_cast<uintptr_t>(token_loss) & 3u)))
+    return FLCE_ERR_INVALID_ARG;
   const int64_t vt = (V + kVocabTile - 1) / kVocabTile;
   // tokens per chunk: up to 4096, a multiple of 128, whatever fits the scratch
   int64_t C = 0;

@@ -129,6 +129,35 @@ def plan(N: int, H: int, V: int, dtype: str = "bf16", chunk: int = 0, hbm_budget
     return p.as_dict()
 
 
+def check_call_tensors(x, W, t, dx, dW, dtype, in_device, out_device) -> None:
+    """Shapes, dtypes, devices and contiguity of one call's tensors. The C ABI
+    takes bare pointers and sizes, so a mismatch left unchecked here would
+    become an out-of-bounds access there. x (N, H) and W (V, H) of `dtype` and
+    t (N,) int64 on in_device; dx (N, H) of `dtype` and dW (V, H) float32 on
+    out_device, when given. Raises ValueError."""
+    import torch
+    if x.dim() != 2 or W.dim() != 2 or t.dim() != 1:
+        raise ValueError("x and W must be 2-D, t 1-D")
+    N, H = x.shape
+    V = W.shape[0]
+    if W.shape[1] != H:
+        raise ValueError(f"W has {W.shape[1]} columns, x has {H}")
+    if t.shape[0] != N:
+        raise ValueError(f"t has {t.shape[0]} entries, x has {N} rows")
+    if x.dtype != dtype or W.dtype != dtype or t.dtype != torch.int64:
+        raise ValueError(f"x and W must be {dtype}, t must be int64")
+    for name, ten in (("x", x), ("W", W), ("t", t)):
+        if ten.device != in_device or not ten.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor on {in_device}")
+    for name, ten, shape, dt in (("dx", dx, (N, H), dtype), ("dW", dW, (V, H), torch.float32)):
+        if ten is None:
+            continue
+        if tuple(ten.shape) != shape or ten.dtype != dt:
+            raise ValueError(f"{name} must be {dt} of shape {shape}")
+        if ten.device != out_device or not ten.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor on {out_device}")
+
+
 def _stream_ptr(device) -> int:
     import torch
     return torch.cuda.current_stream(device).cuda_stream
@@ -175,14 +204,10 @@ class FLCE:
                          dx=None, dW=None):
         """loss (float), dx (like x), dW (fp32, V x H) for device tensors x, W, t."""
         import torch
+        dev = torch.device("cuda", self.device)
+        check_call_tensors(x, W, t, dx, dW, self._torch_dtype(), dev, dev)
         N, H = x.shape
         V = W.shape[0]
-        dev = torch.device("cuda", self.device)
-        for name, ten in (("x", x), ("W", W), ("t", t)):
-            if ten.device != dev or not ten.is_contiguous():
-                raise ValueError(f"{name} must be a contiguous tensor on {dev}")
-        if x.dtype != self._torch_dtype() or W.dtype != self._torch_dtype() or t.dtype != torch.int64:
-            raise ValueError("x and W must have the handle's dtype, t must be int64")
         if dx is None:
             dx = torch.empty_like(x)
         if dW is None:
@@ -198,9 +223,11 @@ class FLCE:
                               chunk: int = 0, dx=None, dW=None):
         """Same, with x, W, t in host memory (pinned for asynchronous copies)."""
         import torch
+        dev = torch.device("cuda", self.device)
+        check_call_tensors(x_host, W_host, t_host, dx, dW, self._torch_dtype(), torch.device("cpu"),
+                           dev)
         N, H = x_host.shape
         V = W_host.shape[0]
-        dev = torch.device("cuda", self.device)
         if dx is None:
             dx = torch.empty((N, H), dtype=self._torch_dtype(), device=dev)
         if dW is None:
@@ -261,6 +288,10 @@ class FLCE:
 
     def check_gemm(self, A, B, a_mn_major: bool, b_mn_major: bool, M: int, N: int, K: int):
         import torch
+        if (A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or not A.is_contiguous()
+                or not B.is_contiguous() or A.numel() != M * K or B.numel() != N * K
+                or A.device != torch.device("cuda", self.device) or B.device != A.device):
+            raise ValueError("A (M*K) and B (N*K) must be contiguous bf16 on the handle's device")
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
         st = self.lib.flce_check_gemm(self.h, int(a_mn_major), int(b_mn_major), A.data_ptr(),
                                       B.data_ptr(), C.data_ptr(), M, N, K, _stream_ptr(A.device))
@@ -279,12 +310,14 @@ def loss_static(x, W, t, ignore_index: int = -100, token_loss=None):
     all come from their own allocator. Returns (loss, token_loss)."""
     import torch
     lib = load()
+    check_call_tensors(x, W, t, None, None, torch.bfloat16, x.device, x.device)
     N, H = x.shape
     V = W.shape[0]
-    if x.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or t.dtype != torch.int64:
-        raise ValueError("x and W must be bf16, t int64")
     if token_loss is None:
         token_loss = torch.empty(N, dtype=torch.float32, device=x.device)
+    elif (tuple(token_loss.shape) != (N,) or token_loss.dtype != torch.float32
+          or token_loss.device != x.device or not token_loss.is_contiguous()):
+        raise ValueError(f"token_loss must be contiguous float32 of shape ({N},) on {x.device}")
     loss = ctypes.c_float(0.0)
     with torch.cuda.device(x.device):
         st = lib.flce_loss_static(x.data_ptr(), W.data_ptr(), t.data_ptr(), N, H, V, ignore_index,

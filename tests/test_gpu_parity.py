@@ -244,6 +244,35 @@ def test_workspace_bytes_matches_the_call(bf16):
         tiny.close()
 
 
+def test_misaligned_or_mismatched_arguments_are_refused(bf16):
+    """The C ABI refuses pointers its vector loads and TMA maps cannot take
+    (before any launch), and the binding refuses tensors whose shapes do not
+    fit together."""
+    import ctypes
+    w = workloads.generate(workloads.custom(64, 64, 300, "bf16", seed=14))
+    x, W, t = device_inputs(w)
+    dx = torch.empty_like(x)
+    dW = torch.empty(W.shape, dtype=torch.float32, device="cuda")
+    raw = torch.zeros(64 * 8 + 16, dtype=torch.uint8, device="cuda")
+    loss = ctypes.c_float()
+    s = torch.cuda.current_stream().cuda_stream
+    fb = bf16.lib.flce_forward_backward
+    assert fb(bf16.h, x.data_ptr(), W.data_ptr(), raw.data_ptr() + 4, 64, 64, 300, -100, 0,
+              ctypes.byref(loss), dx.data_ptr(), dW.data_ptr(), s) == 1
+    assert fb(bf16.h, x.data_ptr() + 8, W.data_ptr(), t.data_ptr(), 63, 64, 300, -100, 0,
+              ctypes.byref(loss), dx.data_ptr(), dW.data_ptr(), s) == 1
+    assert fb(bf16.h, x.data_ptr(), W.data_ptr(), t.data_ptr(), 64, 60, 300, -100, 0,
+              ctypes.byref(loss), dx.data_ptr(), dW.data_ptr(), s) == 1   # H % 8 != 0
+    with pytest.raises(ValueError):
+        bf16.forward_backward(x, W[:, :32].contiguous(), t)
+    with pytest.raises(ValueError):
+        bf16.forward_backward(x, W, t[:63])
+    with pytest.raises(ValueError):
+        bf16.forward_backward(x, W, t, dW=torch.empty(299, 64, device="cuda"))
+    # the handle still works afterwards
+    assert_parity(run(bf16, w), _oracle(w), "bf16")
+
+
 def test_caller_workspace(bf16):
     from linear_cross_entropy_token_gb300 import FLCE, FlceError, plan
     w = workloads.generate(workloads.custom(500, 64, 1000, "bf16", seed=12))
