@@ -217,6 +217,29 @@ flce_status flce_forward_backward_host(flce_handle_t h, const void* x_host,
                                        int64_t ignore_index, int64_t chunk, float* loss,
                                        void* dx, float* dW, void* stream);
 
+/* The host-buffer call, pipelined: flce_submit_host enqueues it and returns
+ * at once with a ticket; flce_wait(ticket) blocks until that call has
+ * finished and gives its loss and status. The copies of x, W and t run on the
+ * library's own copy stream into one of two staging slots, so the copies of
+ * call k+1 overlap the compute of call k on `stream`; the compute still runs
+ * in submission order on `stream`. At most two submissions may be
+ * outstanding (submit returns INVALID_ARG otherwise). dx and dW are written
+ * by the compute in submission order: a caller reusing them for several
+ * submissions reads them after the wait of the call it wants. Host buffers
+ * must stay unchanged until the call's wait returns; page-locked host memory
+ * makes the copies asynchronous. flce_token_losses and flce_last_plan refer to
+ * the most recent submission. The staging takes two buffers of the inputs'
+ * size in device memory.
+ * Errors: submit as flce_forward_backward_host for its arguments, plus
+ * INVALID_ARG when two are outstanding; wait returns the call's status
+ * (BAD_TARGET, TIMEOUT, CUDA) or INVALID_ARG for a ticket that is not
+ * outstanding. */
+flce_status flce_submit_host(flce_handle_t h, const void* x_host, const void* W_host,
+                             const int64_t* t_host, int64_t N, int64_t H, int64_t V,
+                             int64_t ignore_index, int64_t chunk, void* dx, float* dW,
+                             void* stream, uint64_t* ticket);
+flce_status flce_wait(flce_handle_t h, uint64_t ticket, float* loss);
+
 /* Copy the per-token losses of the last call (N fp32, 0 for ignored tokens)
  * into device memory out. N must equal the last call's N. Errors: INVALID_ARG. */
 flce_status flce_token_losses(flce_handle_t h, float* out, int64_t N, void* stream);

@@ -220,6 +220,20 @@ struct flce_handle_s {
   void* stage = nullptr;
   uint64_t stage_bytes = 0;
   uint32_t* host_ctrl = nullptr;  // pinned
+  // pipelined host-buffer entry: two staging slots, copies on their own stream
+  struct Slot {
+    void* stage = nullptr;
+    uint64_t bytes = 0;
+    cudaEvent_t copied = nullptr;  // the slot's inputs have landed (copy stream)
+    cudaEvent_t freed = nullptr;   // the call that read the slot has finished with it
+    cudaEvent_t done = nullptr;    // the call's control words are in host memory
+    uint32_t* host = nullptr;      // pinned copy of the control words
+    uint64_t ticket = 0;
+    bool pending = false;
+  };
+  Slot slots[2];
+  cudaStream_t copy_stream = nullptr;
+  uint64_t next_ticket = 1;
   flce_plan last_plan{};
   int64_t last_N = -1;
   uint64_t token_loss_off = 0;
@@ -376,12 +390,10 @@ bool map_f32_3d(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, uint64
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-flce_status read_back(flce_handle_t h, uint32_t* ctrl_dev, cudaStream_t s, float* loss) {
-  cudaError_t e = cudaMemcpyAsync(h->host_ctrl, ctrl_dev, 4 * 4, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "read-back: %s", cudaGetErrorString(e));
-  const uint32_t code = h->host_ctrl[kCtrlError];
-  if (loss) std::memcpy(loss, &h->host_ctrl[kCtrlLoss], 4);
+// The status and loss of a finished call from its control words in host memory.
+flce_status decode_ctrl(flce_handle_t h, const uint32_t* hc, float* loss) {
+  const uint32_t code = hc[kCtrlError];
+  if (loss) std::memcpy(loss, &hc[kCtrlLoss], 4);
   if (code == FLCE_ERR_BAD_TARGET)
     return fail(h, FLCE_ERR_BAD_TARGET, "a target is outside [0, V) and is not ignore_index");
   if (code == FLCE_ERR_TIMEOUT)
@@ -389,6 +401,13 @@ flce_status read_back(flce_handle_t h, uint32_t* ctrl_dev, cudaStream_t s, float
                 static_cast<unsigned long long>(h->timeout_ns));
   if (code != 0) return fail(h, FLCE_ERR_CUDA, "device error word %u", code);
   return FLCE_OK;
+}
+
+flce_status read_back(flce_handle_t h, uint32_t* ctrl_dev, cudaStream_t s, float* loss) {
+  cudaError_t e = cudaMemcpyAsync(h->host_ctrl, ctrl_dev, 4 * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "read-back: %s", cudaGetErrorString(e));
+  return decode_ctrl(h, h->host_ctrl, loss);
 }
 
 // One GEMM on the handle's tile shape; sets num_m from the M extent and the
@@ -410,10 +429,54 @@ cudaError_t launch_gemm(flce_handle_t h, int kind, const CUtensorMap& a, const C
   return launch_umma(kind, a, b, o, args, std::min(units, h->num_sms), s);
 }
 
-flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t* t, int64_t N,
-                   int64_t H, int64_t V, int64_t ignore_index, int64_t chunk, float* loss, void* dx,
-                   float* dW, cudaStream_t s) {
-  if (!W || !loss || !dW || (N > 0 && (!x || !t || !dx)))
+// Device copies of a call's host inputs, in one buffer (grown as needed).
+struct Staged {
+  const void* x = nullptr;
+  const void* W = nullptr;
+  const int64_t* t = nullptr;
+};
+
+flce_status stage_inputs(flce_handle_t h, void** buf, uint64_t* buf_bytes, const void* x_host,
+                         const void* W_host, const int64_t* t_host, int64_t N, int64_t H, int64_t V,
+                         cudaStream_t s, Staged* out) {
+  const uint64_t es = h->cfg.dtype == FLCE_DTYPE_BF16 ? 2 : 4;
+  const uint64_t xb = static_cast<uint64_t>(N) * H * es, wb = static_cast<uint64_t>(V) * H * es;
+  const uint64_t tb = static_cast<uint64_t>(N) * 8;
+  const uint64_t ox = 0, ow = align_up(xb, kAlign), ot = ow + align_up(wb, kAlign);
+  const uint64_t need = ot + align_up(std::max<uint64_t>(tb, 8), kAlign);
+  if (*buf_bytes < need) {
+    if (*buf) {
+      cudaDeviceSynchronize();
+      cudaFree(*buf);
+      *buf = nullptr;
+      *buf_bytes = 0;
+    }
+    if (cudaMalloc(buf, need) != cudaSuccess) {
+      cudaGetLastError();
+      *buf = nullptr;
+      return fail(h, FLCE_ERR_BUDGET, "cudaMalloc of %llu staging bytes failed",
+                  static_cast<unsigned long long>(need));
+    }
+    *buf_bytes = need;
+  }
+  uint8_t* st = static_cast<uint8_t*>(*buf);
+  cudaError_t e = cudaSuccess;
+  if (xb) e = cudaMemcpyAsync(st + ox, x_host, xb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(st + ow, W_host, wb, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && tb) e = cudaMemcpyAsync(st + ot, t_host, tb, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "staging copy: %s", cudaGetErrorString(e));
+  out->x = st + ox;
+  out->W = st + ow;
+  out->t = reinterpret_cast<const int64_t*>(st + ot);
+  return FLCE_OK;
+}
+
+// Everything of one call up to its control words on the device (*ctrl_out):
+// the result is read from them once the stream gets there.
+flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int64_t* t, int64_t N,
+                       int64_t H, int64_t V, int64_t ignore_index, int64_t chunk, void* dx,
+                       float* dW, cudaStream_t s, uint32_t** ctrl_out) {
+  if (!W || !dW || (N > 0 && (!x || !t || !dx)))
     return fail(h, FLCE_ERR_INVALID_ARG, "null pointer argument");
   const bool bf16 = h->cfg.dtype == FLCE_DTYPE_BF16;
   if (N > 0 && (reinterpret_cast<uintptr_t>(t) & 7u))
@@ -451,7 +514,8 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
   if (N == 0) {
     e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * 4, s);
     if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
-    return read_back(h, ctrl, s, loss);
+    *ctrl_out = ctrl;
+    return FLCE_OK;
   }
   FLCE_LAUNCH(FLCE_K_COUNT_VALID, 0.0, 8.0 * N, launch_count_valid(t, N, V, ignore_index, ctrl, s));
 
@@ -608,6 +672,17 @@ flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t*
     }
   }
   FLCE_LAUNCH(FLCE_K_LOSS_FINALIZE, 0.0, 4.0 * N, launch_loss_finalize(token_loss, N, ctrl, s));
+  *ctrl_out = ctrl;
+  return FLCE_OK;
+}
+
+flce_status run_fb(flce_handle_t h, const void* x, const void* W, const int64_t* t, int64_t N,
+                   int64_t H, int64_t V, int64_t ignore_index, int64_t chunk, float* loss, void* dx,
+                   float* dW, cudaStream_t s) {
+  if (!loss) return fail(h, FLCE_ERR_INVALID_ARG, "null pointer argument");
+  uint32_t* ctrl = nullptr;
+  const flce_status st = enqueue_fb(h, x, W, t, N, H, V, ignore_index, chunk, dx, dW, s, &ctrl);
+  if (st != FLCE_OK) return st;
   return read_back(h, ctrl, s, loss);
 }
 
@@ -717,6 +792,14 @@ void flce_destroy(flce_handle_t h) {
     if (h->ws && !h->ws_external) cudaFree(h->ws);
     if (h->stage) cudaFree(h->stage);
     if (h->host_ctrl) cudaFreeHost(h->host_ctrl);
+    for (auto& sl : h->slots) {
+      if (sl.stage) cudaFree(sl.stage);
+      if (sl.host) cudaFreeHost(sl.host);
+      if (sl.copied) cudaEventDestroy(sl.copied);
+      if (sl.freed) cudaEventDestroy(sl.freed);
+      if (sl.done) cudaEventDestroy(sl.done);
+    }
+    if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   }
   delete h;
 }
@@ -757,34 +840,71 @@ flce_status flce_forward_backward_host(flce_handle_t h, const void* x_host, cons
     return fail(h, FLCE_ERR_INVALID_ARG, "null host pointer or bad size");
   DeviceGuard g(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const uint64_t es = h->cfg.dtype == FLCE_DTYPE_BF16 ? 2 : 4;
-  const uint64_t xb = static_cast<uint64_t>(N) * H * es, wb = static_cast<uint64_t>(V) * H * es;
-  const uint64_t tb = static_cast<uint64_t>(N) * 8;
-  const uint64_t ox = 0, ow = align_up(xb, kAlign), ot = ow + align_up(wb, kAlign);
-  const uint64_t need = ot + align_up(std::max<uint64_t>(tb, 8), kAlign);
-  if (h->stage_bytes < need) {
-    if (h->stage) {
-      cudaDeviceSynchronize();
-      cudaFree(h->stage);
-      h->stage = nullptr;
-      h->stage_bytes = 0;
-    }
-    if (cudaMalloc(&h->stage, need) != cudaSuccess) {
-      cudaGetLastError();
-      h->stage = nullptr;
-      return fail(h, FLCE_ERR_BUDGET, "cudaMalloc of %llu staging bytes failed",
-                  static_cast<unsigned long long>(need));
-    }
-    h->stage_bytes = need;
-  }
-  uint8_t* st = static_cast<uint8_t*>(h->stage);
+  Staged in;
+  flce_status st = stage_inputs(h, &h->stage, &h->stage_bytes, x_host, W_host, t_host, N, H, V, s, &in);
+  if (st != FLCE_OK) return st;
+  return run_fb(h, in.x, in.W, in.t, N, H, V, ignore_index, chunk, loss, dx, dW, s);
+}
+
+flce_status flce_submit_host(flce_handle_t h, const void* x_host, const void* W_host,
+                             const int64_t* t_host, int64_t N, int64_t H, int64_t V,
+                             int64_t ignore_index, int64_t chunk, void* dx, float* dW, void* stream,
+                             uint64_t* ticket) {
+  if (!h || !ticket) return FLCE_ERR_INVALID_ARG;
+  h->err.clear();
+  *ticket = 0;
+  if (!x_host || !W_host || !t_host || N < 0 || H < 1 || V < 1)
+    return fail(h, FLCE_ERR_INVALID_ARG, "null host pointer or bad size");
+  DeviceGuard g(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  flce_handle_s::Slot& sl = h->slots[h->next_ticket & 1];
+  if (sl.pending)
+    return fail(h, FLCE_ERR_INVALID_ARG, "two submissions are outstanding: wait for ticket %llu first",
+                static_cast<unsigned long long>(sl.ticket));
   cudaError_t e = cudaSuccess;
-  if (xb) e = cudaMemcpyAsync(st + ox, x_host, xb, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(st + ow, W_host, wb, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess && tb) e = cudaMemcpyAsync(st + ot, t_host, tb, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "staging copy: %s", cudaGetErrorString(e));
-  return run_fb(h, st + ox, st + ow, reinterpret_cast<const int64_t*>(st + ot), N, H, V, ignore_index,
-                chunk, loss, dx, dW, s);
+  if (!h->copy_stream) e = cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess && !sl.copied) e = cudaEventCreateWithFlags(&sl.copied, cudaEventDisableTiming);
+  if (e == cudaSuccess && !sl.freed) e = cudaEventCreateWithFlags(&sl.freed, cudaEventDisableTiming);
+  if (e == cudaSuccess && !sl.done) e = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming);
+  if (e == cudaSuccess && !sl.host)
+    e = cudaHostAlloc(reinterpret_cast<void**>(&sl.host), kCtrlWords * 4, cudaHostAllocDefault);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "submit set-up: %s", cudaGetErrorString(e));
+  // the copies wait only for the call that last read this slot, so they
+  // overlap the call running on the other slot
+  e = cudaStreamWaitEvent(h->copy_stream, sl.freed, 0);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "submit: %s", cudaGetErrorString(e));
+  Staged in;
+  flce_status st =
+      stage_inputs(h, &sl.stage, &sl.bytes, x_host, W_host, t_host, N, H, V, h->copy_stream, &in);
+  if (st != FLCE_OK) return st;
+  e = cudaEventRecord(sl.copied, h->copy_stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, sl.copied, 0);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "submit: %s", cudaGetErrorString(e));
+  uint32_t* ctrl = nullptr;
+  st = enqueue_fb(h, in.x, in.W, in.t, N, H, V, ignore_index, chunk, dx, dW, s, &ctrl);
+  if (st != FLCE_OK) return st;
+  e = cudaEventRecord(sl.freed, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(sl.host, ctrl, kCtrlWords * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaEventRecord(sl.done, s);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "submit: %s", cudaGetErrorString(e));
+  sl.pending = true;
+  sl.ticket = h->next_ticket++;
+  *ticket = sl.ticket;
+  return FLCE_OK;
+}
+
+flce_status flce_wait(flce_handle_t h, uint64_t ticket, float* loss) {
+  if (!h || !loss) return FLCE_ERR_INVALID_ARG;
+  h->err.clear();
+  flce_handle_s::Slot& sl = h->slots[ticket & 1];
+  if (ticket == 0 || !sl.pending || sl.ticket != ticket)
+    return fail(h, FLCE_ERR_INVALID_ARG, "ticket %llu is not outstanding",
+                static_cast<unsigned long long>(ticket));
+  DeviceGuard g(h->device);
+  const cudaError_t e = cudaEventSynchronize(sl.done);
+  sl.pending = false;
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "wait: %s", cudaGetErrorString(e));
+  return decode_ctrl(h, sl.host, loss);
 }
 
 flce_status flce_token_losses(flce_handle_t h, float* out, int64_t N, void* stream) {

@@ -81,6 +81,9 @@ def load() -> ctypes.CDLL:
                                         ctypes.POINTER(ctypes.c_float), vp, vp, vp]),
         "flce_forward_backward_host": (i32, [vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                              ctypes.POINTER(ctypes.c_float), vp, vp, vp]),
+        "flce_submit_host": (i32, [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp,
+                                   ctypes.POINTER(u64)]),
+        "flce_wait": (i32, [vp, u64, ctypes.POINTER(ctypes.c_float)]),
         "flce_token_losses": (i32, [vp, vp, i64, vp]),
         "flce_last_plan": (i32, [vp, ctypes.POINTER(Plan)]),
         "flce_set_profiling": (i32, [vp, i32]),
@@ -239,6 +242,34 @@ class FLCE:
                                                  _stream_ptr(dev))
         self._check(st, "flce_forward_backward_host")
         return loss.value, dx, dW
+
+    def submit_host(self, x_host, W_host, t_host, ignore_index: int = -100, chunk: int = 0,
+                    dx=None, dW=None):
+        """Enqueue the host-buffer call and return (ticket, dx, dW) at once;
+        the copies of this call overlap the compute of the previous one.
+        wait(ticket) gives the loss. At most two may be outstanding."""
+        import torch
+        dev = torch.device("cuda", self.device)
+        check_call_tensors(x_host, W_host, t_host, dx, dW, self._torch_dtype(), torch.device("cpu"),
+                           dev)
+        N, H = x_host.shape
+        V = W_host.shape[0]
+        if dx is None:
+            dx = torch.empty((N, H), dtype=self._torch_dtype(), device=dev)
+        if dW is None:
+            dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+        ticket = ctypes.c_uint64(0)
+        st = self.lib.flce_submit_host(self.h, x_host.data_ptr(), W_host.data_ptr(), t_host.data_ptr(),
+                                       N, H, V, ignore_index, chunk, dx.data_ptr(), dW.data_ptr(),
+                                       _stream_ptr(dev), ctypes.byref(ticket))
+        self._check(st, "flce_submit_host")
+        return ticket.value, dx, dW
+
+    def wait(self, ticket: int) -> float:
+        """Block until the submitted call `ticket` has finished; its loss."""
+        loss = ctypes.c_float(0.0)
+        self._check(self.lib.flce_wait(self.h, ticket, ctypes.byref(loss)), "flce_wait")
+        return loss.value
 
     def token_losses(self, N: int):
         import torch

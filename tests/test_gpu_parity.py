@@ -244,6 +244,32 @@ def test_workspace_bytes_matches_the_call(bf16):
         tiny.close()
 
 
+def test_pipelined_host_submissions(bf16):
+    """submit/wait with two calls in flight: each call's loss and outputs
+    match the oracle on its own inputs. A third submission while two are
+    outstanding, and a wait on a ticket that is not outstanding, are refused."""
+    from linear_cross_entropy_token_gb300 import FlceError
+    ws = [workloads.generate(workloads.custom(600, 128, 3000, "bf16", ignore_frac=0.1, seed=20 + i))
+          for i in range(3)]
+    host = [(torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16).pin_memory(),
+             torch.from_numpy(w.W.view(np.int16)).view(torch.bfloat16).pin_memory(),
+             torch.from_numpy(w.t).pin_memory()) for w in ws]
+    outs = [(torch.empty(600, 128, dtype=torch.bfloat16, device="cuda"),
+             torch.empty(3000, 128, dtype=torch.float32, device="cuda")) for _ in ws]
+    t0, _, _ = bf16.submit_host(*host[0], chunk=256, dx=outs[0][0], dW=outs[0][1])
+    t1, _, _ = bf16.submit_host(*host[1], chunk=256, dx=outs[1][0], dW=outs[1][1])
+    with pytest.raises(FlceError) as e:
+        bf16.submit_host(*host[2], chunk=256, dx=outs[2][0], dW=outs[2][1])
+    assert e.value.status_name == "FLCE_ERR_INVALID_ARG"
+    losses = [bf16.wait(t0)]
+    t2, _, _ = bf16.submit_host(*host[2], chunk=256, dx=outs[2][0], dW=outs[2][1])
+    losses += [bf16.wait(t1), bf16.wait(t2)]
+    with pytest.raises(FlceError):
+        bf16.wait(t2)
+    for w, loss, (dx, dW) in zip(ws, losses, outs):
+        assert_parity({"loss": loss, "dx": to_np64(dx), "dW": to_np64(dW)}, _oracle(w), "bf16")
+
+
 def test_misaligned_or_mismatched_arguments_are_refused(bf16):
     """The C ABI refuses pointers its vector loads and TMA maps cannot take
     (before any launch), and the binding refuses tensors whose shapes do not
