@@ -95,6 +95,18 @@ def aggregate(ws, tokens_per_rank: int, ms_local: float, device=None):
     return ms_max, ws * tokens_per_rank / (ms_max / 1e3)
 
 
+# The pages' own figures for this shape, other hardware: context, not targets.
+PAGE_CONTEXT = {
+    "full_logits_bf16_gb": 4.20,
+    "standard_pytorch_loss_peak_gb": 36.02,
+    "fused_triton_loss_peak_gb": 5.04,
+    "hardware": "A100 (FLCE page, section on memory measured at 16,384 tokens)",
+    "strategies_16b_model_128k_context": {
+        "full logits": "110+ GB, 1.0x throughput", "chunked loss, 8K chunks": "14 GB, 0.85x",
+        "LM-head gradient checkpointing": "4 GB, 0.70x", "fused Triton loss": "6 GB, 1.05x",
+        "hardware": "A100/H100 class, unspecified"},
+}
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -388,6 +400,7 @@ def run_ours(args, ws, rank, local):
         "peak_extra_hbm_gb": plan["workspace_bytes"] / 1e9,
         "peak_extra_hbm_measured_gb": max(0, free0 - free1) / 1e9,
         "full_logits_gb": N * V * 2 / 1e9,
+        "page_context": PAGE_CONTEXT if (N, H, V) == (16384, 4096, 128256) else None,
         "loss": losses[-1],
         "gpu_launches": launches,
         "kernels": kernels,
