@@ -109,6 +109,12 @@ def test_cta_pair_matches_single(bf16_pair):
     (256, 128, 4096, 64, 0.0),       # C < 128 in bf16
     (777, 136, 1000, 256, 0.2),      # H not a multiple of 64 (K tail), V < one 1024-column span
     (130, 64, 300, 0, 0.0),          # everything smaller than one tile along some axis
+    (1, 64, 500, 0, 0.0),            # a single token
+    (300, 8, 1000, 0, 0.1),          # the narrowest hidden size a bf16 row allows (16 bytes)
+    (257, 24, 2000, 128, 0.1),       # H inside the first k-block, N one past a tile
+    (129, 72, 513, 0, 0.0),          # one k-block and a tail; V two past a multiple of 256
+    (200, 64, 1, 0, 0.1),            # one class: every loss and gradient is exactly 0
+    (200, 64, 2, 0, 0.0),            # two classes
 ])
 def test_ragged_shapes(bf16, N, H, V, chunk, ign):
     w = workloads.generate(workloads.custom(N, H, V, "bf16", ignore_frac=ign, seed=N + V))
