@@ -135,7 +135,8 @@ enum {
     FLCE_K_SIMT_GEMM = 9,        /* fp32 path: CUDA-core GEMMs                         */
     FLCE_K_SIMT_TILE_STATS = 10, /* fp32 path: per-vocab-tile max/sum-exp              */
     FLCE_K_GEMM_DX_DW = 11,      /* CTA pairs: the dx and dW GEMMs of a chunk in one launch */
-    FLCE_K_NUM_KINDS = 12
+    FLCE_K_DEVICE_RESULT = 12,   /* loss and n_valid into caller device memory         */
+    FLCE_K_NUM_KINDS = 13
 };
 
 typedef struct flce_kernel_profile {
@@ -206,6 +207,29 @@ flce_status flce_forward_backward(flce_handle_t h, const void* x, const void* W,
                                   const int64_t* t, int64_t N, int64_t H, int64_t V,
                                   int64_t ignore_index, int64_t chunk, float* loss,
                                   void* dx, float* dW, void* stream);
+
+/* The fused forward + backward with no host synchronisation, for streams
+ * under CUDA graph capture and for pipelines that must not block. Arguments
+ * as flce_forward_backward, except that the results go to DEVICE memory when
+ * the stream gets there: loss_dev (one fp32) and n_valid_dev (one int32);
+ * either may be NULL. The call returns once its work is enqueued. A
+ * device-side error (a target out of range, a wait that ran out) makes
+ * *loss_dev NaN and is kept until flce_async_status reads it. Under capture
+ * the call must not allocate: run it once outside capture first (or give a
+ * workspace with flce_set_workspace) and keep profiling off.
+ * Errors: those found on the host before any launch, as
+ * flce_forward_backward; device-side errors only through flce_async_status. */
+flce_status flce_forward_backward_async(flce_handle_t h, const void* x, const void* W,
+                                        const int64_t* t, int64_t N, int64_t H, int64_t V,
+                                        int64_t ignore_index, int64_t chunk, float* loss_dev,
+                                        int32_t* n_valid_dev, void* dx, float* dW,
+                                        void* stream);
+
+/* Waits for `stream` and returns the first device-side error that
+ * flce_forward_backward_async calls recorded since the last flce_async_status
+ * (FLCE_OK if none), then clears it. It reads the workspace the handle holds
+ * now: an error recorded before the workspace was replaced is lost. */
+flce_status flce_async_status(flce_handle_t h, void* stream);
 
 /* The same call with x, W and t in HOST memory: the library copies them into
  * its own device staging buffers on the stream (one cudaMemcpyAsync each),

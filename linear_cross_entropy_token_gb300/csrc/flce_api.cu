@@ -216,6 +216,7 @@ struct flce_handle_s {
   void* ws = nullptr;
   uint64_t ws_bytes = 0;
   bool ws_external = false;
+  bool ws_fresh = true;  // the control block, sticky word included, needs zeroing
   // staging for the host-buffer entry point
   void* stage = nullptr;
   uint64_t stage_bytes = 0;
@@ -338,6 +339,7 @@ flce_status ensure_workspace(flce_handle_t h, uint64_t bytes) {
                 static_cast<unsigned long long>(bytes));
   }
   h->ws_bytes = bytes;
+  h->ws_fresh = true;
   return FLCE_OK;
 }
 
@@ -509,8 +511,10 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
   h->token_loss_off = L.token_loss;
   h->has_plan = true;
 
-  cudaError_t e = cudaMemsetAsync(ctrl, 0, kCtrlWords * 4, s);
+  // per-call words; the sticky error word only when the block is new
+  cudaError_t e = cudaMemsetAsync(ctrl, 0, (h->ws_fresh ? kCtrlWords : kCtrlSticky) * 4, s);
   if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+  h->ws_fresh = false;
   if (N == 0) {
     e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * 4, s);
     if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
@@ -721,6 +725,7 @@ const char* flce_kernel_name(int32_t kind) {
     case FLCE_K_SIMT_GEMM: return "simt_gemm_f32";
     case FLCE_K_SIMT_TILE_STATS: return "simt_tile_stats_f32";
     case FLCE_K_GEMM_DX_DW: return "gemm_dx_dw";
+    case FLCE_K_DEVICE_RESULT: return "device_result";
     default: return "?";
   }
 }
@@ -817,6 +822,7 @@ flce_status flce_set_workspace(flce_handle_t h, void* dev_ptr, uint64_t bytes) {
   h->ws = dev_ptr;
   h->ws_bytes = dev_ptr ? bytes : 0;
   h->ws_external = dev_ptr != nullptr;
+  h->ws_fresh = true;
   return FLCE_OK;
 }
 
@@ -828,6 +834,43 @@ flce_status flce_forward_backward(flce_handle_t h, const void* x, const void* W,
   DeviceGuard g(h->device);
   return run_fb(h, x, W, t, N, H, V, ignore_index, chunk, loss, dx, dW,
                 static_cast<cudaStream_t>(stream));
+}
+
+flce_status flce_forward_backward_async(flce_handle_t h, const void* x, const void* W,
+                                        const int64_t* t, int64_t N, int64_t H, int64_t V,
+                                        int64_t ignore_index, int64_t chunk, float* loss_dev,
+                                        int32_t* n_valid_dev, void* dx, float* dW, void* stream) {
+  if (!h) return FLCE_ERR_INVALID_ARG;
+  h->err.clear();
+  if ((reinterpret_cast<uintptr_t>(loss_dev) & 3u) || (reinterpret_cast<uintptr_t>(n_valid_dev) & 3u))
+    return fail(h, FLCE_ERR_INVALID_ARG, "loss_dev and n_valid_dev must be 4-byte aligned");
+  DeviceGuard g(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* ctrl = nullptr;
+  const flce_status st = enqueue_fb(h, x, W, t, N, H, V, ignore_index, chunk, dx, dW, s, &ctrl);
+  if (st != FLCE_OK) return st;
+  FLCE_LAUNCH(FLCE_K_DEVICE_RESULT, 0.0, 16.0, launch_device_result(ctrl, loss_dev, n_valid_dev, s));
+  return FLCE_OK;
+}
+
+flce_status flce_async_status(flce_handle_t h, void* stream) {
+  if (!h) return FLCE_ERR_INVALID_ARG;
+  h->err.clear();
+  DeviceGuard g(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "async status: %s", cudaGetErrorString(e));
+  if (!h->ws || h->ws_fresh) return FLCE_OK;
+  uint32_t* sticky = static_cast<uint32_t*>(h->ws) + kCtrlSticky;  // the control block leads the workspace
+  uint32_t code = 0;
+  e = cudaMemcpy(&code, sticky, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && code != 0) e = cudaMemset(sticky, 0, 4);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "async status: %s", cudaGetErrorString(e));
+  if (code == FLCE_ERR_BAD_TARGET)
+    return fail(h, FLCE_ERR_BAD_TARGET, "a target is outside [0, V) and is not ignore_index");
+  if (code == FLCE_ERR_TIMEOUT) return fail(h, FLCE_ERR_TIMEOUT, "a device-side wait ran out");
+  if (code != 0) return fail(h, FLCE_ERR_CUDA, "device error word %u", code);
+  return FLCE_OK;
 }
 
 flce_status flce_forward_backward_host(flce_handle_t h, const void* x_host, const void* W_host,

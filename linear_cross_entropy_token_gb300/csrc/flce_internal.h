@@ -13,6 +13,7 @@ enum CtrlWord : int {
   kCtrlNValid = 1,   // number of non-ignored tokens
   kCtrlLoss = 2,     // fp32 bits of the mean loss
   kCtrlSched = 3,    // work-unit counter of a dynamically scheduled launch
+  kCtrlSticky = 15,  // first error of the device-result calls, kept across calls
   kCtrlWords = 16
 };
 
@@ -111,6 +112,7 @@ cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_st
                              int64_t H, const __nv_bfloat16* W, int64_t V, const int64_t* t_chunk,
                              int64_t ignore_index, const uint32_t* ctrl, const float* dcorr,
                              __nv_bfloat16* dx, cudaStream_t s);
+cudaError_t launch_device_result(uint32_t* ctrl, float* loss_dev, int32_t* n_valid_dev, cudaStream_t s);
 cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* ctrl,
                                  cudaStream_t s);
 

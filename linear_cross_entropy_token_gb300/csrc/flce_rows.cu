@@ -253,7 +253,22 @@ __global__ void loss_finalize_kernel(const float* __restrict__ token_loss, int64
   }
 }
 
+// The call's result into caller device memory, for the entry point that
+// never synchronises: the loss (NaN when a kernel recorded an error) and
+// n_valid; the first such error is also kept in the sticky word.
+__global__ void device_result_kernel(uint32_t* ctrl, float* loss_dev, int32_t* n_valid_dev) {
+  const uint32_t err = ctrl[kCtrlError];
+  if (loss_dev) *loss_dev = err ? __uint_as_float(0x7fc00000u) : __uint_as_float(ctrl[kCtrlLoss]);
+  if (n_valid_dev) *n_valid_dev = static_cast<int32_t>(ctrl[kCtrlNValid]);
+  if (err && ctrl[kCtrlSticky] == 0u) ctrl[kCtrlSticky] = err;
+}
+
 }  // namespace
+
+cudaError_t launch_device_result(uint32_t* ctrl, float* loss_dev, int32_t* n_valid_dev, cudaStream_t s) {
+  device_result_kernel<<<1, 1, 0, s>>>(ctrl, loss_dev, n_valid_dev);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_count_valid(const int64_t* t, int64_t N, int64_t V, int64_t ignore_index,
                                uint32_t* ctrl, cudaStream_t s) {

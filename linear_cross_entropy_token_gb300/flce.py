@@ -25,7 +25,8 @@ CTA = {"auto": 0, "single": 1, "pair": 2, "quad": 3}
 BACKWARD = {"auto": 0, "separate": 1, "one_launch": 2}
 KERNEL_KINDS = ["count_valid", "gemm_logits_lse", "lse_combine", "dlogits_inplace",
                 "gemm_dlogits_recompute", "gemm_dx", "dx_split_reduce", "gemm_dw",
-                "loss_finalize", "simt_gemm_f32", "simt_tile_stats_f32", "gemm_dx_dw"]
+                "loss_finalize", "simt_gemm_f32", "simt_tile_stats_f32", "gemm_dx_dw",
+                "device_result"]
 
 
 class FlceError(RuntimeError):
@@ -81,6 +82,9 @@ def load() -> ctypes.CDLL:
                                         ctypes.POINTER(ctypes.c_float), vp, vp, vp]),
         "flce_forward_backward_host": (i32, [vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                              ctypes.POINTER(ctypes.c_float), vp, vp, vp]),
+        "flce_forward_backward_async": (i32, [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp,
+                                              vp, vp]),
+        "flce_async_status": (i32, [vp, vp]),
         "flce_submit_host": (i32, [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp,
                                    ctypes.POINTER(u64)]),
         "flce_wait": (i32, [vp, u64, ctypes.POINTER(ctypes.c_float)]),
@@ -221,6 +225,43 @@ class FLCE:
                                             dW.data_ptr(), _stream_ptr(dev))
         self._check(st, "flce_forward_backward")
         return loss.value, dx, dW
+
+    def forward_backward_async(self, x, W, t, ignore_index: int = -100, chunk: int = 0,
+                               loss=None, n_valid=None, dx=None, dW=None):
+        """The fused call with no host synchronisation (capturable in a CUDA
+        graph once the workspace exists): returns device tensors (loss, a
+        0-dim float32, NaN after a device-side error; n_valid, a 0-dim
+        int32; dx; dW), filled when the current stream gets there.
+        async_status() reports device-side errors."""
+        import torch
+        dev = torch.device("cuda", self.device)
+        check_call_tensors(x, W, t, dx, dW, self._torch_dtype(), dev, dev)
+        N, H = x.shape
+        V = W.shape[0]
+        for name, ten, dt in (("loss", loss, torch.float32), ("n_valid", n_valid, torch.int32)):
+            if ten is not None and (ten.numel() != 1 or ten.dtype != dt or ten.device != dev):
+                raise ValueError(f"{name} must be one {dt} element on {dev}")
+        if loss is None:
+            loss = torch.empty((), dtype=torch.float32, device=dev)
+        if n_valid is None:
+            n_valid = torch.empty((), dtype=torch.int32, device=dev)
+        if dx is None:
+            dx = torch.empty_like(x)
+        if dW is None:
+            dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+        st = self.lib.flce_forward_backward_async(self.h, x.data_ptr(), W.data_ptr(), t.data_ptr(), N,
+                                                  H, V, ignore_index, chunk, loss.data_ptr(),
+                                                  n_valid.data_ptr(), dx.data_ptr(), dW.data_ptr(),
+                                                  _stream_ptr(dev))
+        self._check(st, "flce_forward_backward_async")
+        return loss, n_valid, dx, dW
+
+    def async_status(self) -> None:
+        """Wait for the current stream; raise FlceError for a device-side
+        error recorded by forward_backward_async calls since the last check."""
+        import torch
+        st = self.lib.flce_async_status(self.h, _stream_ptr(torch.device("cuda", self.device)))
+        self._check(st, "flce_async_status")
 
     def forward_backward_host(self, x_host, W_host, t_host, ignore_index: int = -100,
                               chunk: int = 0, dx=None, dW=None):

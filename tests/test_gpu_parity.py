@@ -276,6 +276,62 @@ def test_pipelined_host_submissions(bf16):
         assert_parity({"loss": loss, "dx": to_np64(dx), "dW": to_np64(dW)}, _oracle(w), "bf16")
 
 
+def test_device_result_entry_and_graph_capture(bf16):
+    """flce_forward_backward_async leaves loss and n_valid in device memory
+    without a host sync. Captured in a CUDA graph and replayed after new
+    inputs are written into the same buffers, it gives the oracle's results
+    on those inputs."""
+    ws = [workloads.generate(workloads.custom(1000, 256, 4099, "bf16", ignore_frac=0.1, seed=s))
+          for s in (40, 41)]
+    x, W, t = device_inputs(ws[0])
+    dx = torch.empty_like(x)
+    dW = torch.empty(W.shape, dtype=torch.float32, device="cuda")
+    loss = torch.empty((), dtype=torch.float32, device="cuda")
+    nv = torch.empty((), dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # outside capture: allocates the workspace
+        bf16.forward_backward_async(x, W, t, chunk=300, loss=loss, n_valid=nv, dx=dx, dW=dW)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert_parity({"loss": loss.item(), "dx": to_np64(dx), "dW": to_np64(dW)}, _oracle(ws[0]), "bf16")
+    assert nv.item() == int((ws[0].t != -100).sum())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bf16.forward_backward_async(x, W, t, chunk=300, loss=loss, n_valid=nv, dx=dx, dW=dW)
+    for w in ws[::-1]:
+        x2, W2, t2 = device_inputs(w)
+        x.copy_(x2)
+        W.copy_(W2)
+        t.copy_(t2)
+        g.replay()
+        torch.cuda.synchronize()
+        assert_parity({"loss": loss.item(), "dx": to_np64(dx), "dW": to_np64(dW)}, _oracle(w), "bf16")
+        assert nv.item() == int((w.t != -100).sum())
+    bf16.async_status()
+
+
+def test_device_result_reports_errors_late(bf16):
+    """An out-of-range target in a sync-free call: the device loss is NaN and
+    the error comes out of flce_async_status once, then the handle is clean."""
+    from linear_cross_entropy_token_gb300 import FlceError
+    w = workloads.generate(workloads.custom(200, 64, 500, "bf16", seed=42))
+    w.t[5] = 600
+    x, W, t = device_inputs(w)
+    loss, _, _, _ = bf16.forward_backward_async(x, W, t)
+    torch.cuda.synchronize()
+    assert math.isnan(loss.item())
+    with pytest.raises(FlceError) as e:
+        bf16.async_status()
+    assert e.value.status_name == "FLCE_ERR_BAD_TARGET"
+    bf16.async_status()
+    w.t[5] = 3
+    x, W, t = device_inputs(w)
+    loss, _, _, _ = bf16.forward_backward_async(x, W, t)
+    bf16.async_status()
+    assert abs(loss.item() - _oracle(w).loss) <= 1e-3 * _oracle(w).loss
+
+
 def test_misaligned_or_mismatched_arguments_are_refused(bf16):
     """The C ABI refuses pointers its vector loads and TMA maps cannot take
     (before any launch), and the binding refuses tensors whose shapes do not
