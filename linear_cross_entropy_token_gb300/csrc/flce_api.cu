@@ -14,9 +14,11 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <array>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -125,6 +127,48 @@ int pick_dx_splits(int64_t C, int64_t H, int64_t V, int slots, int tile_m) {
     if (score > best_score + 1e-12) {
       best_score = score;
       best = s;
+    }
+  }
+  return best;
+}
+
+// Tile order for a GEMM whose operands are both streamed from DRAM: dx,
+// whose A (the chunk's dlogits) and B (W) are each far larger than L2. The
+// persistent grid runs `slots` units at once, moving along k together, so a
+// wave of consecutive units reads the k-slices of each tile row's A slab and
+// each tile column's B slab once, whatever the number of units sharing them.
+// Returns the group_m of the grouped order (1 = columns fastest, num_m =
+// rows fastest) whose waves read the fewest slabs in total.
+int pick_group_m(int num_m, int num_n, int num_s, int slots) {
+  const int per_s = num_m * num_n;
+  const int units = per_s * num_s;
+  std::vector<int> seen_m(static_cast<size_t>(num_m) * num_s), seen_n(static_cast<size_t>(num_n) * num_s);
+  int best = num_m;
+  int64_t best_cost = -1;
+  for (int G = num_m; G >= 1; --G) {
+    std::fill(seen_m.begin(), seen_m.end(), -1);
+    std::fill(seen_n.begin(), seen_n.end(), -1);
+    int64_t cost = 0;
+    for (int u = 0; u < units; ++u) {
+      const int wave = u / slots;
+      const int sp = u / per_s, w = u - sp * per_s;
+      const int per = G * num_n, g = w / per, idx = w - g * per;
+      const int rows = std::min(G, num_m - g * G);
+      const int m = g * G + idx % rows, n = idx / rows;
+      int& sm = seen_m[static_cast<size_t>(sp) * num_m + m];
+      if (sm != wave) {
+        sm = wave;
+        ++cost;
+      }
+      int& sn = seen_n[static_cast<size_t>(sp) * num_n + n];
+      if (sn != wave) {
+        sn = wave;
+        ++cost;
+      }
+    }
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = G;
     }
   }
   return best;
@@ -241,6 +285,7 @@ struct flce_handle_s {
   bool has_plan = false;
   int64_t launches = 0;
   Profiler prof;
+  std::map<std::array<int, 4>, int> group_cache;  // pick_group_m by (num_m, num_n, num_s, slots)
 };
 
 namespace {
@@ -414,21 +459,26 @@ flce_status read_back(flce_handle_t h, uint32_t* ctrl_dev, cudaStream_t s, float
 
 // One GEMM on the handle's tile shape; sets num_m from the M extent and the
 // grid from the work units (persistent CTAs, or CTA pairs).
+int group_for(flce_handle_t h, int num_m, int num_n, int num_s, int slots) {
+  const std::array<int, 4> key{num_m, num_n, num_s, slots};
+  auto it = h->group_cache.find(key);
+  if (it != h->group_cache.end()) return it->second;
+  const int g = pick_group_m(num_m, num_n, num_s, slots);
+  h->group_cache.emplace(key, g);
+  return g;
+}
+
 cudaError_t launch_gemm(flce_handle_t h, int kind, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& o, UmmaArgs args, int64_t M, cudaStream_t s) {
-  if (h->use_quad) {
-    args.num_m = static_cast<int>(cdiv(M, 4 * kBM));
-    const int units = args.num_m * args.num_n * args.num_s;
-    return launch_umma_quad(kind, a, b, o, args, std::min(units, h->quad_clusters), s);
-  }
-  if (h->use_pair) {
-    args.num_m = static_cast<int>(cdiv(M, 2 * kBM));
-    const int units = args.num_m * args.num_n * args.num_s;
-    return launch_umma_pair(kind, a, b, o, args, std::min(units, h->pair_clusters), s);
-  }
-  args.num_m = static_cast<int>(cdiv(M, kBM));
+  const int rows_per_unit = h->use_quad ? 4 * kBM : h->use_pair ? 2 * kBM : kBM;
+  const int slots_max = h->use_quad ? h->quad_clusters : h->use_pair ? h->pair_clusters : h->num_sms;
+  args.num_m = static_cast<int>(cdiv(M, rows_per_unit));
   const int units = args.num_m * args.num_n * args.num_s;
-  return launch_umma(kind, a, b, o, args, std::min(units, h->num_sms), s);
+  const int slots = std::min(units, slots_max);
+  if (args.raster == 2) args.group_m = group_for(h, args.num_m, args.num_n, args.num_s, slots);
+  if (h->use_quad) return launch_umma_quad(kind, a, b, o, args, slots, s);
+  if (h->use_pair) return launch_umma_pair(kind, a, b, o, args, slots, s);
+  return launch_umma(kind, a, b, o, args, slots, s);
 }
 
 // Device copies of a call's host inputs, in one buffer (grown as needed).
@@ -620,7 +670,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       b.num_s = S;
       b.kb_total = kb_v;
       b.kb_per_split = kbps;
-      b.raster = 0;
+      b.raster = 2;  // grouped: both operands stream from DRAM (group_m set at launch)
       b.rows = rows;
       b.cols = static_cast<int>(H);
       b.reduce_add = 0;
@@ -657,6 +707,8 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
         da.p[0].num_m = static_cast<int>(cdiv(rows, 2 * kBM));
         da.p[1].num_m = static_cast<int>(cdiv(V, 2 * kBM));
         da.units0 = da.p[0].num_m * da.p[0].num_n * da.p[0].num_s;
+        da.p[0].group_m = group_for(h, da.p[0].num_m, da.p[0].num_n, da.p[0].num_s,
+                                    std::min(da.units0, h->pair_clusters));
         da.pad = 0;
         da.sched_ctr = reinterpret_cast<int32_t*>(ctrl + kCtrlSched);
         e = cudaMemsetAsync(da.sched_ctr, 0, 4, s);

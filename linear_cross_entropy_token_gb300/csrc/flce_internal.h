@@ -47,13 +47,14 @@ struct UmmaArgs {
   int32_t num_m, num_n, num_s;   // output tiles along M, N and splits of K
   int32_t kb_total;              // 64-deep k-blocks over the whole K
   int32_t kb_per_split;          // k-blocks per split
-  int32_t raster;                // 0: m fastest; 1: n fastest (then the other, then s)
+  int32_t raster;                // 0: m fastest; 1: n fastest; 2: groups of group_m rows of
+                                 // tiles, m fastest inside a group (then the other, then s)
   int32_t rows;                  // valid output rows (M extent)
   int32_t cols;                  // valid output columns (N extent; V for the logits GEMM)
   int32_t vocab_tiles;           // log-sum-exp partials per token
   int32_t reduce_add;            // kEpiF32: 1 = add into the output instead of storing
   int32_t store_logits;          // kEpiLse: 1 = also store bf16 logits
-  int32_t pad0;
+  int32_t group_m;               // raster 2: tile rows per group
   int64_t ignore_index;
   const int64_t* targets;        // targets of this chunk's tokens
   float2* partials;              // [rows][vocab_tiles] (running max, sum of exp)

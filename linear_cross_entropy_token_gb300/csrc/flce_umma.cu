@@ -75,6 +75,15 @@ __device__ __forceinline__ Unit unit_coords(const UmmaArgs& a, int u) {
   if (a.raster == 0) {
     r.m = w % a.num_m;
     r.n = w / a.num_m;
+  } else if (a.raster == 2) {
+    // a group of group_m tile rows (fewer in the last group) sweeps all the
+    // columns, its rows fastest: consecutive units share both operands
+    const int per = a.group_m * a.num_n;
+    const int g = w / per;
+    const int idx = w - g * per;
+    const int rows = min(a.group_m, a.num_m - g * a.group_m);
+    r.m = g * a.group_m + idx % rows;
+    r.n = idx / rows;
   } else {
     r.n = w % a.num_n;
     r.m = w / a.num_n;
