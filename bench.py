@@ -33,6 +33,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 HBM_BOUND = {"dlogits_inplace", "lse_combine", "dx_split_reduce", "count_valid", "loss_finalize"}
+ALU_BOUND = {"simt_gemm_f32"}
 
 
 def parse():
@@ -255,14 +256,20 @@ def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     w = workloads.make(args.config)
     N, H, V = w.N, w.H, w.V
-    x_h = torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16)
-    W_h = torch.from_numpy(w.W.view(np.int16)).view(torch.bfloat16)
+    bf16 = w.x.dtype == np.uint16   # bf16 configs hold RNE-rounded bit patterns
+    if bf16:
+        x_h = torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16)
+        W_h = torch.from_numpy(w.W.view(np.int16)).view(torch.bfloat16)
+    else:
+        x_h = torch.from_numpy(w.x)
+        W_h = torch.from_numpy(w.W)
+    esize = x_h.element_size()
     t_h = torch.from_numpy(w.t)
     x, W, t = x_h.to(dev), W_h.to(dev), t_h.to(dev)
     dx = torch.empty_like(x)
     dW = torch.empty((V, H), dtype=torch.float32, device=dev)
     budget = int(args.budget_gib * (1 << 30))
-    h = FLCE("bf16", local, hbm_budget_bytes=budget, dlogits_mode=args.dlogits, cta=args.cta,
+    h = FLCE("bf16" if bf16 else "fp32", local, hbm_budget_bytes=budget, dlogits_mode=args.dlogits, cta=args.cta,
              backward=args.backward)
     stream = torch.cuda.current_stream(dev)
 
@@ -310,13 +317,20 @@ def run_ours(args, ws, rank, local):
     if name in HBM_BOUND:
         achieved = pk["bytes"] / pk["launches"] / (per_launch_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    elif name in ALU_BOUND:
+        # fp32 CUDA-core FMAs: SMs x 128 FP32 lanes x 2 FLOP x the maximum SM clock
+        achieved = pk["flops"] / pk["launches"] / (per_launch_ms / 1e3) / 1e12
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s"}
     else:
         achieved = pk["flops"] / pk["launches"] / (per_launch_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = traffic_for(name, args.config, plan["chunk"])
     roof["kernel"] = name
-    roof["peak_source"] = f"{peaks_kind} ({'sustained bf16' if roof['bound'] == 'tensor' else 'hbm copy'})"
+    roof["peak_source"] = {"tensor": f"{peaks_kind} (sustained bf16)", "hbm": f"{peaks_kind} (hbm copy)",
+                           "alu": "derived: SMs x 128 fp32 lanes x 2 x max SM clock"}[roof["bound"]]
     kernels = {k: {"launches": v["launches"], "ms_per_launch": v["total_ms"] / v["launches"],
                    "share": v["total_ms"] / sum(q["total_ms"] for q in prof.values()),
                    ("tflops" if k not in HBM_BOUND else "gbs"):
@@ -362,7 +376,7 @@ def run_ours(args, ws, rank, local):
         ems, evalue = aggregate(ws, tokens, pipe_ms, dev if ws > 1 else None)
         sync_max, _ = aggregate(ws, tokens, sync_ms, dev if ws > 1 else None)
         e2e = {"value": evalue, "unit": UNIT,
-               "h2d_bytes_per_step": int(x_h.numel() * 2 + W_h.numel() * 2 + t_h.numel() * 8),
+               "h2d_bytes_per_step": int((x_h.numel() + W_h.numel()) * esize + t_h.numel() * 8),
                "d2h_bytes_per_step": 4 * 16, "ms_per_step": ems,
                "path": "flce_submit_host / flce_wait: pinned host x, W, t copied in every step on "
                        "the library's copy stream (overlapping the previous step's compute); "
@@ -384,12 +398,13 @@ def run_ours(args, ws, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
         "config": {"workload": args.config, "N": N, "H": H, "V": V, "chunk": plan["chunk"],
                    "num_chunks": plan["num_chunks"], "dx_splits": plan["dx_splits"],
                    "dlogits": "recompute" if args.dlogits == "recompute" else "inplace",
-                   "gemm_tiles": {128: "128x256, one CTA", 256: "256x256, CTA pairs",
-                                  512: "512x256, two CTA pairs sharing B"}[plan["tile_m"]],
+                   "gemm_tiles": ({128: "128x256, one CTA", 256: "256x256, CTA pairs",
+                                   512: "512x256, two CTA pairs sharing B"}[plan["tile_m"]]
+                                  if bf16 else "fp32 CUDA-core GEMMs"),
                    "backward_gemms": "one launch" if args.backward == "one_launch" else "two launches",
                    "targets": w.spec.targets, "ignore_frac": float(w.spec.ignore_frac),
                    "l2": "inputs larger than L2 (W is 1.05 GB bf16; the chunk buffer 1.05 GB)",
