@@ -109,7 +109,6 @@ int cta_group_size(const flce_config* cfg) {
   return mode == FLCE_CTA_QUAD ? 4 : mode == FLCE_CTA_PAIR ? 2 : 1;
 }
 
-bool wants_pair(const flce_config* cfg) { return cta_group_size(cfg) == 2; }
 
 // Splits of the dx GEMM's V reduction that fill the machine's waves best:
 // `slots` work units run at once (SMs, or SM pairs), each tile_m x 256.
