@@ -109,7 +109,6 @@ int cta_group_size(const flce_config* cfg) {
   return mode == FLCE_CTA_QUAD ? 4 : mode == FLCE_CTA_PAIR ? 2 : 1;
 }
 
-
 // Splits of the dx GEMM's V reduction that fill the machine's waves best:
 // `slots` work units run at once (SMs, or SM pairs), each tile_m x 256.
 int pick_dx_splits(int64_t C, int64_t H, int64_t V, int slots, int tile_m) {
