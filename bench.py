@@ -96,6 +96,18 @@ def aggregate(ws, tokens_per_rank: int, ms_local: float, device=None):
     return ms_max, ws * tokens_per_rank / (ms_max / 1e3)
 
 
+L2_BYTES = 129 * 10**6   # GB300 L2
+
+
+def l2_note(w_bytes: int, buf_bytes: int) -> str:
+    """How the timed steps stand to L2: every step streams W and the chunk
+    buffer, so the inputs are larger than L2 when either is."""
+    size = f"W {w_bytes / 1e9:.3g} GB, chunk buffer {buf_bytes / 1e9:.3g} GB"
+    if max(w_bytes, buf_bytes) > L2_BYTES:
+        return f"inputs larger than L2 ({size}; L2 129 MB)"
+    return f"inputs smaller than L2 ({size}; L2 129 MB): steps may hit in L2, no flush"
+
+
 # The pages' own figures for this shape, other hardware: context, not targets.
 PAGE_CONTEXT = {
     "full_logits_bf16_gb": 4.20,
@@ -407,7 +419,7 @@ def run_ours(args, ws, rank, local):
                                   if bf16 else "fp32 CUDA-core GEMMs"),
                    "backward_gemms": "one launch" if args.backward == "one_launch" else "two launches",
                    "targets": w.spec.targets, "ignore_frac": float(w.spec.ignore_frac),
-                   "l2": "inputs larger than L2 (W is 1.05 GB bf16; the chunk buffer 1.05 GB)",
+                   "l2": l2_note(V * H * esize, plan["logits_bytes"]),
                    "parallelism": "replicas" if ws > 1 else "single"},
         "tflops": tflops, "frac_of_bf16_peak": tflops / sustained,
         "frac_of_bf16_peak_burst": tflops / peaks["bf16_tflops"],
