@@ -202,6 +202,21 @@ def traffic_for(kernel: str, workload: str, chunk: int):
 
 # ------------------------------------------------------------- cpu oracle
 
+def blas_threads() -> int:
+    """Threads numpy's BLAS runs the oracle's products on."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p["num_threads"] for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
 def oracle_sample_rate(w, target_s: float, max_tokens: int = 4096):
     """The fp64 oracle on the first n tokens of the workload (all of W), n
     grown until one run takes about target_s seconds. Returns tokens/s, n,
@@ -209,8 +224,9 @@ def oracle_sample_rate(w, target_s: float, max_tokens: int = 4096):
     import numpy as np
     import oracle
     Wd = w.W_f64()
-    cores = len(os.sched_getaffinity(0))
-    n = 8
+    cores = blas_threads()
+    max_tokens = min(max_tokens, w.N)
+    n = min(8, max_tokens)
     while True:
         xs = w.x_f64(np.arange(n))
         t0 = time.perf_counter()
