@@ -361,6 +361,38 @@ def test_misaligned_or_mismatched_arguments_are_refused(bf16):
     assert_parity(run(bf16, w), _oracle(w), "bf16")
 
 
+def test_two_handles_on_two_streams():
+    """Two handles driven on two streams at once (each call only waits for its
+    own stream) give the same results as the same calls made one at a time."""
+    from linear_cross_entropy_token_gb300 import FLCE
+    ws = [workloads.generate(workloads.custom(1500, 256, 7000, "bf16", ignore_frac=0.1, seed=s))
+          for s in (50, 51)]
+    hs = [FLCE("bf16", 0, cta="pair"), FLCE("bf16", 0, cta="pair")]
+    try:
+        inputs = [device_inputs(w) for w in ws]
+        alone = []
+        for h, (x, W, t) in zip(hs, inputs):
+            loss, dx, dW = h.forward_backward(x, W, t, chunk=512)
+            alone.append((loss, dx.clone(), dW.clone()))
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        outs = [None, None]
+        torch.cuda.synchronize()
+        for rep in range(3):
+            for i in (0, 1):
+                with torch.cuda.stream(streams[i]):
+                    loss, n_valid, dx, dW = hs[i].forward_backward_async(*inputs[i], chunk=512)
+                    outs[i] = (loss, dx, dW)
+            torch.cuda.synchronize()
+            for i in (0, 1):
+                assert outs[i][0].item() == alone[i][0]
+                assert torch.equal(outs[i][1], alone[i][1]) and torch.equal(outs[i][2], alone[i][2])
+        for h in hs:
+            h.async_status()
+    finally:
+        for h in hs:
+            h.close()
+
+
 def test_caller_workspace(bf16):
     from linear_cross_entropy_token_gb300 import FLCE, FlceError, plan
     w = workloads.generate(workloads.custom(500, 64, 1000, "bf16", seed=12))
