@@ -393,6 +393,29 @@ def test_two_handles_on_two_streams():
             h.close()
 
 
+def test_workspace_allocation_failure_is_reported():
+    """A plan whose workspace the device cannot hold (a 328 GB chunk buffer
+    under a 1 TB budget) fails in cudaMalloc before any launch: the call
+    reports FLCE_ERR_BUDGET and the handle still works afterwards."""
+    from linear_cross_entropy_token_gb300 import FLCE, FlceError
+    N, H, V = 32768, 8, 5_000_000
+    h = FLCE("bf16", 0, hbm_budget_bytes=1 << 40)
+    try:
+        assert h.workspace_bytes(N, H, V) > 300e9
+        x = torch.zeros(N, H, dtype=torch.bfloat16, device="cuda")
+        W = torch.zeros(V, H, dtype=torch.bfloat16, device="cuda")
+        t = torch.zeros(N, dtype=torch.int64, device="cuda")
+        with pytest.raises(FlceError) as e:
+            h.forward_backward(x, W, t)
+        assert e.value.status_name == "FLCE_ERR_BUDGET"
+        del x, W, t
+        torch.cuda.empty_cache()
+        w = workloads.generate(workloads.custom(500, 64, 1000, "bf16", seed=15))
+        assert_parity(run(h, w), _oracle(w), "bf16")
+    finally:
+        h.close()
+
+
 def test_caller_workspace(bf16):
     from linear_cross_entropy_token_gb300 import FLCE, FlceError, plan
     w = workloads.generate(workloads.custom(500, 64, 1000, "bf16", seed=12))
