@@ -27,7 +27,8 @@ _PLAIN = {"count_valid_kernel": "count_valid", "lse_combine_kernel": "lse_combin
           "dlogits_bf16_kernel": "dlogits_inplace", "dlogits_f32_kernel": "dlogits_inplace_f32",
           "dx_reduce_kernel": "dx_split_reduce", "loss_finalize_kernel": "loss_finalize",
           "simt_gemm_f32_kernel": "simt_gemm_f32", "simt_tile_stats_kernel": "simt_tile_stats_f32",
-          "wait_check_kernel": "wait_check", "umma_pair_dual_kernel": "gemm_dx_dw"}
+          "wait_check_kernel": "wait_check", "umma_pair_dual_kernel": "gemm_dx_dw",
+          "device_result_kernel": "device_result"}
 
 RAW_METRICS = [
     ("gpu__time_duration.sum", "time_us", 1e-3),
