@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--chunk", type=int, default=0)
     p.add_argument("--budget-gib", type=float, default=0.0)
     p.add_argument("--dlogits", choices=["auto", "inplace", "recompute"], default="auto")
-    p.add_argument("--cta", choices=["auto", "single", "pair", "quad"], default="auto",
+    p.add_argument("--cta", choices=["auto", "single", "pair", "quad", "wide"], default="auto",
                    help="GEMM tile shape: one CTA per 128x256 tile, CTA pairs per 256x256, "
                         "or two pairs sharing B per 512x256")
     p.add_argument("--backward", choices=["auto", "separate", "one_launch"], default="auto",
@@ -440,8 +440,10 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": args.config, "N": N, "H": H, "V": V, "chunk": plan["chunk"],
                    "num_chunks": plan["num_chunks"], "dx_splits": plan["dx_splits"],
                    "dlogits": "recompute" if args.dlogits == "recompute" else "inplace",
-                   "gemm_tiles": ({128: "128x256, one CTA", 256: "256x256, CTA pairs",
-                                   512: "512x256, two CTA pairs sharing B"}[plan["tile_m"]]
+                   "gemm_tiles": ({(128, 256): "128x256, one CTA", (256, 256): "256x256, CTA pairs",
+                                   (256, 512): "256x512, CTA pairs sharing A through the collector",
+                                   (512, 256): "512x256, two CTA pairs sharing B"}[
+                                      (plan["tile_m"], plan["tile_n"])]
                                   if bf16 else "fp32 CUDA-core GEMMs"),
                    "backward_gemms": "one launch" if args.backward == "one_launch" else "two launches",
                    "targets": w.spec.targets, "ignore_frac": float(w.spec.ignore_frac),

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define FLCE_ABI_VERSION 1
+#define FLCE_ABI_VERSION 2
 
 typedef struct flce_handle_s* flce_handle_t;
 
@@ -83,7 +83,13 @@ enum { FLCE_DLOGITS_AUTO = 0, FLCE_DLOGITS_INPLACE = 1, FLCE_DLOGITS_RECOMPUTE =
  *          (tcgen05 cta_group::2): each CTA loads half of the B operand.
  *  AUTO:   PAIR (measured faster on GB300: 34.1 vs 36.9 ms for the 16384-token,
  *          128256-vocabulary step), SINGLE where pairs cannot be scheduled. */
-enum { FLCE_CTA_AUTO = 0, FLCE_CTA_SINGLE = 1, FLCE_CTA_PAIR = 2, FLCE_CTA_QUAD = 3 };
+enum { FLCE_CTA_AUTO = 0, FLCE_CTA_SINGLE = 1, FLCE_CTA_PAIR = 2, FLCE_CTA_QUAD = 3,
+       FLCE_CTA_WIDE = 4 };
+/*  WIDE:   CTA pairs on 256 x 512 tiles: per k-step two 256 x 256 MMAs share
+ *          their A operand through the tensor core's collector buffer, so a
+ *          CTA's shared memory moves 25% fewer bytes per FLOP. The 512
+ *          accumulator columns fill TMEM: the epilogue does not overlap the
+ *          next tile's main loop. */
 /*  QUAD:   clusters of two CTA pairs on consecutive 256-row blocks of the same
  *          256 columns (512 x 256 tiles); the pairs share B through TMA
  *          multicast, so a CTA fetches a quarter of the B tile instead of a
@@ -119,8 +125,9 @@ typedef struct flce_plan {
     int64_t dx_splits;           /* split of the V reduction of the dx GEMM            */
     uint64_t workspace_bytes;    /* device bytes one call needs                        */
     uint64_t logits_bytes;       /* of which the C x ldv logits / dlogits buffer       */
-    int64_t tile_m;              /* rows of a GEMM output tile: 128 (one CTA), 256 (CTA pair)
-                                    or 512 (two pairs)                                  */
+    int64_t tile_m;              /* rows of a GEMM output tile: 128 (one CTA), 256 (CTA pair,
+                                    normal or wide) or 512 (two pairs)                  */
+    int64_t tile_n;              /* columns of a GEMM output tile: 256, or 512 (wide)   */
 } flce_plan;
 
 /* Kernel kinds, for the per-kernel timing of flce_profile_read(). */

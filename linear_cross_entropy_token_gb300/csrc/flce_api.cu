@@ -108,13 +108,19 @@ constexpr int kAutoCta = FLCE_CTA_PAIR;
 int cta_group_size(const flce_config* cfg) {
   if (cfg->dtype != FLCE_DTYPE_BF16) return 1;
   const int mode = cfg->cta_pair == FLCE_CTA_AUTO ? kAutoCta : cfg->cta_pair;
-  return mode == FLCE_CTA_QUAD ? 4 : mode == FLCE_CTA_PAIR ? 2 : 1;
+  return mode == FLCE_CTA_QUAD ? 4 : (mode == FLCE_CTA_PAIR || mode == FLCE_CTA_WIDE) ? 2 : 1;
+}
+
+// Output-tile columns of the handle's GEMMs: 512 for wide CTA-pair tiles
+int tile_cols(const flce_config* cfg) {
+  const int mode = cfg->cta_pair == FLCE_CTA_AUTO ? kAutoCta : cfg->cta_pair;
+  return cfg->dtype == FLCE_DTYPE_BF16 && mode == FLCE_CTA_WIDE ? 2 * kBN : kBN;
 }
 
 // Splits of the dx GEMM's V reduction that fill the machine's waves best:
-// `slots` work units run at once (SMs, or SM pairs), each tile_m x 256.
-int pick_dx_splits(int64_t C, int64_t H, int64_t V, int slots, int tile_m) {
-  const int64_t tiles = cdiv(C, tile_m) * cdiv(H, kBN);
+// `slots` work units run at once (SMs, or SM pairs), each tile_m x tile_n.
+int pick_dx_splits(int64_t C, int64_t H, int64_t V, int slots, int tile_m, int tile_n) {
+  const int64_t tiles = cdiv(C, tile_m) * cdiv(H, tile_n);
   const int64_t kb = cdiv(V, kBK);
   int best = 1;
   double best_score = -1;
@@ -197,7 +203,7 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   out->vocab_tiles = cdiv(V, kVocabTile);
   const int group = cta_group_size(cfg);
   auto splits_for = [&](int64_t C) {
-    return bf16 ? pick_dx_splits(C, H, V, num_sms / group, group * kBM) : 0;
+    return bf16 ? pick_dx_splits(C, H, V, num_sms / group, group * kBM, tile_cols(cfg)) : 0;
   };
   auto ws = [&](int64_t C) {
     return make_layout(N, H, C, out->ldv, out->vocab_tiles, splits_for(C), esize).total;
@@ -239,6 +245,7 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
       make_layout(N, H, C, out->ldv, out->vocab_tiles, C ? splits_for(C) : 0, esize).total;
   out->logits_bytes = static_cast<uint64_t>(C) * out->ldv * esize;
   out->tile_m = group * kBM;
+  out->tile_n = tile_cols(cfg);
   return FLCE_OK;
 }
 
@@ -254,6 +261,8 @@ struct flce_handle_s {
   bool use_pair = false;  // GEMMs on CTA pairs (256 x 256 tiles)
   int quad_clusters = 0;  // clusters of four the quad kernels fit at once
   bool use_quad = false;  // GEMMs on two pairs sharing B (512 x 256 tiles)
+  int wide_clusters = 0;  // clusters of two the wide kernels fit at once
+  bool use_wide = false;  // GEMMs on CTA pairs with 256 x 512 tiles
   uint64_t timeout_ns = 0;
   std::string err;
   // workspace
@@ -481,13 +490,17 @@ int group_for(flce_handle_t h, int num_m, int num_n, int num_s, int slots) {
 
 cudaError_t launch_gemm(flce_handle_t h, int kind, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& o, UmmaArgs args, int64_t M, cudaStream_t s) {
-  const int rows_per_unit = h->use_quad ? 4 * kBM : h->use_pair ? 2 * kBM : kBM;
-  const int slots_max = h->use_quad ? h->quad_clusters : h->use_pair ? h->pair_clusters : h->num_sms;
+  const int rows_per_unit = h->use_quad ? 4 * kBM : (h->use_pair || h->use_wide) ? 2 * kBM : kBM;
+  const int slots_max = h->use_quad ? h->quad_clusters
+                        : h->use_wide ? h->wide_clusters
+                        : h->use_pair ? h->pair_clusters : h->num_sms;
   args.num_m = static_cast<int>(cdiv(M, rows_per_unit));
+  if (h->use_wide) args.num_n = static_cast<int>(cdiv(args.cols, 2 * kBN));
   const int units = args.num_m * args.num_n * args.num_s;
   const int slots = std::min(units, slots_max);
   if (args.raster == 2) args.group_m = group_for(h, args.num_m, args.num_n, args.num_s, slots);
   if (h->use_quad) return launch_umma_quad(kind, a, b, o, args, slots, s);
+  if (h->use_wide) return launch_umma_wide(kind, a, b, o, args, slots, s);
   if (h->use_pair) return launch_umma_pair(kind, a, b, o, args, slots, s);
   return launch_umma(kind, a, b, o, args, slots, s);
 }
@@ -624,7 +637,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     const bool recompute = h->cfg.dlogits_mode == FLCE_DLOGITS_RECOMPUTE;
     CUtensorMap mW_k, mW_mn, mX_k, mX_mn, mZ_out, mZ_k, mZ_mn, mDx, mDw;
     // a CTA of a pair loads 128 of the tile's 256 columns of a K-major B
-    if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, h->use_quad ? 64 : h->use_pair ? 128 : 256, &why) ||
+    if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, h->use_quad ? 64 : (h->use_pair || h->use_wide) ? 128 : 256, &why) ||
         !map_bf16_2d(&mW_mn, W, H, V, H * 2, 64, 64, &why) ||
         !map_f32_3d(&mDw, dW, H, V, 1, H * 4, static_cast<uint64_t>(V) * H * 4, &why))
       return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
@@ -835,6 +848,13 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
         return FLCE_ERR_UNSUPPORTED;
       }
       h->use_quad = true;
+    } else if (group == 2 && tile_cols(cfg) == 2 * kBN) {
+      h->wide_clusters = umma_wide_max_clusters();
+      if (h->wide_clusters <= 0) {
+        delete h;
+        return FLCE_ERR_UNSUPPORTED;
+      }
+      h->use_wide = true;
     } else if (group == 2) {
       h->pair_clusters = umma_pair_max_clusters();
       if (cfg->cta_pair == FLCE_CTA_PAIR && h->pair_clusters <= 0) {
@@ -844,7 +864,10 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
       h->use_pair = h->pair_clusters > 0;
     }
     // the handle's plans follow the tile shape it actually runs
-    h->cfg.cta_pair = h->use_quad ? FLCE_CTA_QUAD : h->use_pair ? FLCE_CTA_PAIR : FLCE_CTA_SINGLE;
+    h->cfg.cta_pair = h->use_quad   ? FLCE_CTA_QUAD
+                      : h->use_wide ? FLCE_CTA_WIDE
+                      : h->use_pair ? FLCE_CTA_PAIR
+                                    : FLCE_CTA_SINGLE;
   }
   if (cudaMallocHost(&h->host_ctrl, kCtrlWords * 4) != cudaSuccess) {
     cudaGetLastError();
@@ -1094,7 +1117,7 @@ flce_status flce_check_gemm(flce_handle_t h, int32_t a_mn_major, int32_t b_mn_ma
   bool ok = a_mn_major ? map_bf16_2d(&ma, A, M, K, M * 2, 64, 64, &why)
                        : map_bf16_2d(&ma, A, K, M, K * 2, 64, 128, &why);
   ok = ok && (b_mn_major ? map_bf16_2d(&mb, B, N, K, N * 2, 64, 64, &why)
-                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, h->use_quad ? 64 : h->use_pair ? 128 : 256, &why));
+                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, h->use_quad ? 64 : (h->use_pair || h->use_wide) ? 128 : 256, &why));
   ok = ok && map_f32_3d(&mc, C, N, M, 1, N * 4, static_cast<uint64_t>(M) * N * 4, &why);
   if (!ok) return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
   UmmaArgs a{};

@@ -74,6 +74,12 @@ cudaError_t launch_umma(int kind, const CUtensorMap& a, const CUtensorMap& b, co
 cudaError_t launch_umma_pair(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                              const UmmaArgs& args, int pairs, cudaStream_t s);
 int umma_pair_max_clusters();
+// Wide CTA-pair kernels: 256 x 512 tiles (two MMAs per k-step sharing A);
+// num_m counts 256-row tiles, num_n 512-column tiles; B maps of K-major
+// operands use a 64 x 128 box, as for pairs
+cudaError_t launch_umma_wide(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                             const UmmaArgs& args, int pairs, cudaStream_t s);
+int umma_wide_max_clusters();
 // Two CTA pairs per cluster sharing B through multicast: 512 x 256 tiles;
 // num_m counts 512-row tiles; B maps of K-major operands use a 64 x 64 box
 cudaError_t launch_umma_quad(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,

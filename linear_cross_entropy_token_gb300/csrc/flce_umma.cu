@@ -55,13 +55,20 @@ constexpr uint32_t kSmemBytes =
     1024 + kStages * kStageBytes + 2 * kEpiBytes + (2 * kStages + 5) * 8 + 16;
 constexpr uint32_t kSmemBytesPair =
     1024 + kStagesPair * kStageBytesPair + 2 * kEpiBytes + (2 * kStagesPair + 5) * 8 + 16;
+// wide CTA-pair tiles: 256 x 512, each CTA holding 128 rows of A and 256
+// columns of B per k-block
+constexpr int kStagesWide = 4;
+constexpr uint32_t kStageBytesWide = kABytes + kBBytes;    // 48 KB per CTA
+constexpr uint32_t kSmemBytesWide =
+    1024 + kStagesWide * kStageBytesWide + 2 * kEpiBytes + (2 * kStagesWide + 3) * 8 + 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kEpiBar = 1;
 constexpr float kLog2e = 1.4426950408889634f;
 
-static_assert(kSmemBytes <= 232448 && kSmemBytesPair <= 232448, "shared memory per CTA");
+static_assert(kSmemBytes <= 232448 && kSmemBytesPair <= 232448 && kSmemBytesWide <= 232448,
+              "shared memory per CTA");
 
 struct Unit {
   int m, n, s;
@@ -643,6 +650,211 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// ============================================ wide CTA-pair tiles (256 x 512)
+//
+// The pair kernel's shared memory is the limit: per k-block a CTA takes
+// 32 KB of TMA writes and serves 32 KB of MMA reads for 8.4 MFLOP, about the
+// 128 bytes per clock its shared memory moves at the tensor cores' full rate.
+// Here a pair computes a 256 x 512 tile as two 256 x 256 MMAs per k-step that
+// share their A operand through the tensor core's collector buffer
+// (collector::a::fill, then ::lastuse), so A is read from shared memory once
+// for twice the work: 48 KB written and 48 KB read per 16.8 MFLOP. The 512
+// accumulator columns fill TMEM, so the accumulator is single-buffered and the
+// epilogue of a tile does not overlap the next tile's main loop: the shape
+// pays where K per tile is long.
+template <int AMN, int BMN, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    umma_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmO, const UmmaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStagesWide * kABytes;
+  uint8_t* sE = sB + kStagesWide * kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesWide + 3);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStagesWide + s); };
+  const uint32_t tfull_bar = bar0 + 8u * (2 * kStagesWide);
+  const uint32_t tempty_bar = bar0 + 8u * (2 * kStagesWide + 1);
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStagesWide + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0: the CTA that issues the MMAs
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(num_clusters_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesWide; ++s) {
+      mbar_init(full_bar(s), 1);     // used in CTA 0 only: both CTAs' loads land here
+      mbar_init(empty_bar(s), 1);    // each CTA's own, released by the pair's MMA commit
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, 2 * kEpiThreads);  // used in CTA 0: both epilogues arrive
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    tma_prefetch_map(&tmA);
+    tma_prefetch_map(&tmB);
+    tma_prefetch_map(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_units = a.num_m * a.num_n * a.num_s;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      uint32_t n_issued = 0;
+      bool failed = false;
+      for (int u = pair; u < num_units && !failed; u += npairs) {
+        const Unit t = unit_coords(a, u);
+        const int kb0 = t.s * a.kb_per_split;
+        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+        const int mA = t.m * 2 * kBM + static_cast<int>(rank) * kBM;      // this CTA's rows of A
+        const int nB0 = t.n * 2 * kBN + static_cast<int>(rank) * (kBN / 2);  // its columns, MMA 0
+        const int nB1 = nB0 + kBN;                                          // and MMA 1
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int stage = n_issued % kStagesWide;
+          const uint32_t phase = (n_issued / kStagesWide) & 1u;
+          if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, a.ctrl, a.timeout_ns)) {
+            failed = true;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytesWide);
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          const uint32_t sa = smem_u32(sA + stage * kABytes);
+          const uint32_t sb = smem_u32(sB + stage * kBBytes);
+          const int k0 = kb * kBK;
+          if (AMN == 0) {
+            tma_load_2d_pair(sa, &tmA, fb, k0, mA);
+          } else {
+            tma_load_2d_pair(sa, &tmA, fb, mA, k0);
+            tma_load_2d_pair(sa + 8192, &tmA, fb, mA + 64, k0);
+          }
+          if (BMN == 0) {
+            tma_load_2d_pair(sb, &tmB, fb, k0, nB0);
+            tma_load_2d_pair(sb + kBHalfBytes, &tmB, fb, k0, nB1);
+          } else {
+            tma_load_2d_pair(sb, &tmB, fb, nB0, k0);
+            tma_load_2d_pair(sb + 8192, &tmB, fb, nB0 + 64, k0);
+            tma_load_2d_pair(sb + kBHalfBytes, &tmB, fb, nB1, k0);
+            tma_load_2d_pair(sb + kBHalfBytes + 8192, &tmB, fb, nB1 + 64, k0);
+          }
+          ++n_issued;
+        }
+      }
+      if (failed && rank == 0) {
+        const uint32_t first = n_issued > kStagesWide ? n_issued - kStagesWide : 0;
+        for (uint32_t i = first; i < n_issued; ++i)
+          mbar_drain_wait(full_bar(i % kStagesWide), (i / kStagesWide) & 1u, a.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------- MMA issuer (CTA 0 of the pair)
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, AMN, BMN);
+      uint32_t n_consumed = 0;
+      bool issued = false, failed = false;
+      int it = 0;
+      for (int u = pair; u < num_units && !failed; u += npairs, ++it) {
+        const Unit t = unit_coords(a, u);
+        const int kb0 = t.s * a.kb_per_split;
+        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+        if (!mbar_wait_bounded_cluster(tempty_bar, (it & 1) ^ 1u, a.ctrl, a.timeout_ns)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int stage = n_consumed % kStagesWide;
+          const uint32_t phase = (n_consumed / kStagesWide) & 1u;
+          if (!mbar_wait_bounded_cluster(full_bar(stage), phase, a.ctrl, a.timeout_ns)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(sA + stage * kABytes);
+          const uint32_t sb = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = AMN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                    : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+            const uint32_t ko = BMN ? 2048u * k : 32u * k;
+            const uint64_t bd0 = BMN ? smem_desc_sw128(sb + ko, 8192u, 1024u)
+                                     : smem_desc_sw128(sb + ko, 16u, 1024u);
+            const uint64_t bd1 = BMN ? smem_desc_sw128(sb + kBHalfBytes + ko, 8192u, 1024u)
+                                     : smem_desc_sw128(sb + kBHalfBytes + ko, 16u, 1024u);
+            const uint32_t acc_in = (kb > kb0 || k > 0) ? 1u : 0u;
+            tc_mma_bf16_pair_a_fill(tmem_base, ad, bd0, idesc, acc_in);
+            tc_mma_bf16_pair_a_lastuse(tmem_base + kBN, ad, bd1, idesc, acc_in);
+          }
+          issued = true;
+          tc_commit_pair_multicast(empty_bar(stage), 0x3);
+          ++n_consumed;
+        }
+        if (failed) break;
+        tc_commit_pair_multicast(tfull_bar, 0x3);
+      }
+      if (failed && issued) {
+        tc_commit_pair(drain_bar);
+        mbar_drain_wait(drain_bar, 0, a.timeout_ns);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const bool leader = threadIdx.x == 64;
+    uint32_t ebuf = 0;
+    int it = 0;
+    for (int u = pair; u < num_units; u += npairs, ++it) {
+      const bool ok = mbar_wait_bounded_cluster(tfull_bar, it & 1, a.ctrl, a.timeout_ns);
+      if (named_bar_or(kEpiBar, kEpiThreads, !ok)) break;
+      tc_fence_after();
+      const Unit t = unit_coords(a, u);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
+      const int m0 = t.m * 2 * kBM + static_cast<int>(rank) * kBM;
+      const int n0 = t.n * 2 * kBN;
+      auto release = [&] {
+        tc_fence_before();
+        if (rank == 0)
+          mbar_arrive(tempty_bar);
+        else
+          mbar_arrive_cluster(mapa_shared(tempty_bar, 0));
+      };
+      // the two 256-column halves; the accumulator is handed back after the
+      // second half's last TMEM read (or at once if it has no valid columns)
+      epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, m0, n0, 2 * t.n, t.s, tbase, [] {});
+      if (n0 + kBN < a.cols)
+        epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, m0, n0 + kBN, 2 * t.n + 1, t.s,
+                           tbase + kBN, release);
+      else
+        release();
+    }
+    if (leader) bulk_wait_group<0>();
+  }
+
+  __syncwarp();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair's MMAs may touch its memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 // ============================================ two CTA pairs sharing B (quad)
 //
 // A cluster of four CTAs is two CTA pairs (ranks 0,1 and 2,3) on the same
@@ -1156,6 +1368,17 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   return cudaGetLastError();
 }
 
+template <int AMN, int BMN, int EPI>
+cudaError_t launch_wide_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+                          const UmmaArgs& args, int pairs, cudaStream_t s) {
+  auto kern = umma_wide_kernel<AMN, BMN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytesWide));
+  if (e != cudaSuccess) return e;
+  kern<<<2 * pairs, kThreads, kSmemBytesWide, s>>>(ta, tb, to, args);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int umma_smem_bytes() { return static_cast<int>(kSmemBytes > kSmemBytesPair ? kSmemBytes : kSmemBytesPair); }
@@ -1185,6 +1408,47 @@ cudaError_t launch_umma_pair(int kind, const CUtensorMap& a, const CUtensorMap& 
     case kUmmaCheckMK: return launch_pair<1, 0, kEpiF32>(a, b, o, args, pairs, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// wide tiles: num_n counts 512-column tiles
+cudaError_t launch_umma_wide(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                             const UmmaArgs& args, int pairs, cudaStream_t s) {
+  switch (kind) {
+    case kUmmaLogits: return launch_wide_t<0, 0, kEpiLse>(a, b, o, args, pairs, s);
+    case kUmmaDlogits: return launch_wide_t<0, 0, kEpiDlogits>(a, b, o, args, pairs, s);
+    case kUmmaDxF32: return launch_wide_t<0, 1, kEpiF32>(a, b, o, args, pairs, s);
+    case kUmmaDw: return launch_wide_t<1, 1, kEpiF32>(a, b, o, args, pairs, s);
+    case kUmmaCheckKK: return launch_wide_t<0, 0, kEpiF32>(a, b, o, args, pairs, s);
+    case kUmmaCheckMK: return launch_wide_t<1, 0, kEpiF32>(a, b, o, args, pairs, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Clusters of two that fit on the device at once for the wide kernels
+int umma_wide_max_clusters() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytesWide;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  auto kern = umma_wide_kernel<1, 1, kEpiF32>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytesWide)) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 // grid = 4 x quads (a multiple of the cluster size)

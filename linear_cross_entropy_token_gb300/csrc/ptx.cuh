@@ -368,6 +368,31 @@ __device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_des
       : "memory");
 }
 
+// The same MMA with the A operand held in the tensor core's collector buffer:
+// `fill` reads A from shared memory and keeps it, `lastuse` takes it from the
+// collector (a_desc must describe the same A) and then frees it. Two MMAs on
+// one A tile so read it from shared memory once.
+__device__ __forceinline__ void tc_mma_bf16_pair_a_fill(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16.collector::a::fill [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_bf16_pair_a_lastuse(uint32_t d_tmem, uint64_t a_desc,
+                                                           uint64_t b_desc, uint32_t idesc,
+                                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16.collector::a::lastuse [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), descriptor version 1 at bit 46, and the
 // 128-byte swizzle layout (value 2 in bits 61..63). Tiles are 1024-byte

@@ -21,7 +21,7 @@ STATUS = {0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3:
           4: "FLCE_ERR_BAD_TARGET", 5: "FLCE_ERR_TIMEOUT", 6: "FLCE_ERR_CUDA"}
 DTYPE_BF16, DTYPE_FP32 = 0, 1
 DLOGITS = {"auto": 0, "inplace": 1, "recompute": 2}
-CTA = {"auto": 0, "single": 1, "pair": 2, "quad": 3}
+CTA = {"auto": 0, "single": 1, "pair": 2, "quad": 3, "wide": 4}
 BACKWARD = {"auto": 0, "separate": 1, "one_launch": 2}
 KERNEL_KINDS = ["count_valid", "gemm_logits_lse", "lse_combine", "dlogits_inplace",
                 "gemm_dlogits_recompute", "gemm_dx", "dx_split_reduce", "gemm_dw",
@@ -47,7 +47,8 @@ class Plan(ctypes.Structure):
     _fields_ = [("chunk", ctypes.c_int64), ("num_chunks", ctypes.c_int64),
                 ("vocab_tiles", ctypes.c_int64), ("ldv", ctypes.c_int64),
                 ("dx_splits", ctypes.c_int64), ("workspace_bytes", ctypes.c_uint64),
-                ("logits_bytes", ctypes.c_uint64), ("tile_m", ctypes.c_int64)]
+                ("logits_bytes", ctypes.c_uint64), ("tile_m", ctypes.c_int64),
+                ("tile_n", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -24,7 +24,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.flce_abi_version() == 1
+    assert lib.flce_abi_version() == 2
     assert lib.flce_status_string(0) == b"FLCE_OK"
     assert lib.flce_status_string(4) == b"FLCE_ERR_BAD_TARGET"
     assert lib.flce_kernel_name(1) == b"gemm_logits_lse"

@@ -1,6 +1,7 @@
-"""The tcgen05 GEMM core alone, for each operand majorness and both tile
-shapes (one CTA per 128 x 256 tile; a CTA pair per 256 x 256 tile), against
-the float64 product of the same bf16 operands; and the bounded device wait."""
+"""The tcgen05 GEMM core alone, for each operand majorness and each tile
+shape (one CTA per 128 x 256 tile, a CTA pair per 256 x 256 tile, two pairs
+per 512 x 256 tile, a pair per 256 x 512 tile), against the float64 product
+of the same bf16 operands; and the bounded device wait."""
 import numpy as np
 import pytest
 import torch
@@ -8,7 +9,7 @@ import torch
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=["single", "pair", "quad"])
+@pytest.fixture(scope="module", params=["single", "pair", "quad", "wide"])
 def handle(request):
     from linear_cross_entropy_token_gb300 import FLCE
     h = FLCE("bf16", 0, cta=request.param)

@@ -1,6 +1,6 @@
 """Parity with the fp64 oracle on seeded random shapes: token counts, hidden
 sizes (multiples of 8), vocabulary sizes, ignore fractions, target
-distributions and chunk sizes drawn per case, on all three tile shapes, one
+distributions and chunk sizes drawn per case, on all four tile shapes, one
 handle per shape reused across the cases (workspace growth, cached tile
 orders, changing tensor maps)."""
 import numpy as np
@@ -12,7 +12,7 @@ from flce_testing import assert_parity, run
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = ("single", "pair", "quad")
+SHAPES = ("single", "pair", "quad", "wide")
 
 
 @pytest.fixture(scope="module")
@@ -41,5 +41,5 @@ def test_random_case(handles, i):
     w = workloads.generate(workloads.custom(N, H, V, "bf16", targets=targets, ignore_frac=ign,
                                             seed=i))
     ref = oracle.flce_reference(w.x_f64(), w.W_f64(), w.t, w.ignore_index)
-    res = run(handles[SHAPES[i % 3]], w, chunk=chunk)
+    res = run(handles[SHAPES[i % len(SHAPES)]], w, chunk=chunk)
     assert_parity(res, ref, "bf16", token_rtol=1e-3)
