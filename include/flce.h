@@ -81,8 +81,9 @@ enum { FLCE_DLOGITS_AUTO = 0, FLCE_DLOGITS_INPLACE = 1, FLCE_DLOGITS_RECOMPUTE =
  *  SINGLE: one CTA per 128 x 256 output tile (tcgen05 cta_group::1).
  *  PAIR:   a cluster of two CTAs on two SMs per 256 x 256 tile
  *          (tcgen05 cta_group::2): each CTA loads half of the B operand.
- *  AUTO:   PAIR (measured faster on GB300: 34.1 vs 36.9 ms for the 16384-token,
- *          128256-vocabulary step), SINGLE where pairs cannot be scheduled. */
+ *  AUTO:   WIDE (measured fastest on GB300 for the 16384-token,
+ *          128256-vocabulary step: 31.6 ms, against 34.9 ms for PAIR and
+ *          36.9 ms for SINGLE). */
 enum { FLCE_CTA_AUTO = 0, FLCE_CTA_SINGLE = 1, FLCE_CTA_PAIR = 2, FLCE_CTA_QUAD = 3,
        FLCE_CTA_WIDE = 4 };
 /*  WIDE:   CTA pairs on 256 x 512 tiles: per k-step two 256 x 256 MMAs share

@@ -102,7 +102,7 @@ Layout make_layout(int64_t N, int64_t H, int64_t C, int64_t ldv, int64_t vt, int
 }
 
 // Tile shape that FLCE_CTA_AUTO resolves to
-constexpr int kAutoCta = FLCE_CTA_PAIR;
+constexpr int kAutoCta = FLCE_CTA_WIDE;
 
 // CTAs per GEMM work unit: 1 (single), 2 (pair) or 4 (two pairs sharing B)
 int cta_group_size(const flce_config* cfg) {

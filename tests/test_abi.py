@@ -73,7 +73,10 @@ def test_plan_llama3_default_budget():
     assert p["vocab_tiles"] == 501 and p["ldv"] == 128256
     assert p["logits_bytes"] == 4096 * 128256 * 2
     assert p["workspace_bytes"] <= int(1.25 * GiB)
-    assert p["dx_splits"] == 2          # 512 dx tiles on 152 SMs: 2 splits fill the waves
+    assert p["tile_m"] == 256 and p["tile_n"] == 512   # wide CTA-pair tiles by default
+    assert p["dx_splits"] == 4          # 128 wide dx tiles on 76 SM pairs: 4 splits fill the waves
+    q = flce.plan(16384, 4096, 128256, "bf16", cta="pair")
+    assert (q["tile_n"], q["dx_splits"]) == (256, 2)   # 256 tiles of 256 x 256: 2 splits
 
 
 def test_plan_long_context_stays_O_CV():
