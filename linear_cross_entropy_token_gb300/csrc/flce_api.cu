@@ -144,8 +144,9 @@ int pick_dx_splits(int64_t C, int64_t H, int64_t V, int slots, int tile_m, int t
 // wave of consecutive units reads the k-slices of each tile row's A slab and
 // each tile column's B slab once, whatever the number of units sharing them.
 // Returns the group_m of the grouped order (1 = columns fastest, num_m =
-// rows fastest) whose waves read the fewest slabs in total.
-int pick_group_m(int num_m, int num_n, int num_s, int slots) {
+// rows fastest) whose waves read the fewest slab bytes in total (a row slab
+// weighs tile_m, a column slab tile_n).
+int pick_group_m(int num_m, int num_n, int num_s, int slots, int tile_m, int tile_n) {
   const int per_s = num_m * num_n;
   const int units = per_s * num_s;
   std::vector<int> seen_m(static_cast<size_t>(num_m) * num_s), seen_n(static_cast<size_t>(num_n) * num_s);
@@ -164,12 +165,12 @@ int pick_group_m(int num_m, int num_n, int num_s, int slots) {
       int& sm = seen_m[static_cast<size_t>(sp) * num_m + m];
       if (sm != wave) {
         sm = wave;
-        ++cost;
+        cost += tile_m;
       }
       int& sn = seen_n[static_cast<size_t>(sp) * num_n + n];
       if (sn != wave) {
         sn = wave;
-        ++cost;
+        cost += tile_n;
       }
     }
     if (best_cost < 0 || cost < best_cost) {
@@ -483,7 +484,8 @@ int group_for(flce_handle_t h, int num_m, int num_n, int num_s, int slots) {
   const std::array<int, 4> key{num_m, num_n, num_s, slots};
   auto it = h->group_cache.find(key);
   if (it != h->group_cache.end()) return it->second;
-  const int g = pick_group_m(num_m, num_n, num_s, slots);
+  const int tile_m = h->use_quad ? 4 * kBM : (h->use_pair || h->use_wide) ? 2 * kBM : kBM;
+  const int g = pick_group_m(num_m, num_n, num_s, slots, tile_m, h->use_wide ? 2 * kBN : kBN);
   h->group_cache.emplace(key, g);
   return g;
 }
