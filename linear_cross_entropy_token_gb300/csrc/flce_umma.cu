@@ -63,6 +63,7 @@ constexpr uint32_t kSmemBytesWide =
     1024 + kStagesWide * kStageBytesWide + 2 * kEpiBytes + (2 * kStagesWide + 3) * 8 + 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 192;
+constexpr int kThreadsWide = 320;   // producer warp, MMA warp, two epilogues of four warps
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kEpiBar = 1;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -131,28 +132,31 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int r, const uint32_t (&
 // epilogue threads; thread `row` owns one tile row. `release` is called right
 // after the last tcgen05.ld of the tile, handing the accumulator back to the
 // MMA issuer.
-template <int EPI, class Release>
+// NBUF staging buffers of kEpiBytes at sE (2: alternate, 1: reuse one), and
+// the named barrier `bar` over this epilogue's 128 threads.
+template <int EPI, int NBUF = 2, class Release>
 __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorMap* tmO, uint8_t* sE,
                                               uint32_t& ebuf, int row, bool leader, int m0, int n0,
                                               int n_tile, int s_idx, uint32_t tbase,
-                                              Release&& release) {
+                                              Release&& release, uint32_t bar = kEpiBar) {
+  static_assert(NBUF == 1 || NBUF == 2, "staging buffers");
   const int grow = m0 + row;
   const bool rvalid = grow < a.rows;
 
   // stage one 16 KB sub-tile and hand it to the TMA unit
   auto stage_and_store = [&](const uint32_t (&w)[32], auto&& issue) {
     uint8_t* buf = sE + ebuf * kEpiBytes;
-    if (leader) bulk_wait_group_read<1>();
-    named_bar_sync(kEpiBar, kEpiThreads);
+    if (leader) bulk_wait_group_read<NBUF - 1>();
+    named_bar_sync(bar, kEpiThreads);
     stage_row(buf, row, w);
     fence_proxy_async_smem();
-    named_bar_sync(kEpiBar, kEpiThreads);
+    named_bar_sync(bar, kEpiThreads);
     if (leader) {
       issue(smem_u32(buf));
       bulk_commit_group();
     }
     __syncwarp();
-    ebuf ^= 1u;
+    if (NBUF == 2) ebuf ^= 1u;
   };
 
   if constexpr (EPI == kEpiLse || EPI == kEpiDlogits) {
@@ -663,7 +667,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // epilogue of a tile does not overlap the next tile's main loop: the shape
 // pays where K per tile is long.
 template <int AMN, int BMN, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
     umma_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO, const UmmaArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -694,7 +698,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(empty_bar(s), 1);    // each CTA's own, released by the pair's MMA commit
     }
     mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, 2 * kEpiThreads);  // used in CTA 0: both epilogues arrive
+    mbar_init(tempty_bar, 2 * 2 * kEpiThreads);  // used in CTA 0: both CTAs' two epilogues arrive
     mbar_init(drain_bar, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -814,19 +818,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // two epilogues of four warps, one per 256-column half of the tile, each
+    // with its own staging buffer and named barrier; every thread of both
+    // hands the accumulator back after its last TMEM read
+    const int grp = (warp - 2) >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
-    const bool leader = threadIdx.x == 64;
+    const bool leader = threadIdx.x == 64 + grp * kEpiThreads;
+    const uint32_t bar = kEpiBar + static_cast<uint32_t>(grp);
+    uint8_t* sEg = sE + grp * kEpiBytes;
     uint32_t ebuf = 0;
     int it = 0;
     for (int u = pair; u < num_units; u += npairs, ++it) {
       const bool ok = mbar_wait_bounded_cluster(tfull_bar, it & 1, a.ctrl, a.timeout_ns);
-      if (named_bar_or(kEpiBar, kEpiThreads, !ok)) break;
+      if (named_bar_or(bar, kEpiThreads, !ok)) break;
       tc_fence_after();
       const Unit t = unit_coords(a, u);
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + grp * kBN;
       const int m0 = t.m * 2 * kBM + static_cast<int>(rank) * kBM;
-      const int n0 = t.n * 2 * kBN;
+      const int n0 = t.n * 2 * kBN + grp * kBN;
       auto release = [&] {
         tc_fence_before();
         if (rank == 0)
@@ -834,14 +844,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         else
           mbar_arrive_cluster(mapa_shared(tempty_bar, 0));
       };
-      // the two 256-column halves; the accumulator is handed back after the
-      // second half's last TMEM read (or at once if it has no valid columns)
-      epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, m0, n0, 2 * t.n, t.s, tbase, [] {});
-      if (n0 + kBN < a.cols)
-        epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, m0, n0 + kBN, 2 * t.n + 1, t.s,
-                           tbase + kBN, release);
+      if (n0 < a.cols)
+        epilogue_tile<EPI, 1>(a, &tmO, sEg, ebuf, row, leader, m0, n0, 2 * t.n + grp, t.s, tbase,
+                              release, bar);
       else
-        release();
+        release();   // the second half lies beyond the last column
     }
     if (leader) bulk_wait_group<0>();
   }
@@ -1375,7 +1382,7 @@ cudaError_t launch_wide_t(const CUtensorMap& ta, const CUtensorMap& tb, const CU
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytesWide));
   if (e != cudaSuccess) return e;
-  kern<<<2 * pairs, kThreads, kSmemBytesWide, s>>>(ta, tb, to, args);
+  kern<<<2 * pairs, kThreadsWide, kSmemBytesWide, s>>>(ta, tb, to, args);
   return cudaGetLastError();
 }
 
@@ -1428,7 +1435,7 @@ cudaError_t launch_umma_wide(int kind, const CUtensorMap& a, const CUtensorMap& 
 int umma_wide_max_clusters() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kThreadsWide, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytesWide;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
