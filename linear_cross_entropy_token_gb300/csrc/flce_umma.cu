@@ -57,10 +57,17 @@ constexpr uint32_t kSmemBytesPair =
     1024 + kStagesPair * kStageBytesPair + 2 * kEpiBytes + (2 * kStagesPair + 5) * 8 + 16;
 // wide CTA-pair tiles: 256 x 512, each CTA holding 128 rows of A and 256
 // columns of B per k-block
-constexpr int kStagesWide = 4;
+#ifndef FLCE_WIDE_STAGES
+#define FLCE_WIDE_STAGES 4
+#endif
+#ifndef FLCE_WIDE_EPI_BUFS
+#define FLCE_WIDE_EPI_BUFS 1
+#endif
+constexpr int kStagesWide = FLCE_WIDE_STAGES;
+constexpr int kEpiBufsWide = FLCE_WIDE_EPI_BUFS;            // staging buffers per epilogue
 constexpr uint32_t kStageBytesWide = kABytes + kBBytes;    // 48 KB per CTA
-constexpr uint32_t kSmemBytesWide =
-    1024 + kStagesWide * kStageBytesWide + 2 * kEpiBytes + (2 * kStagesWide + 3) * 8 + 16;
+constexpr uint32_t kSmemBytesWide = 1024 + kStagesWide * kStageBytesWide +
+                                    2 * kEpiBufsWide * kEpiBytes + (2 * kStagesWide + 3) * 8 + 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 192;
 constexpr int kThreadsWide = 320;   // producer warp, MMA warp, two epilogues of four warps
@@ -172,22 +179,44 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
       lse_l2 = rvalid ? a.lse[grow] * kLog2e : 0.f;
     }
     if constexpr (EPI == kEpiLse) {
-      // pass 1 over the accumulator: the tile's row max and the target logit
+      // pass 1 over the accumulator: the tile's row max and the target logit,
+      // 64 columns per TMEM wait; full groups take the max as eight
+      // independent chains
 #pragma unroll 1
-      for (int g = 0; g < kBN / 32; ++g) {
-        const int ncv = a.cols - (n0 + g * 32);
+      for (int g = 0; g < kBN / 64; ++g) {
+        const int ncv = a.cols - (n0 + g * 64);
         if (ncv <= 0) break;  // uniform across the epilogue threads
-        uint32_t r0[32];
-        tmem_ld_32x32b_x32(tbase + g * 32, r0);
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(tbase + g * 64, r0);
+        tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
         tmem_ld_wait();
+        tmem_regs_ready(r0);
+        tmem_regs_ready(r1);
+        if (ncv >= 64) {
+          float m[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < ncv) tmax = fmaxf(tmax, __uint_as_float(r0[i]));
-        if (tcol >= g * 32 && tcol < g * 32 + 32) {
-          const int k = tcol - g * 32;
+          for (int j = 0; j < 8; ++j) m[j] = fmaxf(__uint_as_float(r0[j]), __uint_as_float(r1[j]));
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 8; i < 32; ++i) {
+            m[i & 7] = fmaxf(m[i & 7], __uint_as_float(r0[i]));
+            m[i & 7] = fmaxf(m[i & 7], __uint_as_float(r1[i]));
+          }
+          tmax = fmaxf(tmax, fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])),
+                                   fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7]))));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i < ncv) tmax = fmaxf(tmax, __uint_as_float(r0[i]));
+            if (i + 32 < ncv) tmax = fmaxf(tmax, __uint_as_float(r1[i]));
+          }
+        }
+        if (tcol >= g * 64 && tcol < g * 64 + 64) {
+          const int k = tcol - g * 64;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
             if (i == k) zt = __uint_as_float(r0[i]);
+            if (i + 32 == k) zt = __uint_as_float(r1[i]);
+          }
         }
       }
     }
@@ -199,6 +228,8 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
       tmem_ld_32x32b_x32(tbase + g * 64, r0);
       tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
       tmem_ld_wait();
+      tmem_regs_ready(r0);
+      tmem_regs_ready(r1);
       if (g == last_g) release();
       const int c0 = n0 + g * 64;
       const int ncv = a.cols - c0;  // valid columns in this group, >= 1 (uniform)
@@ -207,10 +238,20 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
         // tile max, y = z - tmax, so that the largest entries are stored near
         // 0 where bf16 is most precise
         const float ml = tmax * kLog2e;
+        if (ncv >= 64) {
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (i < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r0[i]), kLog2e, -ml));
-          if (i + 32 < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r1[i]), kLog2e, -ml));
+          for (int i = 0; i < 32; ++i) {
+            s4[i & 3] += ex2_approx(fmaf(__uint_as_float(r0[i]), kLog2e, -ml));
+            s4[i & 3] += ex2_approx(fmaf(__uint_as_float(r1[i]), kLog2e, -ml));
+          }
+          tsum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r0[i]), kLog2e, -ml));
+            if (i + 32 < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r1[i]), kLog2e, -ml));
+          }
         }
         if (a.store_logits) {
           uint32_t w[32];
@@ -278,18 +319,31 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
       stage_and_store(w, [&](uint32_t src) { tma_store_2d(tmO, src, c0, m0); });
     }
   } else {  // kEpiF32
-#pragma unroll 1
-    for (int g = 0; g < kBN / 32; ++g) {
-      uint32_t r0[32];
-      tmem_ld_32x32b_x32(tbase + g * 32, r0);
+    // The TMEM reads run kAhead 32-column groups ahead of the stores, in
+    // registers. The stores are paced by the TMA unit draining the staging
+    // buffer, so the accumulator goes back to the MMA issuer after
+    // kG - kAhead store rounds rather than kG - 1, and the last rounds' stores
+    // overlap the next tile's MMAs.
+    constexpr int kG = kBN / 32;
+    constexpr int kAhead = 4;
+    static_assert(kAhead <= kG, "look-ahead");
+    uint32_t r[kAhead][32];
+#pragma unroll
+    for (int g = 0; g < kAhead; ++g) tmem_ld_32x32b_x32(tbase + g * 32, r[g]);
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      uint32_t (&cur)[32] = r[g % kAhead];
       tmem_ld_wait();
-      if (g == kBN / 32 - 1) release();
+      tmem_regs_ready(cur);
+      if (g == kG - kAhead) release();  // every column of the tile is in registers
       const int c0 = n0 + g * 32;
-      if (c0 >= a.cols) continue;
-      if (a.reduce_add)
-        stage_and_store(r0, [&](uint32_t src) { tma_reduce_add_3d(tmO, src, c0, m0, s_idx); });
-      else
-        stage_and_store(r0, [&](uint32_t src) { tma_store_3d(tmO, src, c0, m0, s_idx); });
+      if (c0 < a.cols) {  // uniform across the epilogue threads
+        if (a.reduce_add)
+          stage_and_store(cur, [&](uint32_t src) { tma_reduce_add_3d(tmO, src, c0, m0, s_idx); });
+        else
+          stage_and_store(cur, [&](uint32_t src) { tma_store_3d(tmO, src, c0, m0, s_idx); });
+      }
+      if (g + kAhead < kG) tmem_ld_32x32b_x32(tbase + (g + kAhead) * 32, cur);
     }
   }
 }
@@ -676,7 +730,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStagesWide * kABytes;
   uint8_t* sE = sB + kStagesWide * kBBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBufsWide * kEpiBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesWide + 3);
 
   const uint32_t bar0 = smem_u32(bars);
@@ -826,7 +880,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
     const int row = wq * 32 + lane;
     const bool leader = threadIdx.x == 64 + grp * kEpiThreads;
     const uint32_t bar = kEpiBar + static_cast<uint32_t>(grp);
-    uint8_t* sEg = sE + grp * kEpiBytes;
+    uint8_t* sEg = sE + grp * kEpiBufsWide * kEpiBytes;
     uint32_t ebuf = 0;
     int it = 0;
     for (int u = pair; u < num_units; u += npairs, ++it) {
@@ -845,7 +899,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
           mbar_arrive_cluster(mapa_shared(tempty_bar, 0));
       };
       if (n0 < a.cols)
-        epilogue_tile<EPI, 1>(a, &tmO, sEg, ebuf, row, leader, m0, n0, 2 * t.n + grp, t.s, tbase,
+        epilogue_tile<EPI, kEpiBufsWide>(a, &tmO, sEg, ebuf, row, leader, m0, n0, 2 * t.n + grp, t.s, tbase,
                               release, bar);
       else
         release();   // the second half lies beyond the last column
