@@ -46,7 +46,7 @@ def parse():
     p.add_argument("--config", default="llama3_bf16")
     p.add_argument("--chunk", type=int, default=0)
     p.add_argument("--budget-gib", type=float, default=0.0)
-    p.add_argument("--dlogits", choices=["auto", "inplace", "recompute"], default="auto")
+    p.add_argument("--dlogits", choices=["auto", "inplace", "recompute", "slabs"], default="auto")
     p.add_argument("--cta", choices=["auto", "single", "pair", "quad", "wide"], default="auto",
                    help="GEMM tile shape: one CTA per 128x256 tile, CTA pairs per 256x256, "
                         "or two pairs sharing B per 512x256")
@@ -439,7 +439,7 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None, "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
         "config": {"workload": args.config, "N": N, "H": H, "V": V, "chunk": plan["chunk"],
                    "num_chunks": plan["num_chunks"], "dx_splits": plan["dx_splits"],
-                   "dlogits": "recompute" if args.dlogits == "recompute" else "inplace",
+                   "dlogits": "inplace" if args.dlogits == "auto" else args.dlogits,
                    "gemm_tiles": ({(128, 256): "128x256, one CTA", (256, 256): "256x256, CTA pairs",
                                    (256, 512): "256x512, CTA pairs sharing A through the collector",
                                    (512, 256): "512x256, two CTA pairs sharing B"}[

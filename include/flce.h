@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define FLCE_ABI_VERSION 2
+#define FLCE_ABI_VERSION 3
 
 typedef struct flce_handle_s* flce_handle_t;
 
@@ -74,8 +74,20 @@ enum { FLCE_DTYPE_BF16 = 0, FLCE_DTYPE_FP32 = 1 };
  *             them with (softmax - onehot)/n_valid (the FLCE page's step 2).
  *  RECOMPUTE: the logits GEMM keeps only per-row statistics; a second GEMM
  *             recomputes each logits tile and writes dlogits directly.
- *  AUTO:      INPLACE, the faster of the two on GB300 by measurement. */
-enum { FLCE_DLOGITS_AUTO = 0, FLCE_DLOGITS_INPLACE = 1, FLCE_DLOGITS_RECOMPUTE = 2 };
+ *  SLABS:     the logits GEMM keeps only per-row statistics; the backward
+ *             then walks the vocabulary in slabs of flce_plan.vocab_slab
+ *             columns: per slab a GEMM recomputes the slab's dlogits into a
+ *             C x vocab_slab buffer (sized to stay in L2), and the dx and dW
+ *             GEMMs consume it (dx accumulated over the slabs in fp32). The
+ *             workspace no longer grows with V: O(C·(vocab_slab + H)) bytes
+ *             against O(C·V) for the other two, for 8·N·H·V FLOPs instead of
+ *             6·N·H·V (the buffer-free variant the pages leave as the next
+ *             step, with the dlogits tile held in a small L2-resident slab
+ *             rather than in registers). bf16 only: an fp32 handle returns
+ *             UNSUPPORTED.
+ *  AUTO:      INPLACE, the fastest of the three on GB300 by measurement. */
+enum { FLCE_DLOGITS_AUTO = 0, FLCE_DLOGITS_INPLACE = 1, FLCE_DLOGITS_RECOMPUTE = 2,
+       FLCE_DLOGITS_SLABS = 3 };
 
 /* Tile shape of the tcgen05 GEMMs (bf16 only).
  *  SINGLE: one CTA per 128 x 256 output tile (tcgen05 cta_group::1).
@@ -129,6 +141,8 @@ typedef struct flce_plan {
     int64_t tile_m;              /* rows of a GEMM output tile: 128 (one CTA), 256 (CTA pair,
                                     normal or wide) or 512 (two pairs)                  */
     int64_t tile_n;              /* columns of a GEMM output tile: 256, or 512 (wide)   */
+    int64_t vocab_slab;          /* SLABS: vocabulary columns per backward slab (the
+                                    buffer is chunk x vocab_slab); other modes: V       */
 } flce_plan;
 
 /* Kernel kinds, for the per-kernel timing of flce_profile_read(). */

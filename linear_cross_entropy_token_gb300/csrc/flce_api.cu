@@ -34,6 +34,13 @@ namespace {
 
 constexpr uint64_t kDefaultBudget = 5ull << 28;  // 1.25 GiB
 constexpr int64_t kMaxChunk = 32768;
+// SLABS: the slab buffer (chunk x slab bf16) is sized to stay in L2, and the
+// chunk is capped so that slabs stay many output tiles wide (at 4096 tokens
+// the per-slab dlogits and dW GEMMs of the 128256-vocabulary shape fill 98%
+// of their waves; at 8192, with half-width slabs, 86%)
+constexpr uint64_t kSlabBytes = 64ull << 20;
+constexpr int64_t kSlabAlign = 512;
+constexpr int64_t kSlabMaxChunk = 4096;
 constexpr int64_t kMaxDim = (1ll << 31) - 1;
 constexpr uint64_t kAlign = 1024;
 
@@ -195,25 +202,65 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
     *why = "dtype must be FLCE_DTYPE_BF16 or FLCE_DTYPE_FP32";
     return FLCE_ERR_UNSUPPORTED;
   }
+  if (cfg->dlogits_mode < FLCE_DLOGITS_AUTO || cfg->dlogits_mode > FLCE_DLOGITS_SLABS) {
+    *why = "dlogits_mode must be one of FLCE_DLOGITS_*";
+    return FLCE_ERR_INVALID_ARG;
+  }
   if (num_sms <= 0) num_sms = 152;
   const bool bf16 = cfg->dtype == FLCE_DTYPE_BF16;
+  const bool slabs = cfg->dlogits_mode == FLCE_DLOGITS_SLABS;
+  if (slabs && !bf16) {
+    *why = "FLCE_DLOGITS_SLABS runs on the bf16 tcgen05 path only";
+    return FLCE_ERR_UNSUPPORTED;
+  }
   const int esize = bf16 ? 2 : 4;
   const uint64_t budget = cfg->hbm_budget_bytes ? cfg->hbm_budget_bytes : kDefaultBudget;
   std::memset(out, 0, sizeof(*out));
-  out->ldv = static_cast<int64_t>(align_up(static_cast<uint64_t>(V), 64));
   out->vocab_tiles = cdiv(V, kVocabTile);
   const int group = cta_group_size(cfg);
+  const int slots = num_sms / group;
+  const int tile_m = group * kBM, tile_n = tile_cols(cfg);
+  // SLABS: the widest slab (a multiple of 512 columns) whose C x slab buffer
+  // fits kSlabBytes, narrowed where that fills the waves of the per-slab
+  // dlogits GEMM (C x slab tiles) and dW GEMM (slab x H tiles) better; within
+  // half a percent the wider slab wins
+  auto slab_for = [&](int64_t C) -> int64_t {
+    if (!slabs) return V;
+    const int64_t cmax = std::max<int64_t>(
+        kSlabAlign, static_cast<int64_t>(kSlabBytes / (2 * static_cast<uint64_t>(std::max<int64_t>(C, 1)))) /
+                        kSlabAlign * kSlabAlign);
+    if (cmax >= V) return V;
+    auto eff = [&](int64_t units) {
+      return static_cast<double>(units) / static_cast<double>(cdiv(units, slots) * slots);
+    };
+    int64_t best = cmax;
+    double best_eff = -1;
+    for (int64_t vs = cmax; vs >= kSlabAlign; vs -= kSlabAlign) {
+      const double e = 0.5 * (eff(cdiv(std::max<int64_t>(C, 1), tile_m) * cdiv(vs, tile_n)) +
+                              eff(cdiv(vs, tile_m) * cdiv(H, tile_n)));
+      if (e > best_eff + 0.005) {
+        best_eff = e;
+        best = vs;
+      }
+    }
+    return best;
+  };
+  auto ldv_for = [&](int64_t C) {
+    return static_cast<int64_t>(align_up(static_cast<uint64_t>(slab_for(C)), 64));
+  };
+  // SLABS accumulate dx over the slabs in one fp32 buffer (one split)
   auto splits_for = [&](int64_t C) {
-    return bf16 ? pick_dx_splits(C, H, V, num_sms / group, group * kBM, tile_cols(cfg)) : 0;
+    return bf16 ? (slabs ? 1 : pick_dx_splits(C, H, V, slots, tile_m, tile_n)) : 0;
   };
   auto ws = [&](int64_t C) {
-    return make_layout(N, H, C, out->ldv, out->vocab_tiles, splits_for(C), esize).total;
+    return make_layout(N, H, C, ldv_for(C), out->vocab_tiles, splits_for(C), esize).total;
   };
+  const int64_t max_chunk = slabs ? kSlabMaxChunk : kMaxChunk;
   int64_t C;
   if (N == 0) {
     C = 0;
   } else if (chunk > 0) {
-    C = std::min<int64_t>(std::min(chunk, N), kMaxChunk);
+    C = std::min<int64_t>(std::min(chunk, N), max_chunk);
     if (ws(C) > budget) {
       char b[200];
       std::snprintf(b, sizeof b, "chunk %lld needs %llu workspace bytes, above the budget %llu",
@@ -223,7 +270,7 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
       return FLCE_ERR_BUDGET;
     }
   } else {
-    const int64_t cap = std::min<int64_t>(kMaxChunk, static_cast<int64_t>(align_up(N, kBM)));
+    const int64_t cap = std::min<int64_t>(max_chunk, static_cast<int64_t>(align_up(N, kBM)));
     int64_t cmax = 0;
     for (int64_t c = kBM; c <= cap; c += kBM)
       if (ws(c) <= budget) cmax = c;
@@ -241,12 +288,14 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   }
   out->chunk = C;
   out->num_chunks = C ? cdiv(N, C) : 0;
+  out->vocab_slab = slab_for(C);
+  out->ldv = ldv_for(C);
   out->dx_splits = std::max<int64_t>(1, C ? splits_for(C) : 1);
   out->workspace_bytes =
       make_layout(N, H, C, out->ldv, out->vocab_tiles, C ? splits_for(C) : 0, esize).total;
   out->logits_bytes = static_cast<uint64_t>(C) * out->ldv * esize;
-  out->tile_m = group * kBM;
-  out->tile_n = tile_cols(cfg);
+  out->tile_m = tile_m;
+  out->tile_n = tile_n;
   return FLCE_OK;
 }
 
@@ -637,9 +686,12 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     __nv_bfloat16* logits = reinterpret_cast<__nv_bfloat16*>(ws + L.logits);
     float* dxpart = reinterpret_cast<float*>(ws + L.dxpart);
     const bool recompute = h->cfg.dlogits_mode == FLCE_DLOGITS_RECOMPUTE;
+    const bool slabs = h->cfg.dlogits_mode == FLCE_DLOGITS_SLABS;
+    const int64_t zw = slabs ? p.vocab_slab : V;  // columns of the chunk buffer
+    const int b_box = h->use_quad ? 64 : (h->use_pair || h->use_wide) ? 128 : 256;
     CUtensorMap mW_k, mW_mn, mX_k, mX_mn, mZ_out, mZ_k, mZ_mn, mDx, mDw;
     // a CTA of a pair loads 128 of the tile's 256 columns of a K-major B
-    if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, h->use_quad ? 64 : (h->use_pair || h->use_wide) ? 128 : 256, &why) ||
+    if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, b_box, &why) ||
         !map_bf16_2d(&mW_mn, W, H, V, H * 2, 64, 64, &why) ||
         !map_f32_3d(&mDw, dW, H, V, 1, H * 4, static_cast<uint64_t>(V) * H * 4, &why))
       return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
@@ -655,9 +707,9 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       const void* xc = xb + off * H;
       if (!map_bf16_2d(&mX_k, xc, H, rows, H * 2, 64, 128, &why) ||
           !map_bf16_2d(&mX_mn, xc, H, rows, H * 2, 64, 64, &why) ||
-          !map_bf16_2d(&mZ_out, logits, V, rows, ldv * 2, 64, 128, &why) ||
-          !map_bf16_2d(&mZ_k, logits, V, rows, ldv * 2, 64, 128, &why) ||
-          !map_bf16_2d(&mZ_mn, logits, V, rows, ldv * 2, 64, 64, &why))
+          !map_bf16_2d(&mZ_out, logits, zw, rows, ldv * 2, 64, 128, &why) ||
+          !map_bf16_2d(&mZ_k, logits, zw, rows, ldv * 2, 64, 128, &why) ||
+          !map_bf16_2d(&mZ_mn, logits, zw, rows, ldv * 2, 64, 64, &why))
         return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
 
       // 1. projection with the online max / sum-exp epilogue
@@ -670,7 +722,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       a.rows = rows;
       a.cols = static_cast<int>(V);
       a.vocab_tiles = vt;
-      a.store_logits = recompute ? 0 : 1;
+      a.store_logits = (recompute || slabs) ? 0 : 1;
       a.ignore_index = ignore_index;
       a.targets = t + off;
       a.partials = partials;
@@ -680,11 +732,67 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       a.ctrl = ctrl;
       a.timeout_ns = h->timeout_ns;
       FLCE_LAUNCH(FLCE_K_GEMM_LOGITS, 2 * dr * dH * dV,
-                  2 * dr * dH + 2 * dV * dH + (recompute ? 0 : 2 * dr * dV) + 8 * dr * vt + 12 * dr,
+                  2 * dr * dH + 2 * dV * dH + ((recompute || slabs) ? 0 : 2 * dr * dV) + 8 * dr * vt + 12 * dr,
                   launch_gemm(h, kUmmaLogits, mX_k, mW_k, mZ_out, a, rows, s));
       // 2a. cross-tile log-sum-exp and token losses
       FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
                   launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
+      if (slabs) {
+        // 2b-4, slab by slab: the slab's dlogits recomputed into the chunk
+        // buffer (C x vocab_slab), then dx (+)= d_s · W_s into one fp32
+        // buffer (stored by the first slab, added by the others, in slab
+        // order) and dW_s (+)= d_sᵀ · x_c
+        const int64_t Vs = p.vocab_slab;
+        const int64_t n_slabs = cdiv(V, Vs);
+        const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
+        CUtensorMap mWs_k, mWs_mn, mZs_out, mZs_k, mZs_mn, mDws, mDxs;
+        if (!map_f32_3d(&mDxs, dxpart, H, rows, 1, H * 4, static_cast<uint64_t>(C) * H * 4, &why))
+          return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
+        for (int64_t sl = 0; sl < n_slabs; ++sl) {
+          const int64_t v0 = sl * Vs;
+          const int64_t vs = std::min(Vs, V - v0);
+          const double dvs = static_cast<double>(vs);
+          if (!map_bf16_2d(&mWs_k, Wb + v0 * H, H, vs, H * 2, 64, b_box, &why) ||
+              !map_bf16_2d(&mWs_mn, Wb + v0 * H, H, vs, H * 2, 64, 64, &why) ||
+              !map_f32_3d(&mDws, dW + v0 * H, H, vs, 1, H * 4, static_cast<uint64_t>(vs) * H * 4, &why) ||
+              !map_bf16_2d(&mZs_out, logits, vs, rows, ldv * 2, 64, 128, &why) ||
+              !map_bf16_2d(&mZs_k, logits, vs, rows, ldv * 2, 64, 128, &why) ||
+              !map_bf16_2d(&mZs_mn, logits, vs, rows, ldv * 2, 64, 64, &why))
+            return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
+          UmmaArgs g = a;
+          g.num_n = static_cast<int>(cdiv(vs, kBN));
+          g.cols = static_cast<int>(vs);
+          g.col_base = v0;
+          FLCE_LAUNCH(FLCE_K_GEMM_DLOGITS, 2 * dr * dH * dvs, 2 * dr * dH + 2 * dvs * dH + 2 * dr * dvs + 12 * dr,
+                      launch_gemm(h, kUmmaDlogits, mX_k, mWs_k, mZs_out, g, rows, s));
+          UmmaArgs b = a;
+          b.num_n = static_cast<int>(cdiv(H, kBN));
+          b.num_s = 1;
+          b.kb_total = static_cast<int>(cdiv(vs, kBK));
+          b.kb_per_split = b.kb_total;
+          b.raster = 2;
+          b.rows = rows;
+          b.cols = static_cast<int>(H);
+          b.reduce_add = sl > 0 ? 1 : 0;
+          FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dvs * dH, 2 * dr * dvs + 2 * dvs * dH + (sl > 0 ? 8.0 : 4.0) * dr * dH,
+                      launch_gemm(h, kUmmaDxF32, mZs_k, mWs_mn, mDxs, b, rows, s));
+          UmmaArgs d = a;
+          d.num_n = static_cast<int>(cdiv(H, kBN));
+          d.num_s = 1;
+          d.kb_total = static_cast<int>(cdiv(rows, kBK));
+          d.kb_per_split = d.kb_total;
+          d.raster = 1;
+          d.rows = static_cast<int>(vs);
+          d.cols = static_cast<int>(H);
+          d.reduce_add = c > 0 ? 1 : 0;
+          FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dvs * dH, 2 * dr * dvs + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dvs * dH,
+                      launch_gemm(h, kUmmaDw, mZs_mn, mX_mn, mDws, d, vs, s));
+        }
+        FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4 * dr * dH + 2 * dr * dH,
+                    launch_dx_reduce(dxpart, 1, C * H, rows, H, Wb, V, t + off, ignore_index, ctrl, dcorr,
+                                     dxb + off * H, s));
+        continue;
+      }
       // 2b. dlogits = (softmax - onehot) / n_valid over the chunk buffer
       if (recompute) {
         FLCE_LAUNCH(FLCE_K_GEMM_DLOGITS, 2 * dr * dH * dV, 2 * dr * dH + 2 * dV * dH + 2 * dr * dV + 12 * dr,
@@ -825,6 +933,10 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
   if (!out || !cfg) return FLCE_ERR_INVALID_ARG;
   *out = nullptr;
   if (cfg->dtype != FLCE_DTYPE_BF16 && cfg->dtype != FLCE_DTYPE_FP32) return FLCE_ERR_UNSUPPORTED;
+  if (cfg->dlogits_mode < FLCE_DLOGITS_AUTO || cfg->dlogits_mode > FLCE_DLOGITS_SLABS)
+    return FLCE_ERR_INVALID_ARG;
+  if (cfg->dlogits_mode == FLCE_DLOGITS_SLABS && cfg->dtype != FLCE_DTYPE_BF16)
+    return FLCE_ERR_UNSUPPORTED;
   int count = 0;
   if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
     cudaGetLastError();

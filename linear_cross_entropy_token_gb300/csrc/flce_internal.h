@@ -56,6 +56,7 @@ struct UmmaArgs {
   int32_t store_logits;          // kEpiLse: 1 = also store bf16 logits
   int32_t group_m;               // raster 2: tile rows per group
   int64_t ignore_index;
+  int64_t col_base;              // kEpiLse / kEpiDlogits: vocabulary index of output column 0
   const int64_t* targets;        // targets of this chunk's tokens
   float2* partials;              // [rows][vocab_tiles] (running max, sum of exp)
   float* zt;                     // [rows] fp32 target logit

@@ -170,7 +170,8 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
     int64_t tg = -1;
     if (rvalid) tg = a.targets[grow];
     const bool tvalid = rvalid && tg != a.ignore_index;
-    const int tcol = (tvalid && tg >= n0 && tg < n0 + kBN) ? static_cast<int>(tg - n0) : -1;
+    const int64_t tl = tg - a.col_base;  // target column in this GEMM's output
+    const int tcol = (tvalid && tl >= n0 && tl < n0 + kBN) ? static_cast<int>(tl - n0) : -1;
     float tmax = -INFINITY, tsum = 0.f, zt = 0.f;
     float scale = 0.f, lse_l2 = 0.f;
     if constexpr (EPI == kEpiDlogits) {

@@ -20,7 +20,7 @@ FLCE_OK = 0
 STATUS = {0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3: "FLCE_ERR_BUDGET",
           4: "FLCE_ERR_BAD_TARGET", 5: "FLCE_ERR_TIMEOUT", 6: "FLCE_ERR_CUDA"}
 DTYPE_BF16, DTYPE_FP32 = 0, 1
-DLOGITS = {"auto": 0, "inplace": 1, "recompute": 2}
+DLOGITS = {"auto": 0, "inplace": 1, "recompute": 2, "slabs": 3}
 CTA = {"auto": 0, "single": 1, "pair": 2, "quad": 3, "wide": 4}
 BACKWARD = {"auto": 0, "separate": 1, "one_launch": 2}
 KERNEL_KINDS = ["count_valid", "gemm_logits_lse", "lse_combine", "dlogits_inplace",
@@ -48,7 +48,7 @@ class Plan(ctypes.Structure):
                 ("vocab_tiles", ctypes.c_int64), ("ldv", ctypes.c_int64),
                 ("dx_splits", ctypes.c_int64), ("workspace_bytes", ctypes.c_uint64),
                 ("logits_bytes", ctypes.c_uint64), ("tile_m", ctypes.c_int64),
-                ("tile_n", ctypes.c_int64)]
+                ("tile_n", ctypes.c_int64), ("vocab_slab", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -126,10 +126,10 @@ def make_config(dtype: str = "bf16", device: int = 0, hbm_budget_bytes: int = 0,
 
 
 def plan(N: int, H: int, V: int, dtype: str = "bf16", chunk: int = 0, hbm_budget_bytes: int = 0,
-         num_sms: int = 0, cta: str = "auto") -> dict:
+         num_sms: int = 0, cta: str = "auto", dlogits_mode: str = "auto") -> dict:
     """The token-chunk plan for one call (host only; no device needed)."""
     lib = load()
-    cfg = make_config(dtype, 0, hbm_budget_bytes, cta=cta)
+    cfg = make_config(dtype, 0, hbm_budget_bytes, dlogits_mode, cta=cta)
     p = Plan()
     st = lib.flce_make_plan(ctypes.byref(cfg), N, H, V, chunk, num_sms, ctypes.byref(p))
     if st != FLCE_OK:

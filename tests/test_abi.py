@@ -24,7 +24,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.flce_abi_version() == 2
+    assert lib.flce_abi_version() == 3
     assert lib.flce_status_string(0) == b"FLCE_OK"
     assert lib.flce_status_string(4) == b"FLCE_ERR_BAD_TARGET"
     assert lib.flce_kernel_name(1) == b"gemm_logits_lse"
@@ -119,6 +119,39 @@ def test_plan_balances_chunks():
         assert 0 < last <= p["chunk"]
         # no chunk is more than one 128-token tile longer than an even split
         assert p["chunk"] - N / p["num_chunks"] < 128
+
+
+def test_plan_slabs_bounded_in_V():
+    """SLABS: the chunk buffer holds one vocabulary slab (a multiple of 512
+    columns, at most 64 MiB), so the workspace no longer grows with V."""
+    p = flce.plan(16384, 4096, 128256, "bf16", dlogits_mode="slabs")
+    vs = p["vocab_slab"]
+    assert vs % 512 == 0 and p["chunk"] * vs * 2 <= 64 << 20
+    assert p["ldv"] == vs and p["logits_bytes"] == p["chunk"] * vs * 2
+    assert p["dx_splits"] == 1
+    # 256-row x 512-column tiles on 76 SM pairs: the slab is narrowed from
+    # 8192 to 7168 columns, where the dlogits GEMM (16 x 14 tiles) and the dW
+    # GEMM (28 x 8 tiles) both run 224 units, 3 waves of 76 at 98%
+    assert (p["chunk"], vs) == (4096, 7168)
+    inplace = flce.plan(16384, 4096, 128256, "bf16")
+    assert p["workspace_bytes"] < inplace["workspace_bytes"]
+    # doubling V leaves the slab workspace unchanged
+    q = flce.plan(16384, 4096, 256512, "bf16", dlogits_mode="slabs", chunk=p["chunk"])
+    assert q["workspace_bytes"] - p["workspace_bytes"] <= p["chunk"] * 8 * (q["vocab_tiles"] - p["vocab_tiles"]) + 4096
+    # a small budget still plans, with a narrower chunk
+    r = flce.plan(16384, 4096, 128256, "bf16", dlogits_mode="slabs", hbm_budget_bytes=256 << 20)
+    assert r["workspace_bytes"] <= 256 << 20 and r["chunk"] >= 1024
+    # an explicit chunk above 4096 tokens is clamped to 4096
+    assert flce.plan(16384, 4096, 128256, "bf16", dlogits_mode="slabs", chunk=16384)["chunk"] == 4096
+    with pytest.raises(flce.FlceError) as e:
+        flce.plan(16384, 4096, 128256, "bf16", dlogits_mode="slabs", hbm_budget_bytes=64 << 20, chunk=4096)
+    assert e.value.status_name == "FLCE_ERR_BUDGET"
+    # a vocabulary narrower than one slab is one slab
+    s = flce.plan(2048, 1024, 4000, "bf16", dlogits_mode="slabs")
+    assert s["vocab_slab"] == 4000 and s["ldv"] == 4032
+    with pytest.raises(flce.FlceError) as e:
+        flce.plan(256, 128, 4096, "fp32", dlogits_mode="slabs")
+    assert e.value.status_name == "FLCE_ERR_UNSUPPORTED"
 
 
 def test_plan_rejects_bad_sizes():

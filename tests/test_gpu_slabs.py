@@ -1,0 +1,125 @@
+"""The vocabulary-slab backward (FLCE_DLOGITS_SLABS): its workspace does not
+grow with V, and it reaches the oracle's result like the other two modes.
+Shapes are picked so that the planned slab is narrower than V (several
+slabs, the last one ragged) as well as wider (one slab), on every tile
+shape; the full-size Llama-3-shaped batch is checked on sampled outputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from flce_testing import assert_parity, rel_fro, run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", params=["wide", "pair", "single", "quad"])
+def slabs(request):
+    from linear_cross_entropy_token_gb300 import FLCE
+    h = FLCE("bf16", 0, dlogits_mode="slabs", cta=request.param)
+    yield h
+    h.close()
+
+
+def _oracle(w, chunk=512):
+    return oracle.flce_reference(w.x_f64(), w.W_f64(), w.t, w.ignore_index, chunk=chunk)
+
+
+def _slab_count(res, V):
+    return math.ceil(V / res["plan"]["vocab_slab"])
+
+
+def test_small_bf16_config(slabs):
+    w = workloads.make("small_bf16")
+    res = run(slabs, w)
+    assert _slab_count(res, w.V) >= 2       # 2048 tokens: slabs of at most 16384 columns
+    assert_parity(res, _oracle(w), "bf16", token_rtol=1e-3)
+
+
+@pytest.mark.parametrize("N,H,V,chunk,ign,targets,min_slabs", [
+    (2048, 64, 70001, 0, 0.1, "uniform", 5),     # several slabs, the last ragged; odd V
+    (4096, 128, 20000, 0, 0.05, "zipf", 3),      # targets crowd the first slab
+    (3000, 72, 33333, 1500, 0.1, "uniform", 2),  # ragged chunks, a K tail, C % 256 != 0
+    (1000, 256, 4099, 300, 0.1, "uniform", 1),   # one slab wider than V
+    (130, 64, 300, 0, 0.0, "uniform", 1),        # smaller than one tile along every axis
+    (200, 64, 1, 0, 0.1, "uniform", 1),          # one class: every loss and gradient is 0
+])
+def test_shapes(slabs, N, H, V, chunk, ign, targets, min_slabs):
+    w = workloads.generate(workloads.custom(N, H, V, "bf16", targets=targets, ignore_frac=ign,
+                                            seed=N + 7 * V))
+    res = run(slabs, w, chunk=chunk)
+    assert _slab_count(res, V) >= min_slabs
+    assert_parity(res, _oracle(w), "bf16", token_rtol=1e-3)
+
+
+def test_matches_inplace_mode():
+    """Same inputs, the in-place mode: equal loss, and gradients within the
+    bf16 rounding of dlogits."""
+    from linear_cross_entropy_token_gb300 import FLCE
+    w = workloads.generate(workloads.custom(4096, 256, 30000, "bf16", ignore_frac=0.1, seed=12))
+    a_h, b_h = FLCE("bf16", 0), FLCE("bf16", 0, dlogits_mode="slabs")
+    try:
+        a = run(a_h, w, chunk=4096)
+        b = run(b_h, w, chunk=4096)
+    finally:
+        a_h.close()
+        b_h.close()
+    assert _slab_count(b, w.V) >= 3
+    assert b["plan"]["workspace_bytes"] < a["plan"]["workspace_bytes"]
+    assert abs(a["loss"] - b["loss"]) <= 1e-6 * abs(a["loss"])
+    assert rel_fro(b["dx"], a["dx"]) <= 5e-3 and rel_fro(b["dW"], a["dW"]) <= 5e-3
+
+
+def test_all_tokens_ignored(slabs):
+    w = workloads.generate(workloads.custom(2048, 64, 40000, "bf16", seed=13))
+    w.t[:] = -100
+    res = run(slabs, w)
+    assert res["loss"] == 0.0
+    assert np.all(res["dx"] == 0.0) and np.all(res["dW"] == 0.0)
+
+
+def test_zero_weight_closed_form(slabs):
+    """W = 0 over several slabs: loss = ln V, dx = 0 exactly, and
+    dW_j = (1/n_v)(sum_valid x_i / V - sum_{valid, t_i = j} x_i)."""
+    V = 40000
+    w = workloads.generate(workloads.custom(2048, 64, V, "bf16", ignore_frac=0.1, seed=14))
+    w.W[:] = 0
+    res = run(slabs, w)
+    assert _slab_count(res, V) >= 2
+    assert abs(res["loss"] - math.log(V)) <= 2e-6 * math.log(V)
+    assert np.all(res["dx"] == 0.0)
+    x = w.x_f64()
+    valid = w.t != -100
+    dW = np.tile(x[valid].sum(0) / V, (V, 1))
+    np.subtract.at(dW, w.t[valid], x[valid])
+    dW /= valid.sum()
+    assert rel_fro(res["dW"], dW) <= 1e-2
+
+
+def test_repeatable_bit_for_bit(slabs):
+    """dx accumulates over the slabs in slab order: no atomics race."""
+    w = workloads.generate(workloads.custom(2048, 128, 40000, "bf16", ignore_frac=0.1, seed=15))
+    a = run(slabs, w)
+    b = run(slabs, w)
+    assert a["loss"] == b["loss"]
+    assert np.array_equal(a["dx"], b["dx"]) and np.array_equal(a["dW"], b["dW"])
+
+
+@pytest.mark.slow
+def test_llama3_sampled_and_memory():
+    """The 16,384-token, 128,256-vocabulary batch: sampled outputs against
+    the oracle, and an extra HBM footprint far below one chunk of logits."""
+    from test_gpu_fullsize import Ref, _check
+    from linear_cross_entropy_token_gb300 import FLCE
+    w = workloads.make("llama3_bf16")
+    ref = Ref(w)
+    h = FLCE("bf16", 0, dlogits_mode="slabs")
+    try:
+        plan = _check(h, w, ref)
+    finally:
+        h.close()
+    assert plan["chunk"] == 4096 and plan["vocab_slab"] == 7168
+    assert plan["workspace_bytes"] < 0.15e9 < 4096 * w.V * 2
