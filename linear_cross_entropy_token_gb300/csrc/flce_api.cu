@@ -34,12 +34,18 @@ namespace {
 
 constexpr uint64_t kDefaultBudget = 5ull << 28;  // 1.25 GiB
 constexpr int64_t kMaxChunk = 32768;
-// SLABS: the slab buffer (chunk x slab bf16) is sized to stay in L2, and the
-// chunk is capped so that slabs stay many output tiles wide (at 4096 tokens
-// the per-slab dlogits and dW GEMMs of the 128256-vocabulary shape fill 98%
-// of their waves; at 8192, with half-width slabs, 86%)
-constexpr uint64_t kSlabBytes = 64ull << 20;
+// SLABS: the slab buffer (chunk x slab bf16) takes what the budget leaves,
+// up to 256 MiB: wider slabs mean fewer, longer GEMM launches (at the
+// 128256-vocabulary shape 5 slabs of 29184 columns ran 39.7 ms per step,
+// 14 of 9728 41.1 ms and 18 of 7168 41.7 ms). The chunk is capped at 4096
+// tokens: the dx accumulator (C x H fp32) grows with it and leaves less room
+// for the slab.
+#ifndef FLCE_SLAB_MIB
+#define FLCE_SLAB_MIB 256
+#endif
+constexpr uint64_t kSlabBytes = static_cast<uint64_t>(FLCE_SLAB_MIB) << 20;
 constexpr int64_t kSlabAlign = 512;
+constexpr int64_t kMinSlab = 8192;
 constexpr int64_t kSlabMaxChunk = 4096;
 constexpr int64_t kMaxDim = (1ll << 31) - 1;
 constexpr uint64_t kAlign = 1024;
@@ -220,15 +226,22 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   const int group = cta_group_size(cfg);
   const int slots = num_sms / group;
   const int tile_m = group * kBM, tile_n = tile_cols(cfg);
+  // SLABS accumulate dx over the slabs in one fp32 buffer (one split)
+  auto splits_for = [&](int64_t C) {
+    return bf16 ? (slabs ? 1 : pick_dx_splits(C, H, V, slots, tile_m, tile_n)) : 0;
+  };
   // SLABS: the widest slab (a multiple of 512 columns) whose C x slab buffer
-  // fits kSlabBytes, narrowed where that fills the waves of the per-slab
-  // dlogits GEMM (C x slab tiles) and dW GEMM (slab x H tiles) better; within
-  // half a percent the wider slab wins
+  // fits both kSlabBytes and what the budget leaves beside the rest of the
+  // workspace, narrowed where that fills the waves of the per-slab dlogits
+  // GEMM (C x slab tiles) and dW GEMM (slab x H tiles) better; within half a
+  // percent the wider slab wins. Below 512 columns the workspace exceeds the
+  // budget and the planner tries a smaller chunk.
   auto slab_for = [&](int64_t C) -> int64_t {
     if (!slabs) return V;
-    const int64_t cmax = std::max<int64_t>(
-        kSlabAlign, static_cast<int64_t>(kSlabBytes / (2 * static_cast<uint64_t>(std::max<int64_t>(C, 1)))) /
-                        kSlabAlign * kSlabAlign);
+    const uint64_t cc = static_cast<uint64_t>(std::max<int64_t>(C, 1));
+    const uint64_t rest = make_layout(N, H, C, 0, out->vocab_tiles, splits_for(C), esize).total + kAlign;
+    const uint64_t room = budget > rest ? std::min(kSlabBytes, budget - rest) : 0;
+    const int64_t cmax = std::max<int64_t>(kSlabAlign, static_cast<int64_t>(room / (2 * cc)) / kSlabAlign * kSlabAlign);
     if (cmax >= V) return V;
     auto eff = [&](int64_t units) {
       return static_cast<double>(units) / static_cast<double>(cdiv(units, slots) * slots);
@@ -247,10 +260,6 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   };
   auto ldv_for = [&](int64_t C) {
     return static_cast<int64_t>(align_up(static_cast<uint64_t>(slab_for(C)), 64));
-  };
-  // SLABS accumulate dx over the slabs in one fp32 buffer (one split)
-  auto splits_for = [&](int64_t C) {
-    return bf16 ? (slabs ? 1 : pick_dx_splits(C, H, V, slots, tile_m, tile_n)) : 0;
   };
   auto ws = [&](int64_t C) {
     return make_layout(N, H, C, ldv_for(C), out->vocab_tiles, splits_for(C), esize).total;
@@ -272,8 +281,16 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   } else {
     const int64_t cap = std::min<int64_t>(max_chunk, static_cast<int64_t>(align_up(N, kBM)));
     int64_t cmax = 0;
-    for (int64_t c = kBM; c <= cap; c += kBM)
-      if (ws(c) <= budget) cmax = c;
+    if (slabs) {
+      // the largest chunk that still leaves slabs kMinSlab columns wide: a
+      // narrower slab multiplies the launches (chunks x slabs) faster than a
+      // shorter chunk does
+      for (int64_t c = cap; c >= kBM && cmax == 0; c -= kBM)
+        if (ws(c) <= budget && slab_for(c) >= std::min<int64_t>(V, kMinSlab)) cmax = c;
+    }
+    if (cmax == 0)
+      for (int64_t c = kBM; c <= cap; c += kBM)
+        if (ws(c) <= budget) cmax = c;
     if (cmax == 0) {
       const int64_t c = std::min<int64_t>(N, kBM);
       if (ws(c) <= budget) cmax = c;
@@ -337,6 +354,11 @@ struct flce_handle_s {
   };
   Slot slots[2];
   cudaStream_t copy_stream = nullptr;
+  // SLABS: the dW GEMM of a slab runs on a second stream beside the dx GEMM
+  // of the same slab, so each fills the other's last wave
+  cudaStream_t side_stream = nullptr;
+  cudaEvent_t slab_ready = nullptr;  // the slab's dlogits are in the buffer
+  cudaEvent_t slab_freed = nullptr;  // the slab's dW GEMM has read the buffer
   uint64_t next_ticket = 1;
   flce_plan last_plan{};
   int64_t last_N = -1;
@@ -651,6 +673,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
 
   const int64_t C = p.chunk, ldv = p.ldv;
   const int vt = static_cast<int>(p.vocab_tiles);
+  bool side_pending = false;  // SLABS: this call has work on the side stream
   const double dV = static_cast<double>(V), dH = static_cast<double>(H);
 
   if (!bf16) {
@@ -746,6 +769,13 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
         const int64_t n_slabs = cdiv(V, Vs);
         const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
         CUtensorMap mWs_k, mWs_mn, mZs_out, mZs_k, mZs_mn, mDws, mDxs;
+        if (!h->side_stream) {
+          e = cudaStreamCreateWithFlags(&h->side_stream, cudaStreamNonBlocking);
+          if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slab_ready, cudaEventDisableTiming);
+          if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slab_freed, cudaEventDisableTiming);
+          if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
+        }
+        const cudaStream_t side = h->side_stream;
         if (!map_f32_3d(&mDxs, dxpart, H, rows, 1, H * 4, static_cast<uint64_t>(C) * H * 4, &why))
           return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
         for (int64_t sl = 0; sl < n_slabs; ++sl) {
@@ -763,8 +793,17 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
           g.num_n = static_cast<int>(cdiv(vs, kBN));
           g.cols = static_cast<int>(vs);
           g.col_base = v0;
+          // the previous slab's dW GEMM (on the side stream) has read the
+          // buffer; earlier calls' are ordered by the join that ends them
+          if (side_pending) {
+            e = cudaStreamWaitEvent(s, h->slab_freed, 0);
+            if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab wait: %s", cudaGetErrorString(e));
+          }
           FLCE_LAUNCH(FLCE_K_GEMM_DLOGITS, 2 * dr * dH * dvs, 2 * dr * dH + 2 * dvs * dH + 2 * dr * dvs + 12 * dr,
                       launch_gemm(h, kUmmaDlogits, mX_k, mWs_k, mZs_out, g, rows, s));
+          e = cudaEventRecord(h->slab_ready, s);
+          if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->slab_ready, 0);
+          if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab fork: %s", cudaGetErrorString(e));
           UmmaArgs b = a;
           b.num_n = static_cast<int>(cdiv(H, kBN));
           b.num_s = 1;
@@ -785,8 +824,14 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
           d.rows = static_cast<int>(vs);
           d.cols = static_cast<int>(H);
           d.reduce_add = c > 0 ? 1 : 0;
-          FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dvs * dH, 2 * dr * dvs + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dvs * dH,
-                      launch_gemm(h, kUmmaDw, mZs_mn, mX_mn, mDws, d, vs, s));
+          {
+            const cudaStream_t s = side;  // the launch and its timing events go on the side stream
+            FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dvs * dH, 2 * dr * dvs + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dvs * dH,
+                        launch_gemm(h, kUmmaDw, mZs_mn, mX_mn, mDws, d, vs, s));
+          }
+          e = cudaEventRecord(h->slab_freed, side);
+          if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab join: %s", cudaGetErrorString(e));
+          side_pending = true;
         }
         FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4 * dr * dH + 2 * dr * dH,
                     launch_dx_reduce(dxpart, 1, C * H, rows, H, Wb, V, t + off, ignore_index, ctrl, dcorr,
@@ -869,6 +914,11 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     }
   }
   FLCE_LAUNCH(FLCE_K_LOSS_FINALIZE, 0.0, 4.0 * N, launch_loss_finalize(token_loss, N, ctrl, s));
+  if (side_pending) {
+    // the call ends on its stream only once the side stream's dW GEMMs have
+    e = cudaStreamWaitEvent(s, h->slab_freed, 0);
+    if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab join: %s", cudaGetErrorString(e));
+  }
   *ctrl_out = ctrl;
   return FLCE_OK;
 }
@@ -1012,6 +1062,9 @@ void flce_destroy(flce_handle_t h) {
       if (sl.done) cudaEventDestroy(sl.done);
     }
     if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+    if (h->side_stream) cudaStreamDestroy(h->side_stream);
+    if (h->slab_ready) cudaEventDestroy(h->slab_ready);
+    if (h->slab_freed) cudaEventDestroy(h->slab_freed);
   }
   delete h;
 }

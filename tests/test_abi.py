@@ -123,30 +123,34 @@ def test_plan_balances_chunks():
 
 def test_plan_slabs_bounded_in_V():
     """SLABS: the chunk buffer holds one vocabulary slab (a multiple of 512
-    columns, at most 64 MiB), so the workspace no longer grows with V."""
+    columns, at most 256 MiB and what the budget leaves), so the workspace
+    no longer grows with V."""
     p = flce.plan(16384, 4096, 128256, "bf16", dlogits_mode="slabs")
     vs = p["vocab_slab"]
-    assert vs % 512 == 0 and p["chunk"] * vs * 2 <= 64 << 20
+    assert vs % 512 == 0 and p["chunk"] * vs * 2 <= 256 << 20
     assert p["ldv"] == vs and p["logits_bytes"] == p["chunk"] * vs * 2
     assert p["dx_splits"] == 1
     # 256-row x 512-column tiles on 76 SM pairs: the slab is narrowed from
-    # 8192 to 7168 columns, where the dlogits GEMM (16 x 14 tiles) and the dW
-    # GEMM (28 x 8 tiles) both run 224 units, 3 waves of 76 at 98%
-    assert (p["chunk"], vs) == (4096, 7168)
+    # 32768 to 29184 columns, where the dlogits GEMM (16 x 57 tiles) and the
+    # dW GEMM (114 x 8 tiles) both run 912 units, 12 full waves of 76
+    assert (p["chunk"], vs) == (4096, 29184)
     inplace = flce.plan(16384, 4096, 128256, "bf16")
-    assert p["workspace_bytes"] < inplace["workspace_bytes"]
-    # doubling V leaves the slab workspace unchanged
+    assert p["workspace_bytes"] < inplace["workspace_bytes"] / 4
+    # doubling V changes only the per-token log-sum-exp partials
     q = flce.plan(16384, 4096, 256512, "bf16", dlogits_mode="slabs", chunk=p["chunk"])
+    assert q["vocab_slab"] == vs
     assert q["workspace_bytes"] - p["workspace_bytes"] <= p["chunk"] * 8 * (q["vocab_tiles"] - p["vocab_tiles"]) + 4096
-    # a small budget still plans, with a narrower chunk
-    r = flce.plan(16384, 4096, 128256, "bf16", dlogits_mode="slabs", hbm_budget_bytes=256 << 20)
-    assert r["workspace_bytes"] <= 256 << 20 and r["chunk"] >= 1024
+    # small budgets shorten the chunk before they narrow the slab below 8192
+    for mib, chunk, slab in ((128, 3328, 8704), (64, 1664, 9728), (24, 640, 9216)):
+        r = flce.plan(16384, 4096, 128256, "bf16", dlogits_mode="slabs", hbm_budget_bytes=mib << 20)
+        assert (r["chunk"], r["vocab_slab"]) == (chunk, slab)
+        assert r["workspace_bytes"] <= mib << 20
     # an explicit chunk above 4096 tokens is clamped to 4096
     assert flce.plan(16384, 4096, 128256, "bf16", dlogits_mode="slabs", chunk=16384)["chunk"] == 4096
     with pytest.raises(flce.FlceError) as e:
         flce.plan(16384, 4096, 128256, "bf16", dlogits_mode="slabs", hbm_budget_bytes=64 << 20, chunk=4096)
     assert e.value.status_name == "FLCE_ERR_BUDGET"
-    # a vocabulary narrower than one slab is one slab
+    # a vocabulary narrower than the slab room is one slab
     s = flce.plan(2048, 1024, 4000, "bf16", dlogits_mode="slabs")
     assert s["vocab_slab"] == 4000 and s["ldv"] == 4032
     with pytest.raises(flce.FlceError) as e:
