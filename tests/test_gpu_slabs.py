@@ -169,3 +169,55 @@ def test_graph_capture_with_side_stream(slabs):
         assert_parity({"loss": loss.item(), "dx": to_np64(dx), "dW": to_np64(dW)}, _oracle(w), "bf16")
         assert nv.item() == int((w.t != -100).sum())
     slabs.async_status()
+
+
+@pytest.mark.slow
+def test_long_context_sampled_and_memory():
+    """The 131,072-token batch: 32 chunks of 5 slabs, sampled outputs
+    against the oracle, and the measured drop in free HBM within the plan's
+    workspace (0.32 GB, against 33.6 GB of full logits)."""
+    from test_gpu_fullsize import Ref, _check
+    from flce_testing import device_inputs
+    from linear_cross_entropy_token_gb300 import FLCE
+    w = workloads.make("long_bf16")
+    ref = Ref(w, full_lse=False)
+    h = FLCE("bf16", 0, dlogits_mode="slabs")
+    try:
+        x, W, t = device_inputs(w)
+        dx = torch.empty_like(x)
+        dW = torch.empty(W.shape, dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        h.forward_backward(x, W, t, dx=dx, dW=dW)
+        free1, _ = torch.cuda.mem_get_info()
+        plan = h.last_plan()
+        assert (plan["chunk"], plan["num_chunks"], plan["vocab_slab"]) == (4096, 32, 29184)
+        assert free0 - free1 <= plan["workspace_bytes"] + (64 << 20)
+        assert plan["workspace_bytes"] * 100 < w.N * w.V * 2
+        del x, W, t, dx, dW
+        torch.cuda.empty_cache()
+        _check(h, w, ref)
+    finally:
+        h.close()
+
+
+def test_autograd_with_a_slab_handle():
+    """The autograd wrapper takes a handle: a slab handle gives the
+    oracle's loss and gradients through loss.backward()."""
+    from flce_testing import device_inputs
+    from linear_cross_entropy_token_gb300 import FLCE
+    from linear_cross_entropy_token_gb300.autograd import linear_cross_entropy
+    w = workloads.generate(workloads.custom(2048, 128, 40000, "bf16", ignore_frac=0.1, seed=16))
+    h = FLCE("bf16", 0, dlogits_mode="slabs", hbm_budget_bytes=BUDGET)
+    try:
+        x, W, t = device_inputs(w)
+        x.requires_grad_(True)
+        W.requires_grad_(True)
+        loss = linear_cross_entropy(x, W, t, handle=h)
+        loss.backward()
+        assert math.ceil(w.V / h.last_plan()["vocab_slab"]) >= 2
+        res = {"loss": loss.item(), "dx": x.grad.double().cpu().numpy(),
+               "dW": W.grad.double().cpu().numpy()}
+        assert_parity(res, _oracle(w), "bf16")
+    finally:
+        h.close()
