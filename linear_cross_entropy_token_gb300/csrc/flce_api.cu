@@ -673,7 +673,18 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
 
   const int64_t C = p.chunk, ldv = p.ldv;
   const int vt = static_cast<int>(p.vocab_tiles);
-  bool side_pending = false;  // SLABS: this call has work on the side stream
+  // SLABS: whether this call has work on the side stream. However the call
+  // returns, its stream then waits for that work, so that no later call can
+  // overwrite the slab buffer under a dW GEMM still reading it.
+  bool side_pending = false;
+  struct SideJoin {
+    flce_handle_t h;
+    cudaStream_t s;
+    const bool& pending;
+    ~SideJoin() {
+      if (pending) cudaStreamWaitEvent(s, h->slab_freed, 0);
+    }
+  } side_join{h, s, side_pending};
   const double dV = static_cast<double>(V), dH = static_cast<double>(H);
 
   if (!bf16) {
@@ -915,7 +926,8 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
   }
   FLCE_LAUNCH(FLCE_K_LOSS_FINALIZE, 0.0, 4.0 * N, launch_loss_finalize(token_loss, N, ctrl, s));
   if (side_pending) {
-    // the call ends on its stream only once the side stream's dW GEMMs have
+    // the call ends on its stream only once the side stream's dW GEMMs are done
+    side_pending = false;
     e = cudaStreamWaitEvent(s, h->slab_freed, 0);
     if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab join: %s", cudaGetErrorString(e));
   }
