@@ -77,14 +77,18 @@ enum { FLCE_DTYPE_BF16 = 0, FLCE_DTYPE_FP32 = 1 };
  *  SLABS:     the logits GEMM keeps only per-row statistics; the backward
  *             then walks the vocabulary in slabs of flce_plan.vocab_slab
  *             columns: per slab a GEMM recomputes the slab's dlogits into a
- *             C x vocab_slab buffer (sized to stay in L2), and the dx and dW
- *             GEMMs consume it (dx accumulated over the slabs in fp32). The
- *             workspace no longer grows with V: O(C·(vocab_slab + H)) bytes
- *             against O(C·V) for the other two, for 8·N·H·V FLOPs instead of
- *             6·N·H·V (the buffer-free variant the pages leave as the next
- *             step, with the dlogits tile held in a small L2-resident slab
- *             rather than in registers). bf16 only: an fp32 handle returns
- *             UNSUPPORTED.
+ *             C x vocab_slab buffer (at most 256 MiB, sized from the HBM
+ *             budget), which the dx GEMM (dx accumulated over the slabs in
+ *             fp32, in slab order) and the dW GEMM (on a second stream)
+ *             consume. The workspace no longer grows with V:
+ *             O(C·(vocab_slab + H)) bytes against O(C·V) for the other two,
+ *             for 8·N·H·V FLOPs instead of 6·N·H·V. The Unsloth page
+ *             ("Unsloth 심층 아키텍처 …", section "스트리밍 청크 기반 Fast
+ *             CrossEntropy 손실 커널") keeps the logits off HBM altogether
+ *             and adds dx with atomics; here the dlogits tile lives in the
+ *             slab buffer, since no SM holds a token block's whole dx row,
+ *             and dx is reduced in a fixed order. bf16 only: an fp32 handle
+ *             returns UNSUPPORTED.
  *  AUTO:      INPLACE, the fastest of the three on GB300 by measurement. */
 enum { FLCE_DLOGITS_AUTO = 0, FLCE_DLOGITS_INPLACE = 1, FLCE_DLOGITS_RECOMPUTE = 2,
        FLCE_DLOGITS_SLABS = 3 };
