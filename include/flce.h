@@ -105,8 +105,9 @@ enum { FLCE_CTA_AUTO = 0, FLCE_CTA_SINGLE = 1, FLCE_CTA_PAIR = 2, FLCE_CTA_QUAD 
 /*  WIDE:   CTA pairs on 256 x 512 tiles: per k-step two 256 x 256 MMAs share
  *          their A operand through the tensor core's collector buffer, so a
  *          CTA's shared memory moves 25% fewer bytes per FLOP. The 512
- *          accumulator columns fill TMEM: the epilogue does not overlap the
- *          next tile's main loop. */
+ *          accumulator columns fill TMEM: the next tile's MMAs wait until
+ *          the epilogue has read the accumulator out (its stores may still
+ *          run). */
 /*  QUAD:   clusters of two CTA pairs on consecutive 256-row blocks of the same
  *          256 columns (512 x 256 tiles); the pairs share B through TMA
  *          multicast, so a CTA fetches a quarter of the B tile instead of a

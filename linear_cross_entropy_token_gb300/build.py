@@ -35,16 +35,28 @@ def nvcc() -> str:
 GEMM_SOURCES = ("flce_umma.cu", "ptx.cuh", "flce_internal.h")
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source with its comments removed and its whitespace collapsed:
+    what the compiler sees, so that editing a comment does not change the
+    hash. (A "//" inside a string literal also ends the line's code here;
+    the kernel sources hold none that matter.)"""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_hash(names=GEMM_SOURCES) -> str:
-    """Short hash of CUDA sources (by default those of the tcgen05 GEMM
-    kernels), identifying the kernels a profile of them describes."""
+    """Short hash of the code (comments and whitespace aside) of CUDA
+    sources, by default those of the tcgen05 GEMM kernels: it identifies the
+    kernels a profile of them describes."""
     import hashlib
     h = hashlib.sha256()
     for name in sorted(names):
         if os.path.exists(os.path.join(CSRC, name)):
-            with open(os.path.join(CSRC, name), "rb") as f:
+            with open(os.path.join(CSRC, name), encoding="utf-8") as f:
                 h.update(name.encode())
-                h.update(f.read())
+                h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -718,9 +718,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // share their A operand through the tensor core's collector buffer
 // (collector::a::fill, then ::lastuse), so A is read from shared memory once
 // for twice the work: 48 KB written and 48 KB read per 16.8 MFLOP. The 512
-// accumulator columns fill TMEM, so the accumulator is single-buffered and the
-// epilogue of a tile does not overlap the next tile's main loop: the shape
-// pays where K per tile is long.
+// accumulator columns fill TMEM, so the accumulator is single-buffered: the
+// next tile's MMAs wait until the epilogue has read it out (the fp32
+// epilogue's last stores run after that). The shape pays most where K per
+// tile is long.
 template <int AMN, int BMN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
     umma_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
