@@ -620,6 +620,112 @@ flce_status stage_inputs(flce_handle_t h, void** buf, uint64_t* buf_bytes, const
   return FLCE_OK;
 }
 
+// The SLABS backward of one chunk, after its statistics: per vocabulary
+// slab, the slab's dlogits recomputed into the chunk buffer (C x vocab_slab),
+// dx (+)= d_s · W_s into one fp32 C x H buffer (stored by the first slab,
+// added by the others, in slab order) and, on the side stream, dW_s (+)=
+// d_sᵀ · x_c; then the dx reduction. *side_pending is set once work is on
+// the side stream (the caller's stream must join it before the call ends).
+struct SlabChunk {
+  const flce_plan* plan;
+  const UmmaArgs* logits_args;  // the chunk's logits-GEMM arguments
+  const CUtensorMap* mX_k;      // x_c, K-major and MN-major
+  const CUtensorMap* mX_mn;
+  const __nv_bfloat16* W;
+  float* dW;
+  __nv_bfloat16* buf;           // chunk buffer, row stride plan->ldv
+  float* dxacc;                 // C x H fp32
+  __nv_bfloat16* dx;            // this chunk's rows of dx
+  const int64_t* t;             // this chunk's targets
+  float* dcorr;
+  uint32_t* ctrl;
+  int64_t H, V, C, chunk_index, ignore_index;
+  int rows;
+  int b_box;                    // rows of a K-major B box for the handle's tile shape
+};
+
+flce_status slab_backward(flce_handle_t h, const SlabChunk& k, cudaStream_t s, bool* side_pending) {
+  std::string why;
+  cudaError_t e = cudaSuccess;
+  if (!h->side_stream) {
+    e = cudaStreamCreateWithFlags(&h->side_stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slab_ready, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slab_freed, cudaEventDisableTiming);
+    if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
+  }
+  const cudaStream_t side = h->side_stream;
+  const int64_t H = k.H, V = k.V, Vs = k.plan->vocab_slab, ldv = k.plan->ldv;
+  const int rows = k.rows;
+  const double dr = rows, dH = static_cast<double>(H);
+  const int64_t n_slabs = cdiv(V, Vs);
+  CUtensorMap mWs_k, mWs_mn, mZs_out, mZs_k, mZs_mn, mDws, mDxs;
+  if (!map_f32_3d(&mDxs, k.dxacc, H, rows, 1, H * 4, static_cast<uint64_t>(k.C) * H * 4, &why))
+    return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
+  for (int64_t sl = 0; sl < n_slabs; ++sl) {
+    const int64_t v0 = sl * Vs;
+    const int64_t vs = std::min(Vs, V - v0);
+    const double dvs = static_cast<double>(vs);
+    if (!map_bf16_2d(&mWs_k, k.W + v0 * H, H, vs, H * 2, 64, k.b_box, &why) ||
+        !map_bf16_2d(&mWs_mn, k.W + v0 * H, H, vs, H * 2, 64, 64, &why) ||
+        !map_f32_3d(&mDws, k.dW + v0 * H, H, vs, 1, H * 4, static_cast<uint64_t>(vs) * H * 4, &why) ||
+        !map_bf16_2d(&mZs_out, k.buf, vs, rows, ldv * 2, 64, 128, &why) ||
+        !map_bf16_2d(&mZs_k, k.buf, vs, rows, ldv * 2, 64, 128, &why) ||
+        !map_bf16_2d(&mZs_mn, k.buf, vs, rows, ldv * 2, 64, 64, &why))
+      return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
+    // the slab's dlogits: a logits GEMM over W_s with the dlogits epilogue;
+    // the previous slab's dW GEMM (on the side stream) must have read the
+    // buffer first (earlier calls' are ordered by the join that ends them)
+    UmmaArgs g = *k.logits_args;
+    g.num_n = static_cast<int>(cdiv(vs, kBN));
+    g.cols = static_cast<int>(vs);
+    g.col_base = v0;
+    if (*side_pending) {
+      e = cudaStreamWaitEvent(s, h->slab_freed, 0);
+      if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab wait: %s", cudaGetErrorString(e));
+    }
+    FLCE_LAUNCH(FLCE_K_GEMM_DLOGITS, 2 * dr * dH * dvs, 2 * dr * dH + 2 * dvs * dH + 2 * dr * dvs + 12 * dr,
+                launch_gemm(h, kUmmaDlogits, *k.mX_k, mWs_k, mZs_out, g, rows, s));
+    e = cudaEventRecord(h->slab_ready, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->slab_ready, 0);
+    if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab fork: %s", cudaGetErrorString(e));
+    // dx (+)= d_s · W_s
+    UmmaArgs b = *k.logits_args;
+    b.num_n = static_cast<int>(cdiv(H, kBN));
+    b.num_s = 1;
+    b.kb_total = static_cast<int>(cdiv(vs, kBK));
+    b.kb_per_split = b.kb_total;
+    b.raster = 2;
+    b.rows = rows;
+    b.cols = static_cast<int>(H);
+    b.reduce_add = sl > 0 ? 1 : 0;
+    FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dvs * dH, 2 * dr * dvs + 2 * dvs * dH + (sl > 0 ? 8.0 : 4.0) * dr * dH,
+                launch_gemm(h, kUmmaDxF32, mZs_k, mWs_mn, mDxs, b, rows, s));
+    // dW_s (+)= d_sᵀ · x_c, beside it on the side stream
+    UmmaArgs d = *k.logits_args;
+    d.num_n = static_cast<int>(cdiv(H, kBN));
+    d.num_s = 1;
+    d.kb_total = static_cast<int>(cdiv(rows, kBK));
+    d.kb_per_split = d.kb_total;
+    d.raster = 1;
+    d.rows = static_cast<int>(vs);
+    d.cols = static_cast<int>(H);
+    d.reduce_add = k.chunk_index > 0 ? 1 : 0;
+    {
+      const cudaStream_t s = side;  // the launch and its timing events go on the side stream
+      FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dvs * dH,
+                  2 * dr * dvs + 2 * dr * dH + (k.chunk_index > 0 ? 8.0 : 4.0) * dvs * dH,
+                  launch_gemm(h, kUmmaDw, mZs_mn, *k.mX_mn, mDws, d, vs, s));
+    }
+    e = cudaEventRecord(h->slab_freed, side);
+    if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab join: %s", cudaGetErrorString(e));
+    *side_pending = true;
+  }
+  FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4 * dr * dH + 2 * dr * dH,
+              launch_dx_reduce(k.dxacc, 1, k.C * H, rows, H, k.W, V, k.t, k.ignore_index, k.ctrl, k.dcorr,
+                               k.dx, s));
+  return FLCE_OK;
+}
+
 // Everything of one call up to its control words on the device (*ctrl_out):
 // the result is read from them once the stream gets there.
 flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int64_t* t, int64_t N,
@@ -772,81 +878,11 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
                   launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
       if (slabs) {
-        // 2b-4, slab by slab: the slab's dlogits recomputed into the chunk
-        // buffer (C x vocab_slab), then dx (+)= d_s · W_s into one fp32
-        // buffer (stored by the first slab, added by the others, in slab
-        // order) and dW_s (+)= d_sᵀ · x_c
-        const int64_t Vs = p.vocab_slab;
-        const int64_t n_slabs = cdiv(V, Vs);
-        const __nv_bfloat16* Wb = static_cast<const __nv_bfloat16*>(W);
-        CUtensorMap mWs_k, mWs_mn, mZs_out, mZs_k, mZs_mn, mDws, mDxs;
-        if (!h->side_stream) {
-          e = cudaStreamCreateWithFlags(&h->side_stream, cudaStreamNonBlocking);
-          if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slab_ready, cudaEventDisableTiming);
-          if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slab_freed, cudaEventDisableTiming);
-          if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
-        }
-        const cudaStream_t side = h->side_stream;
-        if (!map_f32_3d(&mDxs, dxpart, H, rows, 1, H * 4, static_cast<uint64_t>(C) * H * 4, &why))
-          return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
-        for (int64_t sl = 0; sl < n_slabs; ++sl) {
-          const int64_t v0 = sl * Vs;
-          const int64_t vs = std::min(Vs, V - v0);
-          const double dvs = static_cast<double>(vs);
-          if (!map_bf16_2d(&mWs_k, Wb + v0 * H, H, vs, H * 2, 64, b_box, &why) ||
-              !map_bf16_2d(&mWs_mn, Wb + v0 * H, H, vs, H * 2, 64, 64, &why) ||
-              !map_f32_3d(&mDws, dW + v0 * H, H, vs, 1, H * 4, static_cast<uint64_t>(vs) * H * 4, &why) ||
-              !map_bf16_2d(&mZs_out, logits, vs, rows, ldv * 2, 64, 128, &why) ||
-              !map_bf16_2d(&mZs_k, logits, vs, rows, ldv * 2, 64, 128, &why) ||
-              !map_bf16_2d(&mZs_mn, logits, vs, rows, ldv * 2, 64, 64, &why))
-            return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
-          UmmaArgs g = a;
-          g.num_n = static_cast<int>(cdiv(vs, kBN));
-          g.cols = static_cast<int>(vs);
-          g.col_base = v0;
-          // the previous slab's dW GEMM (on the side stream) has read the
-          // buffer; earlier calls' are ordered by the join that ends them
-          if (side_pending) {
-            e = cudaStreamWaitEvent(s, h->slab_freed, 0);
-            if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab wait: %s", cudaGetErrorString(e));
-          }
-          FLCE_LAUNCH(FLCE_K_GEMM_DLOGITS, 2 * dr * dH * dvs, 2 * dr * dH + 2 * dvs * dH + 2 * dr * dvs + 12 * dr,
-                      launch_gemm(h, kUmmaDlogits, mX_k, mWs_k, mZs_out, g, rows, s));
-          e = cudaEventRecord(h->slab_ready, s);
-          if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->slab_ready, 0);
-          if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab fork: %s", cudaGetErrorString(e));
-          UmmaArgs b = a;
-          b.num_n = static_cast<int>(cdiv(H, kBN));
-          b.num_s = 1;
-          b.kb_total = static_cast<int>(cdiv(vs, kBK));
-          b.kb_per_split = b.kb_total;
-          b.raster = 2;
-          b.rows = rows;
-          b.cols = static_cast<int>(H);
-          b.reduce_add = sl > 0 ? 1 : 0;
-          FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dvs * dH, 2 * dr * dvs + 2 * dvs * dH + (sl > 0 ? 8.0 : 4.0) * dr * dH,
-                      launch_gemm(h, kUmmaDxF32, mZs_k, mWs_mn, mDxs, b, rows, s));
-          UmmaArgs d = a;
-          d.num_n = static_cast<int>(cdiv(H, kBN));
-          d.num_s = 1;
-          d.kb_total = static_cast<int>(cdiv(rows, kBK));
-          d.kb_per_split = d.kb_total;
-          d.raster = 1;
-          d.rows = static_cast<int>(vs);
-          d.cols = static_cast<int>(H);
-          d.reduce_add = c > 0 ? 1 : 0;
-          {
-            const cudaStream_t s = side;  // the launch and its timing events go on the side stream
-            FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dvs * dH, 2 * dr * dvs + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dvs * dH,
-                        launch_gemm(h, kUmmaDw, mZs_mn, mX_mn, mDws, d, vs, s));
-          }
-          e = cudaEventRecord(h->slab_freed, side);
-          if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab join: %s", cudaGetErrorString(e));
-          side_pending = true;
-        }
-        FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4 * dr * dH + 2 * dr * dH,
-                    launch_dx_reduce(dxpart, 1, C * H, rows, H, Wb, V, t + off, ignore_index, ctrl, dcorr,
-                                     dxb + off * H, s));
+        const SlabChunk k{&p, &a, &mX_k, &mX_mn, static_cast<const __nv_bfloat16*>(W), dW, logits,
+                          dxpart, dxb + off * H, t + off, dcorr, ctrl, H, V, C, c, ignore_index, rows,
+                          b_box};
+        st = slab_backward(h, k, s, &side_pending);
+        if (st != FLCE_OK) return st;
         continue;
       }
       // 2b. dlogits = (softmax - onehot) / n_valid over the chunk buffer
