@@ -170,7 +170,9 @@ enum {
 
 typedef struct flce_kernel_profile {
     int64_t launches;            /* launches of this kind since the last reset         */
-    double total_ms;             /* summed device time, CUDA events on the call stream */
+    double total_ms;             /* summed device time, CUDA events on the call stream
+                                    (on the side stream for the SLABS mode's dW GEMMs,
+                                    which overlap the dx GEMMs)                        */
     double flops;                /* algorithmic FLOPs of those launches                */
     double bytes;                /* algorithmic HBM bytes of those launches            */
 } flce_kernel_profile;
