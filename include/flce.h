@@ -69,7 +69,8 @@ typedef enum flce_status {
 /* element type of x, W and dx; dW is always fp32, the loss always fp32 */
 enum { FLCE_DTYPE_BF16 = 0, FLCE_DTYPE_FP32 = 1 };
 
-/* How the dlogits of a chunk are formed (bf16 only; fp32 always in place).
+/* How the dlogits of a chunk are formed (fp32 handles run SLABS as asked and
+ * every other mode in place).
  *  INPLACE:   the logits GEMM stores bf16 logits; a second pass overwrites
  *             them with (softmax - onehot)/n_valid (the FLCE page's step 2).
  *  RECOMPUTE: the logits GEMM keeps only per-row statistics; a second GEMM
@@ -87,8 +88,9 @@ enum { FLCE_DTYPE_BF16 = 0, FLCE_DTYPE_FP32 = 1 };
  *             CrossEntropy 손실 커널") keeps the logits off HBM altogether
  *             and adds dx with atomics; here the dlogits tile lives in the
  *             slab buffer, since no SM holds a token block's whole dx row,
- *             and dx is reduced in a fixed order. bf16 only: an fp32 handle
- *             returns UNSUPPORTED.
+ *             and dx is reduced in a fixed order. On an fp32 handle the
+ *             same walk runs on the CUDA-core kernels, dx accumulated in
+ *             place.
  *  AUTO:      INPLACE, the fastest of the three on GB300 by measurement. */
 enum { FLCE_DLOGITS_AUTO = 0, FLCE_DLOGITS_INPLACE = 1, FLCE_DLOGITS_RECOMPUTE = 2,
        FLCE_DLOGITS_SLABS = 3 };

@@ -215,10 +215,6 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   if (num_sms <= 0) num_sms = 152;
   const bool bf16 = cfg->dtype == FLCE_DTYPE_BF16;
   const bool slabs = cfg->dlogits_mode == FLCE_DLOGITS_SLABS;
-  if (slabs && !bf16) {
-    *why = "FLCE_DLOGITS_SLABS runs on the bf16 tcgen05 path only";
-    return FLCE_ERR_UNSUPPORTED;
-  }
   const int esize = bf16 ? 2 : 4;
   const uint64_t budget = cfg->hbm_budget_bytes ? cfg->hbm_budget_bytes : kDefaultBudget;
   std::memset(out, 0, sizeof(*out));
@@ -241,7 +237,8 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
     const uint64_t cc = static_cast<uint64_t>(std::max<int64_t>(C, 1));
     const uint64_t rest = make_layout(N, H, C, 0, out->vocab_tiles, splits_for(C), esize).total + kAlign;
     const uint64_t room = budget > rest ? std::min(kSlabBytes, budget - rest) : 0;
-    const int64_t cmax = std::max<int64_t>(kSlabAlign, static_cast<int64_t>(room / (2 * cc)) / kSlabAlign * kSlabAlign);
+    const int64_t cmax =
+        std::max<int64_t>(kSlabAlign, static_cast<int64_t>(room / (esize * cc)) / kSlabAlign * kSlabAlign);
     if (cmax >= V) return V;
     auto eff = [&](int64_t units) {
       return static_cast<double>(units) / static_cast<double>(cdiv(units, slots) * slots);
@@ -799,6 +796,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     const float* Wf = static_cast<const float*>(W);
     float* dxf = static_cast<float*>(dx);
     float* logits = reinterpret_cast<float*>(ws + L.logits);
+    const bool slabs = h->cfg.dlogits_mode == FLCE_DLOGITS_SLABS;
     for (int64_t c = 0; c < p.num_chunks; ++c) {
       char nvtx_name[40];
       std::snprintf(nvtx_name, sizeof nvtx_name, "flce chunk %lld", static_cast<long long>(c));
@@ -806,14 +804,47 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       const int64_t off = c * C;
       const int rows = static_cast<int>(std::min(C, N - off));
       const double dr = rows;
+      if (slabs) {
+        // statistics slab by slab, the combine, then each slab's logits again:
+        // dlogits in place, dx (+)= d_s · W_s, dW_s (+)= d_sᵀ · x_c
+        const int64_t Vs = p.vocab_slab, n_slabs = cdiv(V, Vs);
+        for (int64_t sl = 0; sl < n_slabs; ++sl) {
+          const int64_t v0 = sl * Vs, vs = std::min(Vs, V - v0);
+          const double dvs = static_cast<double>(vs);
+          const int vts = static_cast<int>(cdiv(vs, kVocabTile));
+          FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dH * dvs, 4 * (dr * dH + dvs * dH + dr * dvs),
+                      launch_simt_gemm_f32(xf + off * H, H, 1, Wf + v0 * H, 1, H, logits, ldv, rows, vs, H, 0, s));
+          FLCE_LAUNCH(FLCE_K_SIMT_TILE_STATS, 0.0, 4 * dr * dvs + 12 * dr * vts,
+                      launch_simt_tile_stats(logits, ldv, rows, vs, vts, vt, v0, t + off, ignore_index,
+                                             partials + v0 / kVocabTile, zt, s));
+        }
+        FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
+                    launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
+        for (int64_t sl = 0; sl < n_slabs; ++sl) {
+          const int64_t v0 = sl * Vs, vs = std::min(Vs, V - v0);
+          const double dvs = static_cast<double>(vs);
+          FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dH * dvs, 4 * (dr * dH + dvs * dH + dr * dvs),
+                      launch_simt_gemm_f32(xf + off * H, H, 1, Wf + v0 * H, 1, H, logits, ldv, rows, vs, H, 0, s));
+          FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 8 * dr * dvs,
+                      launch_dlogits_f32(logits, ldv, rows, vs, v0, lse, t + off, ignore_index, ctrl, s));
+          FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dvs * dH, 4 * (dr * dvs + dvs * dH + (sl > 0 ? 2 : 1) * dr * dH),
+                      launch_simt_gemm_f32(logits, ldv, 1, Wf + v0 * H, H, 1, dxf + off * H, H, rows, H, vs,
+                                           sl > 0 ? 1 : 0, s));
+          FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dvs * dH, 4 * (dr * dvs + dr * dH + (c > 0 ? 2 : 1) * dvs * dH),
+                      launch_simt_gemm_f32(logits, 1, ldv, xf + off * H, H, 1, dW + v0 * H, H, vs, H, rows,
+                                           c > 0 ? 1 : 0, s));
+        }
+        continue;
+      }
       FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dH * dV, 4 * (dr * dH + dV * dH + dr * dV),
                   launch_simt_gemm_f32(xf + off * H, H, 1, Wf, 1, H, logits, ldv, rows, V, H, 0, s));
       FLCE_LAUNCH(FLCE_K_SIMT_TILE_STATS, 0.0, 4 * dr * dV + 12 * dr * vt,
-                  launch_simt_tile_stats(logits, ldv, rows, V, vt, t + off, ignore_index, partials, zt, s));
+                  launch_simt_tile_stats(logits, ldv, rows, V, vt, vt, 0, t + off, ignore_index, partials,
+                                         zt, s));
       FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
                   launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
       FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 8 * dr * dV,
-                  launch_dlogits_f32(logits, ldv, rows, V, lse, t + off, ignore_index, ctrl, s));
+                  launch_dlogits_f32(logits, ldv, rows, V, 0, lse, t + off, ignore_index, ctrl, s));
       FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dV * dH, 4 * (dr * dV + dV * dH + dr * dH),
                   launch_simt_gemm_f32(logits, ldv, 1, Wf, H, 1, dxf + off * H, H, rows, H, V, 0, s));
       FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dV * dH, 4 * (dr * dV + dr * dH + 2 * dV * dH),
@@ -1033,8 +1064,6 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
   if (cfg->dtype != FLCE_DTYPE_BF16 && cfg->dtype != FLCE_DTYPE_FP32) return FLCE_ERR_UNSUPPORTED;
   if (cfg->dlogits_mode < FLCE_DLOGITS_AUTO || cfg->dlogits_mode > FLCE_DLOGITS_SLABS)
     return FLCE_ERR_INVALID_ARG;
-  if (cfg->dlogits_mode == FLCE_DLOGITS_SLABS && cfg->dtype != FLCE_DTYPE_BF16)
-    return FLCE_ERR_UNSUPPORTED;
   int count = 0;
   if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
     cudaGetLastError();

@@ -113,8 +113,9 @@ cudaError_t launch_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int rows, int64
                                 const float2* partials, int vocab_tiles, const float* lse,
                                 const int64_t* t_chunk, int64_t ignore_index,
                                 const uint32_t* ctrl, float* dcorr, cudaStream_t s);
-cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, const float* lse,
-                               const int64_t* t_chunk, int64_t ignore_index,
+// buf's column 0 is vocabulary column col_base (a slab of the vocabulary)
+cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, int64_t col_base,
+                               const float* lse, const int64_t* t_chunk, int64_t ignore_index,
                                const uint32_t* ctrl, cudaStream_t s);
 cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_stride, int rows,
                              int64_t H, const __nv_bfloat16* W, int64_t V, const int64_t* t_chunk,
@@ -128,8 +129,11 @@ cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* c
 cudaError_t launch_simt_gemm_f32(const float* A, int64_t sam, int64_t sak, const float* B,
                                  int64_t sbk, int64_t sbn, float* C, int64_t ldc, int64_t M,
                                  int64_t N, int64_t K, int accumulate, cudaStream_t s);
+// vocab_tiles tiles of the buffer's V columns; the buffer's column 0 is
+// vocabulary column col_base, and partials rows are part_stride apart
 cudaError_t launch_simt_tile_stats(const float* logits, int64_t ldv, int rows, int64_t V,
-                                   int vocab_tiles, const int64_t* t_chunk, int64_t ignore_index,
-                                   float2* partials, float* zt, cudaStream_t s);
+                                   int vocab_tiles, int part_stride, int64_t col_base,
+                                   const int64_t* t_chunk, int64_t ignore_index, float2* partials,
+                                   float* zt, cudaStream_t s);
 
 }  // namespace flce

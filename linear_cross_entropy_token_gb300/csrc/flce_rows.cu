@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(256) dlogits_bf16_kernel(
 }
 
 // fp32 version: 4 columns per thread
-__global__ void dlogits_f32_kernel(float* __restrict__ buf, int64_t ldv, int64_t V,
+__global__ void dlogits_f32_kernel(float* __restrict__ buf, int64_t ldv, int64_t V, int64_t col_base,
                                    const float* __restrict__ lse, const int64_t* __restrict__ t,
                                    int64_t ignore_index, const uint32_t* __restrict__ ctrl) {
   const int r = blockIdx.y;
@@ -186,7 +186,7 @@ __global__ void dlogits_f32_kernel(float* __restrict__ buf, int64_t ldv, int64_t
   for (int q = 0; q < 4; ++q) {
     const int64_t j = c0 + q;
     float d = expf(f[q] - l);
-    if (j == tg) d -= 1.f;
+    if (j + col_base == tg) d -= 1.f;
     f[q] = (j < V) ? d * scale : 0.f;
   }
   *ptr = make_float4(f[0], f[1], f[2], f[3]);
@@ -297,13 +297,13 @@ cudaError_t launch_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int rows, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, const float* lse,
-                               const int64_t* t_chunk, int64_t ignore_index,
+cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, int64_t col_base,
+                               const float* lse, const int64_t* t_chunk, int64_t ignore_index,
                                const uint32_t* ctrl, cudaStream_t s) {
   const int threads = 256;
   const int64_t per_block = threads * 4;
   dim3 grid(static_cast<unsigned>((ldv + per_block - 1) / per_block), static_cast<unsigned>(rows));
-  dlogits_f32_kernel<<<grid, threads, 0, s>>>(buf, ldv, V, lse, t_chunk, ignore_index, ctrl);
+  dlogits_f32_kernel<<<grid, threads, 0, s>>>(buf, ldv, V, col_base, lse, t_chunk, ignore_index, ctrl);
   return cudaGetLastError();
 }
 

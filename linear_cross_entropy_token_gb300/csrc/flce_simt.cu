@@ -67,9 +67,10 @@ __global__ void __launch_bounds__(256) simt_gemm_f32_kernel(
 }
 
 // One block per (token row, vocab tile of 256): m = max z, l = sum exp(z - m),
-// and z_t when the target falls in the tile.
+// and z_t when the target falls in the tile. The buffer's column 0 is
+// vocabulary column col_base; partials rows are part_stride apart.
 __global__ void __launch_bounds__(256) simt_tile_stats_kernel(
-    const float* __restrict__ logits, int64_t ldv, int64_t V, int vocab_tiles,
+    const float* __restrict__ logits, int64_t ldv, int64_t V, int part_stride, int64_t col_base,
     const int64_t* __restrict__ t, int64_t ignore_index, float2* __restrict__ partials,
     float* __restrict__ zt) {
   __shared__ float red[256];
@@ -91,9 +92,9 @@ __global__ void __launch_bounds__(256) simt_tile_stats_kernel(
     if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
     __syncthreads();
   }
-  if (threadIdx.x == 0) partials[static_cast<size_t>(r) * vocab_tiles + vt] = make_float2(m, red[0]);
+  if (threadIdx.x == 0) partials[static_cast<size_t>(r) * part_stride + vt] = make_float2(m, red[0]);
   const int64_t tg = t[r];
-  if (in && tg != ignore_index && tg == j) zt[r] = z;
+  if (in && tg != ignore_index && tg - col_base == j) zt[r] = z;
 }
 
 }  // namespace
@@ -107,11 +108,12 @@ cudaError_t launch_simt_gemm_f32(const float* A, int64_t sam, int64_t sak, const
 }
 
 cudaError_t launch_simt_tile_stats(const float* logits, int64_t ldv, int rows, int64_t V,
-                                   int vocab_tiles, const int64_t* t_chunk, int64_t ignore_index,
-                                   float2* partials, float* zt, cudaStream_t s) {
+                                   int vocab_tiles, int part_stride, int64_t col_base,
+                                   const int64_t* t_chunk, int64_t ignore_index, float2* partials,
+                                   float* zt, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(vocab_tiles), static_cast<unsigned>(rows));
-  simt_tile_stats_kernel<<<grid, 256, 0, s>>>(logits, ldv, V, vocab_tiles, t_chunk, ignore_index,
-                                              partials, zt);
+  simt_tile_stats_kernel<<<grid, 256, 0, s>>>(logits, ldv, V, part_stride, col_base, t_chunk,
+                                              ignore_index, partials, zt);
   return cudaGetLastError();
 }
 

@@ -153,9 +153,10 @@ def test_plan_slabs_bounded_in_V():
     # a vocabulary narrower than the slab room is one slab
     s = flce.plan(2048, 1024, 4000, "bf16", dlogits_mode="slabs")
     assert s["vocab_slab"] == 4000 and s["ldv"] == 4032
-    with pytest.raises(flce.FlceError) as e:
-        flce.plan(256, 128, 4096, "fp32", dlogits_mode="slabs")
-    assert e.value.status_name == "FLCE_ERR_UNSUPPORTED"
+    # fp32: the same walk on the CUDA-core path, 4-byte buffer entries
+    f = flce.plan(256, 128, 4096, "fp32", chunk=64, dlogits_mode="slabs", hbm_budget_bytes=300 << 10)
+    assert (f["chunk"], f["vocab_slab"], f["dx_splits"]) == (64, 1024, 1)
+    assert f["logits_bytes"] == 64 * 1024 * 4 and f["workspace_bytes"] <= 300 << 10
 
 
 def test_plan_rejects_bad_sizes():

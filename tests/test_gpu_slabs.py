@@ -221,3 +221,22 @@ def test_autograd_with_a_slab_handle():
         assert_parity(res, _oracle(w), "bf16")
     finally:
         h.close()
+
+
+@pytest.mark.parametrize("N,H,V,chunk,budget,min_slabs", [
+    (256, 128, 4096, 64, 0, 1),            # the tiny fp32 config: one slab
+    (256, 128, 4096, 64, 300 << 10, 4),    # four slabs of 1024
+    (300, 100, 2999, 128, 300 << 10, 6),   # ragged chunks, a ragged last slab, odd H
+])
+def test_fp32_slabs(N, H, V, chunk, budget, min_slabs):
+    """The slab walk on the fp32 CUDA-core path, at the fp32 tolerance."""
+    from linear_cross_entropy_token_gb300 import FLCE
+    w = workloads.generate(workloads.custom(N, H, V, "fp32", ignore_frac=0.1, seed=N + V))
+    h = FLCE("fp32", 0, dlogits_mode="slabs", hbm_budget_bytes=budget)
+    try:
+        res = run(h, w, chunk=chunk)
+    finally:
+        h.close()
+    assert _slab_count(res, V) >= min_slabs
+    assert_parity(res, oracle.flce_reference(w.x_f64(), w.W_f64(), w.t, w.ignore_index), "fp32",
+                  token_rtol=1e-5)
