@@ -19,18 +19,20 @@ from .flce import FLCE
 _handles = {}
 
 
-def _handle(device: torch.device, dtype: torch.dtype) -> FLCE:
-    key = (device.index or 0, dtype)
+def _handle(device: torch.device, dtype: torch.dtype, dlogits_mode: str = "auto",
+            hbm_budget_bytes: int = 0) -> FLCE:
+    key = (device.index or 0, dtype, dlogits_mode, hbm_budget_bytes)
     if key not in _handles:
-        _handles[key] = FLCE("bf16" if dtype == torch.bfloat16 else "fp32", key[0])
+        _handles[key] = FLCE("bf16" if dtype == torch.bfloat16 else "fp32", key[0],
+                             hbm_budget_bytes=hbm_budget_bytes, dlogits_mode=dlogits_mode)
     return _handles[key]
 
 
 class LinearCrossEntropyFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, x, W, t, ignore_index: int, chunk: int, reduction: str, handle,
-                sync_free: bool = False):
-        h = handle if handle is not None else _handle(x.device, x.dtype)
+                sync_free: bool = False, dlogits_mode: str = "auto", hbm_budget_bytes: int = 0):
+        h = handle if handle is not None else _handle(x.device, x.dtype, dlogits_mode, hbm_budget_bytes)
         if reduction not in ("mean", "sum"):
             raise ValueError("reduction must be 'mean' or 'sum'")
         ctx.sync_free = sync_free
@@ -61,7 +63,7 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
             g = grad_out * scale
             gx = dx * g.to(dx.dtype) if ctx.needs_input_grad[0] else None
             gW = dW * g if ctx.needs_input_grad[1] else None
-            return gx, gW, None, None, None, None, None, None
+            return gx, gW, None, None, None, None, None, None, None, None
         dx, dW = ctx.saved_tensors
         g = grad_out * ctx.scale
         if ctx.needs_input_grad[0]:
@@ -72,12 +74,13 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
             gW = dW if (ctx.scale == 1.0 and bool(grad_out == 1)) else dW * g
         else:
             gW = None
-        return gx, gW, None, None, None, None, None, None
+        return gx, gW, None, None, None, None, None, None, None, None
 
 
 def linear_cross_entropy(x: torch.Tensor, W: torch.Tensor, t: torch.Tensor,
                          ignore_index: int = -100, reduction: str = "mean", chunk: int = 0,
-                         handle: FLCE = None, sync_free: bool = False) -> torch.Tensor:
+                         handle: FLCE = None, sync_free: bool = False, dlogits_mode: str = "auto",
+                         hbm_budget_bytes: int = 0) -> torch.Tensor:
     """Cross-entropy of x·Wᵀ against t, fused: the N x V logits never exist.
 
     x: (N, H) bf16 or fp32 on a GB300; W: (V, H) same dtype; t: (N,) int64.
@@ -90,6 +93,10 @@ def linear_cross_entropy(x: torch.Tensor, W: torch.Tensor, t: torch.Tensor,
     the incoming gradient (one extra pass over dW). The default synchronises
     once per call, raises on errors at once, and skips that pass when the
     incoming gradient is 1.
+
+    Without a `handle`, one is kept per (device, dtype, dlogits_mode,
+    hbm_budget_bytes): dlogits_mode "slabs" with a small budget gives the
+    vocabulary-slab backward, whose workspace does not grow with V.
     """
     return LinearCrossEntropyFunction.apply(x, W, t, ignore_index, chunk, reduction, handle,
-                                            sync_free)
+                                            sync_free, dlogits_mode, hbm_budget_bytes)

@@ -201,6 +201,21 @@ def test_long_context_sampled_and_memory():
         h.close()
 
 
+def test_autograd_slab_mode_without_a_handle():
+    """linear_cross_entropy(..., dlogits_mode="slabs", hbm_budget_bytes=...)
+    keeps its own slab handle."""
+    from flce_testing import device_inputs
+    from linear_cross_entropy_token_gb300.autograd import linear_cross_entropy
+    w = workloads.generate(workloads.custom(2048, 128, 40000, "bf16", ignore_frac=0.1, seed=17))
+    x, W, t = device_inputs(w)
+    x.requires_grad_(True)
+    W.requires_grad_(True)
+    loss = linear_cross_entropy(x, W, t, dlogits_mode="slabs", hbm_budget_bytes=BUDGET)
+    loss.backward()
+    res = {"loss": loss.item(), "dx": x.grad.double().cpu().numpy(), "dW": W.grad.double().cpu().numpy()}
+    assert_parity(res, _oracle(w), "bf16")
+
+
 def test_autograd_with_a_slab_handle():
     """The autograd wrapper takes a handle: a slab handle gives the
     oracle's loss and gradients through loss.backward()."""
