@@ -255,3 +255,49 @@ def test_fp32_slabs(N, H, V, chunk, budget, min_slabs):
     assert _slab_count(res, V) >= min_slabs
     assert_parity(res, oracle.flce_reference(w.x_f64(), w.W_f64(), w.t, w.ignore_index), "fp32",
                   token_rtol=1e-5)
+
+
+def test_caller_workspace_and_pipelined_host_calls(slabs):
+    """The slab backward in caller-owned workspace, and through the
+    pipelined host-buffer entry with two calls in flight."""
+    from flce_testing import to_np64
+    from linear_cross_entropy_token_gb300 import FlceError
+    ws = [workloads.generate(workloads.custom(2048, 64, 40000, "bf16", ignore_frac=0.1, seed=30 + i))
+          for i in range(2)]
+    buf = torch.empty(slabs.workspace_bytes(2048, 64, 40000) + 4096, dtype=torch.uint8, device="cuda")
+    off = (-buf.data_ptr()) % 1024
+    slabs.set_workspace(buf[off:off + slabs.workspace_bytes(2048, 64, 40000)])
+    try:
+        assert_parity(run(slabs, ws[0]), _oracle(ws[0]), "bf16")
+        assert slabs.last_plan()["vocab_slab"] < 40000
+        host = [(torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16).pin_memory(),
+                 torch.from_numpy(w.W.view(np.int16)).view(torch.bfloat16).pin_memory(),
+                 torch.from_numpy(w.t).pin_memory()) for w in ws]
+        outs = [(torch.empty(2048, 64, dtype=torch.bfloat16, device="cuda"),
+                 torch.empty(40000, 64, dtype=torch.float32, device="cuda")) for _ in ws]
+        t0, _, _ = slabs.submit_host(*host[0], dx=outs[0][0], dW=outs[0][1])
+        t1, _, _ = slabs.submit_host(*host[1], dx=outs[1][0], dW=outs[1][1])
+        losses = [slabs.wait(t0), slabs.wait(t1)]
+        for w, loss, (dx, dW) in zip(ws, losses, outs):
+            assert_parity({"loss": loss, "dx": to_np64(dx), "dW": to_np64(dW)}, _oracle(w), "bf16")
+        slabs.set_workspace(buf[off:off + 1024])
+        with pytest.raises(FlceError) as e:
+            run(slabs, ws[0])
+        assert e.value.status_name == "FLCE_ERR_BUDGET"
+    finally:
+        slabs.set_workspace(None)
+
+
+def test_other_ignore_index_and_bad_target(slabs):
+    from flce_testing import device_inputs
+    from linear_cross_entropy_token_gb300 import FlceError
+    w = workloads.generate(workloads.custom(2048, 64, 40000, "bf16", seed=32))
+    w.t[::5] = 3                     # class 3 marks the ignored tokens
+    res = run(slabs, w, ignore_index=3)
+    ref = oracle.flce_reference(w.x_f64(), w.W_f64(), w.t, ignore_index=3, chunk=512)
+    assert_parity(res, ref, "bf16", token_rtol=1e-3)
+    w.t[17] = 40000
+    x, W, t = device_inputs(w)
+    with pytest.raises(FlceError) as e:
+        slabs.forward_backward(x, W, t, ignore_index=3)
+    assert e.value.status_name == "FLCE_ERR_BAD_TARGET"
