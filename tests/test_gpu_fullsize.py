@@ -126,6 +126,20 @@ def test_qwen3_chunk_sweep(qwen3, chunk):
         h.close()
 
 
+def test_qwen3_slab_backward(qwen3):
+    """The vocabulary-slab backward on the Qwen3-shaped batch (6 slabs of
+    29184 columns per chunk, the last ragged), on the same sampled outputs."""
+    from linear_cross_entropy_token_gb300 import FLCE
+    w, ref = qwen3
+    h = FLCE("bf16", 0, dlogits_mode="slabs")
+    try:
+        plan = _check(h, w, ref)
+    finally:
+        h.close()
+    assert (plan["chunk"], plan["vocab_slab"]) == (4096, 29184)
+    assert plan["workspace_bytes"] < 0.35e9
+
+
 def test_long_context_sampled_and_memory():
     from linear_cross_entropy_token_gb300 import FLCE
     w = workloads.make("long_bf16")
