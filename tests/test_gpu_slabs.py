@@ -301,3 +301,14 @@ def test_other_ignore_index_and_bad_target(slabs):
     with pytest.raises(FlceError) as e:
         slabs.forward_backward(x, W, t, ignore_index=3)
     assert e.value.status_name == "FLCE_ERR_BAD_TARGET"
+
+
+def test_empty_batch_and_single_token(slabs):
+    x = torch.empty(0, 64, device="cuda", dtype=torch.bfloat16)
+    W = torch.randn(3000, 64, device="cuda").to(torch.bfloat16)
+    t = torch.empty(0, device="cuda", dtype=torch.int64)
+    dW = torch.full((3000, 64), 7.0, device="cuda")
+    loss, dx, dW = slabs.forward_backward(x, W, t, dW=dW)
+    assert loss == 0.0 and dx.shape == (0, 64) and torch.all(dW == 0)
+    w = workloads.generate(workloads.custom(1, 64, 40000, "bf16", seed=33))
+    assert_parity(run(slabs, w), _oracle(w), "bf16")
