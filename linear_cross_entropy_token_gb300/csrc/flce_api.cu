@@ -296,9 +296,18 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
       *why = "not even one 128-token chunk fits the HBM budget";
       return FLCE_ERR_BUDGET;
     }
-    const int64_t k = cdiv(N, cmax);
-    C = std::min<int64_t>(static_cast<int64_t>(align_up(cdiv(N, k), kBM)), cmax);
-    C = std::min(C, N);
+    // even the chunks out over ceil(N / cmax) of them; a shorter chunk can
+    // plan more dx splits than cmax did, so take more chunks until the
+    // workspace fits again (cmax itself always does)
+    const int64_t k0 = cdiv(N, cmax);
+    C = cmax;
+    for (int64_t k = k0; k <= 4 * k0; ++k) {
+      const int64_t c = std::min(std::min<int64_t>(static_cast<int64_t>(align_up(cdiv(N, k), kBM)), cmax), N);
+      if (ws(c) <= budget) {
+        C = c;
+        break;
+      }
+    }
   }
   out->chunk = C;
   out->num_chunks = C ? cdiv(N, C) : 0;

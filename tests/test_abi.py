@@ -164,3 +164,25 @@ def test_plan_rejects_bad_sizes():
         with pytest.raises(flce.FlceError) as e:
             flce.plan(*args)
         assert e.value.status_name == "FLCE_ERR_INVALID_ARG"
+
+
+def test_plan_invariants_over_extreme_shapes():
+    """Every plan the SLABS and in-place planners return covers all tokens,
+    fits its budget, keeps 64-column-aligned rows and a slab that is V or a
+    multiple of 512; a budget too small is the only refusal."""
+    import itertools
+    for N, H, V, budget, dt, cta, mode in itertools.product(
+            [1, 100, 16384, 131072], [8, 4096, 16384], [1, 300, 4099, 262147],
+            [0, 32 << 20, 8 << 30], ["bf16", "fp32"], ["auto", "single"], ["slabs", "inplace"]):
+        if dt == "fp32" and cta != "auto":
+            continue
+        try:
+            p = flce.plan(N, H, V, dt, hbm_budget_bytes=budget, dlogits_mode=mode, cta=cta)
+        except flce.FlceError as e:
+            assert e.status_name == "FLCE_ERR_BUDGET", (N, H, V, budget, dt, cta, mode)
+            continue
+        vs = p["vocab_slab"]
+        assert vs == V or (mode == "slabs" and vs % 512 == 0 and vs < V)
+        assert p["workspace_bytes"] <= (budget or int(1.25 * GiB))
+        assert p["num_chunks"] * p["chunk"] >= N > (p["num_chunks"] - 1) * p["chunk"]
+        assert p["ldv"] % 64 == 0 and p["ldv"] >= vs
