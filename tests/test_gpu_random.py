@@ -43,3 +43,30 @@ def test_random_case(handles, i):
     ref = oracle.flce_reference(w.x_f64(), w.W_f64(), w.t, w.ignore_index)
     res = run(handles[SHAPES[i % len(SHAPES)]], w, chunk=chunk)
     assert_parity(res, ref, "bf16", token_rtol=1e-3)
+
+
+@pytest.fixture(scope="module")
+def slab_handles():
+    """Slab-mode handles with a 2 MiB budget, so that most random shapes
+    run several vocabulary slabs per chunk."""
+    from linear_cross_entropy_token_gb300 import FLCE
+    hs = {c: FLCE("bf16", 0, hbm_budget_bytes=2 << 20, cta=c, dlogits_mode="slabs") for c in ("wide", "single")}
+    yield hs
+    for h in hs.values():
+        h.close()
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_case_slabs(slab_handles, i):
+    from linear_cross_entropy_token_gb300 import FlceError
+    N, H, V, ign, chunk, targets = _case(100 + i)
+    w = workloads.generate(workloads.custom(N, H, V, "bf16", targets=targets, ignore_frac=ign,
+                                            seed=100 + i))
+    h = slab_handles["wide" if i % 2 else "single"]
+    try:
+        res = run(h, w, chunk=chunk)
+    except FlceError as e:       # an explicit chunk too long for the 2 MiB budget
+        assert e.status_name == "FLCE_ERR_BUDGET" and chunk > 0
+        res = run(h, w)
+    ref = oracle.flce_reference(w.x_f64(), w.W_f64(), w.t, w.ignore_index)
+    assert_parity(res, ref, "bf16", token_rtol=1e-3)
