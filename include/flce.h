@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define FLCE_ABI_VERSION 3
+#define FLCE_ABI_VERSION 4
 
 typedef struct flce_handle_s* flce_handle_t;
 
@@ -99,22 +99,18 @@ enum { FLCE_DLOGITS_AUTO = 0, FLCE_DLOGITS_INPLACE = 1, FLCE_DLOGITS_RECOMPUTE =
  *  SINGLE: one CTA per 128 x 256 output tile (tcgen05 cta_group::1).
  *  PAIR:   a cluster of two CTAs on two SMs per 256 x 256 tile
  *          (tcgen05 cta_group::2): each CTA loads half of the B operand.
- *  AUTO:   WIDE (measured fastest on GB300 for the 16384-token,
- *          128256-vocabulary step: 31.6 ms, against 34.9 ms for PAIR and
- *          36.9 ms for SINGLE). */
-enum { FLCE_CTA_AUTO = 0, FLCE_CTA_SINGLE = 1, FLCE_CTA_PAIR = 2, FLCE_CTA_QUAD = 3,
-       FLCE_CTA_WIDE = 4 };
-/*  WIDE:   CTA pairs on 256 x 512 tiles: per k-step two 256 x 256 MMAs share
+ *  WIDE:   CTA pairs on 256 x 512 tiles: per k-step two 256 x 256 MMAs share
  *          their A operand through the tensor core's collector buffer, so a
  *          CTA's shared memory moves 25% fewer bytes per FLOP. The 512
  *          accumulator columns fill TMEM: the next tile's MMAs wait until
  *          the epilogue has read the accumulator out (its stores may still
- *          run). */
-/*  QUAD:   clusters of two CTA pairs on consecutive 256-row blocks of the same
- *          256 columns (512 x 256 tiles); the pairs share B through TMA
- *          multicast, so a CTA fetches a quarter of the B tile instead of a
- *          half. Measured slower (35.7 against 34.4 ms): only 36 clusters of
- *          four fit on the GPU at once, leaving 8 of the 152 SMs idle. */
+ *          run).
+ *  AUTO:   WIDE (measured fastest on GB300 for the 16384-token,
+ *          128256-vocabulary step: 31.6 ms, against 34.9 ms for PAIR and
+ *          36.9 ms for SINGLE).
+ * Value 3 names no tile shape: flce_create and flce_make_plan refuse it with
+ * INVALID_ARG. */
+enum { FLCE_CTA_AUTO = 0, FLCE_CTA_SINGLE = 1, FLCE_CTA_PAIR = 2, FLCE_CTA_WIDE = 4 };
 
 typedef struct flce_config {
     int32_t dtype;               /* FLCE_DTYPE_*                                       */
@@ -145,11 +141,13 @@ typedef struct flce_plan {
     int64_t dx_splits;           /* split of the V reduction of the dx GEMM            */
     uint64_t workspace_bytes;    /* device bytes one call needs                        */
     uint64_t logits_bytes;       /* of which the C x ldv logits / dlogits buffer       */
-    int64_t tile_m;              /* rows of a GEMM output tile: 128 (one CTA), 256 (CTA pair,
-                                    normal or wide) or 512 (two pairs)                  */
+    int64_t tile_m;              /* rows of a GEMM output tile: 128 (one CTA) or 256 (CTA
+                                    pair, normal or wide)                               */
     int64_t tile_n;              /* columns of a GEMM output tile: 256, or 512 (wide)   */
     int64_t vocab_slab;          /* SLABS: vocabulary columns per backward slab (the
                                     buffer is chunk x vocab_slab); other modes: V       */
+    int64_t dlogits_mode;        /* the FLCE_DLOGITS_* mode the call runs (AUTO and,
+                                    on fp32 handles, RECOMPUTE resolved to INPLACE)     */
 } flce_plan;
 
 /* Kernel kinds, for the per-kernel timing of flce_profile_read(). */
@@ -259,10 +257,54 @@ flce_status flce_forward_backward_async(flce_handle_t h, const void* x, const vo
                                         void* stream);
 
 /* Waits for `stream` and returns the first device-side error that
- * flce_forward_backward_async calls recorded since the last flce_async_status
+ * flce_forward_backward_async and flce_forward_backward_shard calls recorded
+ * since the last flce_async_status
  * (FLCE_OK if none), then clears it. It reads the workspace the handle holds
  * now: an error recorded before the workspace was replaced is lost. */
 flce_status flce_async_status(flce_handle_t h, void* stream);
+
+/* ---- token-sharded batches (data parallelism over G GPUs) ---------------
+ * The loss is a mean over the whole batch's non-ignored tokens, and dW a sum
+ * over all of its tokens (the FLCE page, "Fused Linear Cross-Entropy: LLM
+ * 학습 logits 메모리 병목 없애기", section "FLCE의 핵심 아이디어": dlogits,
+ * dx and dW per chunk, the sums divided by the token count at the end; chunks
+ * are independent but for those two sums). "Transformer Math 101"
+ * (wonjae.kim), section "3D 병렬화", splits a batch over model replicas in the
+ * same way. A batch whose tokens are split over G ranks, each holding a
+ * replica of W, therefore needs: every rank's count of non-ignored tokens,
+ * summed (one all-reduce of a scalar); each rank's fused call dividing by
+ * that total; then the sum of dW and of the loss shares over the ranks (one
+ * all-reduce each). dx needs nothing: its rows are the rank's own tokens.
+ * The library does the two per-rank steps; the caller owns the collectives
+ * (the Python wrapper linear_cross_entropy_token_gb300.token_parallel uses
+ * torch.distributed). */
+
+/* n_valid of this rank's tokens into DEVICE memory: *n_valid_dev =
+ * #{i < N : t_i != ignore_index} (one int32), written when the stream gets
+ * there; no host synchronisation. Targets are not range-checked here (the
+ * fused call checks them). Errors: INVALID_ARG (null or misaligned pointer:
+ * t 8-byte, n_valid_dev 4-byte; N < 0), CUDA. */
+flce_status flce_count_valid(flce_handle_t h, const int64_t* t, int64_t N, int64_t ignore_index,
+                             int32_t* n_valid_dev, void* stream);
+
+/* flce_forward_backward_async for one shard of a token-sharded batch: every
+ * step divides by *n_valid_total_dev (DEVICE, one int32: the non-ignored
+ * tokens of all shards together) instead of this shard's own count, so
+ *   loss_dev  (device, one fp32, may be NULL) receives this shard's share of
+ *             the batch mean, sum over its tokens of the token loss / total;
+ *   dx        is this shard's rows of the batch's dx, final as written;
+ *   dW        is this shard's term of the batch's dW.
+ * Summing loss_dev and dW over the shards gives the batch's loss and dW. A
+ * total of 0 gives zeros, as for flce_forward_backward. No host
+ * synchronisation; a total below this shard's own count, or negative, is
+ * recorded as INVALID_ARG (and a bad target, or a wait that ran out, as for
+ * the async call) and makes *loss_dev NaN; flce_async_status reports it.
+ * Other arguments and errors as flce_forward_backward_async. */
+flce_status flce_forward_backward_shard(flce_handle_t h, const void* x, const void* W,
+                                        const int64_t* t, int64_t N, int64_t H, int64_t V,
+                                        int64_t ignore_index, int64_t chunk,
+                                        const int32_t* n_valid_total_dev, float* loss_dev,
+                                        void* dx, float* dW, void* stream);
 
 /* The same call with x, W and t in HOST memory: the library copies them into
  * its own device staging buffers on the stream (one cudaMemcpyAsync each),
@@ -337,11 +379,15 @@ const char* flce_last_error(flce_handle_t h);
  *   loss         host, receives the fp32 mean loss
  *   token_loss   device, N fp32 outputs (0 for ignored tokens)
  * The first call on a device looks up the device address of the scratch
- * array (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture. Every call on a device shares the one
- * array, so calls that overlap on the GPU (other streams, other threads)
- * race: run them one after another. Synchronises the stream before
- * returning. Errors: INVALID_ARG, BAD_TARGET, TIMEOUT, CUDA. */
+ * array (cudaGetSymbolAddress) with that device current and keeps it for the
+ * life of the process; that first call should come before any stream
+ * capture begins. Calls after cudaDeviceReset (or any other teardown of the
+ * device's primary context) are not supported: the kept address may then be
+ * stale. Every call on a device shares the one array, which keeps the last
+ * call's contents (each call clears what must start at zero), so calls that
+ * overlap on the GPU (other streams, other threads) race: run them one after
+ * another. Each call ends by synchronising `stream` to read the loss back.
+ * Errors: INVALID_ARG, BAD_TARGET, TIMEOUT, CUDA. */
 flce_status flce_loss_static(const void* x, const void* W, const int64_t* t, int64_t N,
                              int64_t H, int64_t V, int64_t ignore_index, float* loss,
                              float* token_loss, void* stream);

@@ -117,11 +117,16 @@ Layout make_layout(int64_t N, int64_t H, int64_t C, int64_t ldv, int64_t vt, int
 // Tile shape that FLCE_CTA_AUTO resolves to
 constexpr int kAutoCta = FLCE_CTA_WIDE;
 
-// CTAs per GEMM work unit: 1 (single), 2 (pair) or 4 (two pairs sharing B)
+// CTAs per GEMM work unit: 1 (single) or 2 (pair, wide)
 int cta_group_size(const flce_config* cfg) {
   if (cfg->dtype != FLCE_DTYPE_BF16) return 1;
   const int mode = cfg->cta_pair == FLCE_CTA_AUTO ? kAutoCta : cfg->cta_pair;
-  return mode == FLCE_CTA_QUAD ? 4 : (mode == FLCE_CTA_PAIR || mode == FLCE_CTA_WIDE) ? 2 : 1;
+  return (mode == FLCE_CTA_PAIR || mode == FLCE_CTA_WIDE) ? 2 : 1;
+}
+
+bool valid_cta_mode(int mode) {
+  return mode == FLCE_CTA_AUTO || mode == FLCE_CTA_SINGLE || mode == FLCE_CTA_PAIR ||
+         mode == FLCE_CTA_WIDE;
 }
 
 // Output-tile columns of the handle's GEMMs: 512 for wide CTA-pair tiles
@@ -210,6 +215,10 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   }
   if (cfg->dlogits_mode < FLCE_DLOGITS_AUTO || cfg->dlogits_mode > FLCE_DLOGITS_SLABS) {
     *why = "dlogits_mode must be one of FLCE_DLOGITS_*";
+    return FLCE_ERR_INVALID_ARG;
+  }
+  if (!valid_cta_mode(cfg->cta_pair)) {
+    *why = "cta_pair must be one of FLCE_CTA_AUTO, _SINGLE, _PAIR, _WIDE";
     return FLCE_ERR_INVALID_ARG;
   }
   if (num_sms <= 0) num_sms = 152;
@@ -319,6 +328,10 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   out->logits_bytes = static_cast<uint64_t>(C) * out->ldv * esize;
   out->tile_m = tile_m;
   out->tile_n = tile_n;
+  // fp32 handles run SLABS as asked and every other mode in place
+  out->dlogits_mode = slabs ? FLCE_DLOGITS_SLABS
+                      : (bf16 && cfg->dlogits_mode == FLCE_DLOGITS_RECOMPUTE) ? FLCE_DLOGITS_RECOMPUTE
+                                                                               : FLCE_DLOGITS_INPLACE;
   return FLCE_OK;
 }
 
@@ -332,8 +345,6 @@ struct flce_handle_s {
   int num_sms = 0;
   int pair_clusters = 0;  // clusters of two the pair kernels fit at once
   bool use_pair = false;  // GEMMs on CTA pairs (256 x 256 tiles)
-  int quad_clusters = 0;  // clusters of four the quad kernels fit at once
-  bool use_quad = false;  // GEMMs on two pairs sharing B (512 x 256 tiles)
   int wide_clusters = 0;  // clusters of two the wide kernels fit at once
   bool use_wide = false;  // GEMMs on CTA pairs with 256 x 512 tiles
   uint64_t timeout_ns = 0;
@@ -535,17 +546,25 @@ bool map_f32_3d(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, uint64
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The status and loss of a finished call from its control words in host memory.
-flce_status decode_ctrl(flce_handle_t h, const uint32_t* hc, float* loss) {
-  const uint32_t code = hc[kCtrlError];
-  if (loss) std::memcpy(loss, &hc[kCtrlLoss], 4);
+// The status a device error word stands for (0: FLCE_OK).
+flce_status device_status(flce_handle_t h, uint32_t code) {
   if (code == FLCE_ERR_BAD_TARGET)
     return fail(h, FLCE_ERR_BAD_TARGET, "a target is outside [0, V) and is not ignore_index");
   if (code == FLCE_ERR_TIMEOUT)
     return fail(h, FLCE_ERR_TIMEOUT, "a device-side wait ran out (limit %llu ns)",
                 static_cast<unsigned long long>(h->timeout_ns));
+  if (code == FLCE_ERR_INVALID_ARG)
+    return fail(h, FLCE_ERR_INVALID_ARG,
+                "the token-sharded divisor is negative or below this shard's own n_valid");
   if (code != 0) return fail(h, FLCE_ERR_CUDA, "device error word %u", code);
   return FLCE_OK;
+}
+
+// The status and loss of a finished call from its control words in host memory.
+flce_status decode_ctrl(flce_handle_t h, const uint32_t* hc, float* loss) {
+  const uint32_t code = hc[kCtrlError];
+  if (loss) std::memcpy(loss, &hc[kCtrlLoss], 4);
+  return device_status(h, code);
 }
 
 flce_status read_back(flce_handle_t h, uint32_t* ctrl_dev, cudaStream_t s, float* loss) {
@@ -561,7 +580,7 @@ int group_for(flce_handle_t h, int num_m, int num_n, int num_s, int slots) {
   const std::array<int, 4> key{num_m, num_n, num_s, slots};
   auto it = h->group_cache.find(key);
   if (it != h->group_cache.end()) return it->second;
-  const int tile_m = h->use_quad ? 4 * kBM : (h->use_pair || h->use_wide) ? 2 * kBM : kBM;
+  const int tile_m = (h->use_pair || h->use_wide) ? 2 * kBM : kBM;
   const int g = pick_group_m(num_m, num_n, num_s, slots, tile_m, h->use_wide ? 2 * kBN : kBN);
   h->group_cache.emplace(key, g);
   return g;
@@ -569,16 +588,13 @@ int group_for(flce_handle_t h, int num_m, int num_n, int num_s, int slots) {
 
 cudaError_t launch_gemm(flce_handle_t h, int kind, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& o, UmmaArgs args, int64_t M, cudaStream_t s) {
-  const int rows_per_unit = h->use_quad ? 4 * kBM : (h->use_pair || h->use_wide) ? 2 * kBM : kBM;
-  const int slots_max = h->use_quad ? h->quad_clusters
-                        : h->use_wide ? h->wide_clusters
-                        : h->use_pair ? h->pair_clusters : h->num_sms;
+  const int rows_per_unit = (h->use_pair || h->use_wide) ? 2 * kBM : kBM;
+  const int slots_max = h->use_wide ? h->wide_clusters : h->use_pair ? h->pair_clusters : h->num_sms;
   args.num_m = static_cast<int>(cdiv(M, rows_per_unit));
   if (h->use_wide) args.num_n = static_cast<int>(cdiv(args.cols, 2 * kBN));
   const int units = args.num_m * args.num_n * args.num_s;
   const int slots = std::min(units, slots_max);
   if (args.raster == 2) args.group_m = group_for(h, args.num_m, args.num_n, args.num_s, slots);
-  if (h->use_quad) return launch_umma_quad(kind, a, b, o, args, slots, s);
   if (h->use_wide) return launch_umma_wide(kind, a, b, o, args, slots, s);
   if (h->use_pair) return launch_umma_pair(kind, a, b, o, args, slots, s);
   return launch_umma(kind, a, b, o, args, slots, s);
@@ -734,9 +750,12 @@ flce_status slab_backward(flce_handle_t h, const SlabChunk& k, cudaStream_t s, b
 
 // Everything of one call up to its control words on the device (*ctrl_out):
 // the result is read from them once the stream gets there.
+// nv_total: the divisor of a token-sharded batch (device, one int32), or
+// null to divide by this call's own n_valid.
 flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int64_t* t, int64_t N,
                        int64_t H, int64_t V, int64_t ignore_index, int64_t chunk, void* dx,
-                       float* dW, cudaStream_t s, uint32_t** ctrl_out) {
+                       float* dW, cudaStream_t s, uint32_t** ctrl_out,
+                       const int32_t* nv_total = nullptr) {
   NvtxRange nvtx_call("flce_forward_backward");
   if (!W || !dW || (N > 0 && (!x || !t || !dx)))
     return fail(h, FLCE_ERR_INVALID_ARG, "null pointer argument");
@@ -781,7 +800,8 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     *ctrl_out = ctrl;
     return FLCE_OK;
   }
-  FLCE_LAUNCH(FLCE_K_COUNT_VALID, 0.0, 8.0 * N, launch_count_valid(t, N, V, ignore_index, ctrl, s));
+  FLCE_LAUNCH(FLCE_K_COUNT_VALID, 0.0, 8.0 * N,
+              launch_count_valid(t, N, V, ignore_index, nv_total, ctrl, s));
 
   const int64_t C = p.chunk, ldv = p.ldv;
   const int vt = static_cast<int>(p.vocab_tiles);
@@ -868,7 +888,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     const bool recompute = h->cfg.dlogits_mode == FLCE_DLOGITS_RECOMPUTE;
     const bool slabs = h->cfg.dlogits_mode == FLCE_DLOGITS_SLABS;
     const int64_t zw = slabs ? p.vocab_slab : V;  // columns of the chunk buffer
-    const int b_box = h->use_quad ? 64 : (h->use_pair || h->use_wide) ? 128 : 256;
+    const int b_box = (h->use_pair || h->use_wide) ? 128 : 256;
     CUtensorMap mW_k, mW_mn, mX_k, mX_mn, mZ_out, mZ_k, mZ_mn, mDx, mDw;
     // a CTA of a pair loads 128 of the tile's 256 columns of a K-major B
     if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, b_box, &why) ||
@@ -1071,7 +1091,8 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
   if (!out || !cfg) return FLCE_ERR_INVALID_ARG;
   *out = nullptr;
   if (cfg->dtype != FLCE_DTYPE_BF16 && cfg->dtype != FLCE_DTYPE_FP32) return FLCE_ERR_UNSUPPORTED;
-  if (cfg->dlogits_mode < FLCE_DLOGITS_AUTO || cfg->dlogits_mode > FLCE_DLOGITS_SLABS)
+  if (cfg->dlogits_mode < FLCE_DLOGITS_AUTO || cfg->dlogits_mode > FLCE_DLOGITS_SLABS ||
+      !valid_cta_mode(cfg->cta_pair))
     return FLCE_ERR_INVALID_ARG;
   int count = 0;
   if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
@@ -1091,14 +1112,7 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
   DeviceGuard g(h->device);
   if (cfg->dtype == FLCE_DTYPE_BF16) {
     const int group = cta_group_size(cfg);
-    if (group == 4) {
-      h->quad_clusters = umma_quad_max_clusters();
-      if (h->quad_clusters <= 0) {
-        delete h;
-        return FLCE_ERR_UNSUPPORTED;
-      }
-      h->use_quad = true;
-    } else if (group == 2 && tile_cols(cfg) == 2 * kBN) {
+    if (group == 2 && tile_cols(cfg) == 2 * kBN) {
       h->wide_clusters = umma_wide_max_clusters();
       if (h->wide_clusters <= 0) {
         delete h;
@@ -1114,10 +1128,7 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
       h->use_pair = h->pair_clusters > 0;
     }
     // the handle's plans follow the tile shape it actually runs
-    h->cfg.cta_pair = h->use_quad   ? FLCE_CTA_QUAD
-                      : h->use_wide ? FLCE_CTA_WIDE
-                      : h->use_pair ? FLCE_CTA_PAIR
-                                    : FLCE_CTA_SINGLE;
+    h->cfg.cta_pair = h->use_wide ? FLCE_CTA_WIDE : h->use_pair ? FLCE_CTA_PAIR : FLCE_CTA_SINGLE;
   }
   if (cudaMallocHost(&h->host_ctrl, kCtrlWords * 4) != cudaSuccess) {
     cudaGetLastError();
@@ -1212,10 +1223,40 @@ flce_status flce_async_status(flce_handle_t h, void* stream) {
   e = cudaMemcpy(&code, sticky, 4, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && code != 0) e = cudaMemset(sticky, 0, 4);
   if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "async status: %s", cudaGetErrorString(e));
-  if (code == FLCE_ERR_BAD_TARGET)
-    return fail(h, FLCE_ERR_BAD_TARGET, "a target is outside [0, V) and is not ignore_index");
-  if (code == FLCE_ERR_TIMEOUT) return fail(h, FLCE_ERR_TIMEOUT, "a device-side wait ran out");
-  if (code != 0) return fail(h, FLCE_ERR_CUDA, "device error word %u", code);
+  return device_status(h, code);
+}
+
+flce_status flce_count_valid(flce_handle_t h, const int64_t* t, int64_t N, int64_t ignore_index,
+                             int32_t* n_valid_dev, void* stream) {
+  if (!h) return FLCE_ERR_INVALID_ARG;
+  h->err.clear();
+  if (!n_valid_dev || (N > 0 && !t) || N < 0 || N > kMaxDim)
+    return fail(h, FLCE_ERR_INVALID_ARG, "null pointer or bad size");
+  if ((reinterpret_cast<uintptr_t>(t) & 7u) || (reinterpret_cast<uintptr_t>(n_valid_dev) & 3u))
+    return fail(h, FLCE_ERR_INVALID_ARG, "t must be 8-byte and n_valid_dev 4-byte aligned");
+  DeviceGuard g(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  FLCE_LAUNCH(FLCE_K_COUNT_VALID, 0.0, 8.0 * N + 4.0, launch_count_only(t, N, ignore_index, n_valid_dev, s));
+  return FLCE_OK;
+}
+
+flce_status flce_forward_backward_shard(flce_handle_t h, const void* x, const void* W,
+                                        const int64_t* t, int64_t N, int64_t H, int64_t V,
+                                        int64_t ignore_index, int64_t chunk,
+                                        const int32_t* n_valid_total_dev, float* loss_dev,
+                                        void* dx, float* dW, void* stream) {
+  if (!h) return FLCE_ERR_INVALID_ARG;
+  h->err.clear();
+  if (!n_valid_total_dev || (reinterpret_cast<uintptr_t>(n_valid_total_dev) & 3u) ||
+      (reinterpret_cast<uintptr_t>(loss_dev) & 3u))
+    return fail(h, FLCE_ERR_INVALID_ARG, "n_valid_total_dev (non-null) and loss_dev must be 4-byte aligned");
+  DeviceGuard g(h->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* ctrl = nullptr;
+  const flce_status st =
+      enqueue_fb(h, x, W, t, N, H, V, ignore_index, chunk, dx, dW, s, &ctrl, n_valid_total_dev);
+  if (st != FLCE_OK) return st;
+  FLCE_LAUNCH(FLCE_K_DEVICE_RESULT, 0.0, 16.0, launch_device_result(ctrl, loss_dev, nullptr, s));
   return FLCE_OK;
 }
 
@@ -1370,7 +1411,7 @@ flce_status flce_check_gemm(flce_handle_t h, int32_t a_mn_major, int32_t b_mn_ma
   bool ok = a_mn_major ? map_bf16_2d(&ma, A, M, K, M * 2, 64, 64, &why)
                        : map_bf16_2d(&ma, A, K, M, K * 2, 64, 128, &why);
   ok = ok && (b_mn_major ? map_bf16_2d(&mb, B, N, K, N * 2, 64, 64, &why)
-                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, h->use_quad ? 64 : (h->use_pair || h->use_wide) ? 128 : 256, &why));
+                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, (h->use_pair || h->use_wide) ? 128 : 256, &why));
   ok = ok && map_f32_3d(&mc, C, N, M, 1, N * 4, static_cast<uint64_t>(M) * N * 4, &why);
   if (!ok) return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
   UmmaArgs a{};

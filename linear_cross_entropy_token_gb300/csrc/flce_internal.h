@@ -13,6 +13,8 @@ enum CtrlWord : int {
   kCtrlNValid = 1,   // number of non-ignored tokens
   kCtrlLoss = 2,     // fp32 bits of the mean loss
   kCtrlSched = 3,    // work-unit counter of a dynamically scheduled launch
+  kCtrlNValidLocal = 4,  // this call's own non-ignored tokens (kCtrlNValid may be a
+                         // token-sharded batch's total)
   kCtrlSticky = 15,  // first error of the device-result calls, kept across calls
   kCtrlWords = 16
 };
@@ -81,11 +83,6 @@ int umma_pair_max_clusters();
 cudaError_t launch_umma_wide(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                              const UmmaArgs& args, int pairs, cudaStream_t s);
 int umma_wide_max_clusters();
-// Two CTA pairs per cluster sharing B through multicast: 512 x 256 tiles;
-// num_m counts 512-row tiles; B maps of K-major operands use a 64 x 64 box
-cudaError_t launch_umma_quad(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                             const UmmaArgs& args, int quads, cudaStream_t s);
-int umma_quad_max_clusters();
 
 // The dx and dW GEMMs of one chunk in one CTA-pair launch: problem 0 = dx
 // (A K-major), problem 1 = dW (A MN-major); B MN-major, fp32 epilogue in both.
@@ -104,8 +101,12 @@ cudaError_t launch_umma_pair_dual(const DualMaps& maps, const DualArgs& args, in
 cudaError_t launch_wait_check(uint32_t* ctrl, uint64_t timeout_ns, cudaStream_t s);
 
 // flce_rows.cu
+// nv_total: device divisor of a token-sharded batch, or null (divide by the
+// call's own count)
 cudaError_t launch_count_valid(const int64_t* t, int64_t N, int64_t V, int64_t ignore_index,
-                               uint32_t* ctrl, cudaStream_t s);
+                               const int32_t* nv_total, uint32_t* ctrl, cudaStream_t s);
+cudaError_t launch_count_only(const int64_t* t, int64_t N, int64_t ignore_index, int32_t* out,
+                              cudaStream_t s);
 cudaError_t launch_lse_combine(const float2* partials, int vocab_tiles, const float* zt,
                                const int64_t* t_chunk, int rows, int64_t ignore_index, float* lse,
                                float* token_loss_chunk, cudaStream_t s);

@@ -28,8 +28,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 // n_valid = #{i : t_i != ignore_index}; any other target outside [0, V)
 // records FLCE_ERR_BAD_TARGET. One block; fixed-order integer sum.
+// nv_total (device, may be null) is the divisor of a token-sharded batch:
+// the number of non-ignored tokens over every shard. When given, it becomes
+// the n_valid word that every later step of the call divides by, and the
+// local count goes to kCtrlNValidLocal; a total below the local count is an
+// argument error.
 __global__ void count_valid_kernel(const int64_t* __restrict__ t, int64_t N, int64_t V,
-                                   int64_t ignore_index, uint32_t* ctrl) {
+                                   int64_t ignore_index, const int32_t* __restrict__ nv_total,
+                                   uint32_t* ctrl) {
   __shared__ uint32_t warp_cnt[32];
   uint32_t cnt = 0;
   bool bad = false;
@@ -48,7 +54,39 @@ __global__ void count_valid_kernel(const int64_t* __restrict__ t, int64_t N, int
     uint32_t c = threadIdx.x < (blockDim.x >> 5) ? warp_cnt[threadIdx.x] : 0u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    if (threadIdx.x == 0) ctrl[kCtrlNValid] = c;
+    if (threadIdx.x == 0) {
+      ctrl[kCtrlNValidLocal] = c;
+      if (nv_total) {
+        const int32_t tot = *nv_total;
+        if (tot < 0 || static_cast<uint32_t>(tot) < c) {
+          atomicCAS(ctrl + kCtrlError, 0u, kErrInvalidArg);
+          ctrl[kCtrlNValid] = c;
+        } else {
+          ctrl[kCtrlNValid] = static_cast<uint32_t>(tot);
+        }
+      } else {
+        ctrl[kCtrlNValid] = c;
+      }
+    }
+  }
+}
+
+// The count alone, into caller device memory: #{i : t_i != ignore_index}.
+// One block; fixed-order integer sum.
+__global__ void count_only_kernel(const int64_t* __restrict__ t, int64_t N, int64_t ignore_index,
+                                  int32_t* __restrict__ out) {
+  __shared__ uint32_t warp_cnt[32];
+  uint32_t cnt = 0;
+  for (int64_t i = threadIdx.x; i < N; i += blockDim.x) cnt += t[i] != ignore_index ? 1u : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if ((threadIdx.x & 31) == 0) warp_cnt[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    uint32_t c = threadIdx.x < (blockDim.x >> 5) ? warp_cnt[threadIdx.x] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (threadIdx.x == 0) *out = static_cast<int32_t>(c);
   }
 }
 
@@ -271,8 +309,14 @@ cudaError_t launch_device_result(uint32_t* ctrl, float* loss_dev, int32_t* n_val
 }
 
 cudaError_t launch_count_valid(const int64_t* t, int64_t N, int64_t V, int64_t ignore_index,
-                               uint32_t* ctrl, cudaStream_t s) {
-  count_valid_kernel<<<1, 1024, 0, s>>>(t, N, V, ignore_index, ctrl);
+                               const int32_t* nv_total, uint32_t* ctrl, cudaStream_t s) {
+  count_valid_kernel<<<1, 1024, 0, s>>>(t, N, V, ignore_index, nv_total, ctrl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_count_only(const int64_t* t, int64_t N, int64_t ignore_index, int32_t* out,
+                              cudaStream_t s) {
+  count_only_kernel<<<1, 1024, 0, s>>>(t, N, ignore_index, out);
   return cudaGetLastError();
 }
 

@@ -121,7 +121,7 @@ extern "C" flce_status flce_loss_static(const void* x, const void* W, const int6
   // the array keeps the last call's contents: clear the control block
   if (cudaMemsetAsync(ctrl, 0, kCtrlBytes, s) != cudaSuccess) return FLCE_ERR_CUDA;
   if (N > 0) {
-    if (launch_count_valid(t, N, V, ignore_index, ctrl, s) != cudaSuccess) return FLCE_ERR_CUDA;
+    if (launch_count_valid(t, N, V, ignore_index, nullptr, ctrl, s) != cudaSuccess) return FLCE_ERR_CUDA;
     CUtensorMap mW, mX;
     if (!encode_bf16_2d(&mW, W, H, V, H * 2, 64, 256)) return FLCE_ERR_INVALID_ARG;
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);

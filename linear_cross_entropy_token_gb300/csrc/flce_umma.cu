@@ -918,201 +918,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
   }
 }
 
-// ============================================ two CTA pairs sharing B (quad)
-//
-// A cluster of four CTAs is two CTA pairs (ranks 0,1 and 2,3) on the same
-// 256 output columns and on consecutive 256-row blocks: a 512 x 256 tile.
-// CTAs with the same rank in their pair need the same 128 columns of B, so
-// each of the two loads half of those columns (64) and multicasts it to
-// both: per CTA and k-block, 16 KB of A plus 8 KB of B come from L2 instead
-// of 16 + 16, and the 8 CTA groups that share a B tile in the m-fastest
-// order fetch it half as often. A stage of a CTA is written by its twin in
-// the other pair too, so both pairs' MMAs must release it: each pair's MMA
-// commit is multicast to the "empty" barriers of all four CTAs (count 2).
-
-template <int AMN, int BMN, int EPI>
-__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
-    umma_quad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmO, const UmmaArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kStagesPair * kABytes;
-  uint8_t* sE = sB + kStagesPair * kBHalfBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesPair + 5);
-
-  const uint32_t bar0 = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kStagesPair + s); };
-  auto tfull_bar = [&](int acc) { return bar0 + 8u * (2 * kStagesPair + acc); };
-  auto tempty_bar = [&](int acc) { return bar0 + 8u * (2 * kStagesPair + 2 + acc); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kStagesPair + 4);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();   // 0..3
-  const uint32_t prank = crank & 1u;          // 0: issues its pair's MMAs
-  const uint32_t pidx = crank >> 1;           // which pair of the cluster
-  const uint32_t lead = crank & ~1u;          // cluster rank of this pair's issuing CTA
-  const int quad = static_cast<int>(cluster_id_x());
-  const int nquads = static_cast<int>(num_clusters_x());
-  const uint16_t twins = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
-  const uint16_t my_pair = static_cast<uint16_t>(0x3u << (2 * pidx));
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesPair; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 2);   // released by the MMA of each pair
-    }
-    for (int acc = 0; acc < 2; ++acc) {
-      mbar_init(tfull_bar(acc), 1);
-      mbar_init(tempty_bar(acc), 2 * kEpiThreads);
-    }
-    mbar_init(drain_bar, 1);
-    fence_mbar_init();
-    fence_proxy_async_smem();
-    tma_prefetch_map(&tmA);
-    tma_prefetch_map(&tmB);
-    tma_prefetch_map(&tmO);
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish_pair();
-  }
-  __syncthreads();
-  cluster_sync();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  const int num_units = a.num_m * a.num_n * a.num_s;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      uint32_t n_issued = 0;
-      bool failed = false;
-      for (int u = quad; u < num_units && !failed; u += nquads) {
-        const Unit t = unit_coords(a, u);
-        const int kb0 = t.s * a.kb_per_split;
-        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
-        const int mA = t.m * 4 * kBM + static_cast<int>(pidx * 2 + prank) * kBM;  // this CTA's A rows
-        const int nB = t.n * kBN + static_cast<int>(prank) * (kBN / 2) + static_cast<int>(pidx) * 64;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const int stage = n_issued % kStagesPair;
-          const uint32_t phase = (n_issued / kStagesPair) & 1u;
-          if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, a.ctrl, a.timeout_ns)) {
-            failed = true;
-            break;
-          }
-          if (prank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytesPair);
-          const uint32_t fb = mapa_shared(full_bar(stage), lead);
-          const uint32_t sa = smem_u32(sA + stage * kABytes);
-          const uint32_t sb = smem_u32(sB + stage * kBHalfBytes) + 8192u * pidx;
-          const int k0 = kb * kBK;
-          if (AMN == 0) {
-            tma_load_2d_pair(sa, &tmA, fb, k0, mA);
-          } else {
-            tma_load_2d_pair(sa, &tmA, fb, mA, k0);
-            tma_load_2d_pair(sa + 8192, &tmA, fb, mA + 64, k0);
-          }
-          // 64 of this CTA's 128 B columns, to this CTA and its twin
-          if (BMN == 0)
-            tma_load_2d_pair_multicast(sb, &tmB, fb, k0, nB, twins);
-          else
-            tma_load_2d_pair_multicast(sb, &tmB, fb, nB, k0, twins);
-          ++n_issued;
-        }
-      }
-      if (failed && prank == 0) {
-        const uint32_t first = n_issued > kStagesPair ? n_issued - kStagesPair : 0;
-        for (uint32_t i = first; i < n_issued; ++i)
-          mbar_drain_wait(full_bar(i % kStagesPair), (i / kStagesPair) & 1u, a.timeout_ns);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && prank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, AMN, BMN);
-      uint32_t n_consumed = 0;
-      bool issued = false, failed = false;
-      int it = 0;
-      for (int u = quad; u < num_units && !failed; u += nquads, ++it) {
-        const Unit t = unit_coords(a, u);
-        const int kb0 = t.s * a.kb_per_split;
-        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait_bounded_cluster(tempty_bar(acc), acc_phase ^ 1u, a.ctrl, a.timeout_ns)) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kBN;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const int stage = n_consumed % kStagesPair;
-          const uint32_t phase = (n_consumed / kStagesPair) & 1u;
-          if (!mbar_wait_bounded_cluster(full_bar(stage), phase, a.ctrl, a.timeout_ns)) {
-            failed = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(sA + stage * kABytes);
-          const uint32_t sb = smem_u32(sB + stage * kBHalfBytes);
-#pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = AMN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
-                                    : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-            const uint64_t bd = BMN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
-                                    : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
-            tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-          }
-          issued = true;
-          tc_commit_pair_multicast(empty_bar(stage), 0xF);
-          ++n_consumed;
-        }
-        if (failed) break;
-        tc_commit_pair_multicast(tfull_bar(acc), my_pair);
-      }
-      if (failed && issued) {
-        tc_commit_pair(drain_bar);
-        mbar_drain_wait(drain_bar, 0, a.timeout_ns);
-      }
-    }
-  } else {
-    const int wq = warp & 3;
-    const int row = wq * 32 + lane;
-    const bool leader = threadIdx.x == 64;
-    uint32_t ebuf = 0;
-    int it = 0;
-    for (int u = quad; u < num_units; u += nquads, ++it) {
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
-      const bool ok = mbar_wait_bounded_cluster(tfull_bar(acc), acc_phase, a.ctrl, a.timeout_ns);
-      if (named_bar_or(kEpiBar, kEpiThreads, !ok)) break;
-      tc_fence_after();
-      const Unit t = unit_coords(a, u);
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + acc * kBN;
-      const int m0 = t.m * 4 * kBM + static_cast<int>(pidx * 2 + prank) * kBM;
-      epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, m0, t.n * kBN, t.n, t.s, tbase, [&] {
-        tc_fence_before();
-        if (prank == 0)
-          mbar_arrive(tempty_bar(acc));
-        else
-          mbar_arrive_cluster(mapa_shared(tempty_bar(acc), lead));
-      });
-    }
-    if (leader) bulk_wait_group<0>();
-  }
-
-  __syncwarp();
-  __syncthreads();
-  cluster_sync();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, kTmemCols);
-  }
-}
-
 // ============================================ dx and dW GEMMs in one launch
 //
 // Both backward contractions of a chunk read the finished dlogits buffer
@@ -1503,58 +1308,6 @@ int umma_wide_max_clusters() {
   auto kern = umma_wide_kernel<1, 1, kEpiF32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kSmemBytesWide)) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
-}
-
-// grid = 4 x quads (a multiple of the cluster size)
-template <int AMN, int BMN, int EPI>
-cudaError_t launch_quad_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
-                          const UmmaArgs& args, int quads, cudaStream_t s) {
-  auto kern = umma_quad_kernel<AMN, BMN, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytesPair));
-  if (e != cudaSuccess) return e;
-  kern<<<4 * quads, kThreads, kSmemBytesPair, s>>>(ta, tb, to, args);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_umma_quad(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                             const UmmaArgs& args, int quads, cudaStream_t s) {
-  switch (kind) {
-    case kUmmaLogits: return launch_quad_t<0, 0, kEpiLse>(a, b, o, args, quads, s);
-    case kUmmaDlogits: return launch_quad_t<0, 0, kEpiDlogits>(a, b, o, args, quads, s);
-    case kUmmaDxF32: return launch_quad_t<0, 1, kEpiF32>(a, b, o, args, quads, s);
-    case kUmmaDw: return launch_quad_t<1, 1, kEpiF32>(a, b, o, args, quads, s);
-    case kUmmaCheckKK: return launch_quad_t<0, 0, kEpiF32>(a, b, o, args, quads, s);
-    case kUmmaCheckMK: return launch_quad_t<1, 0, kEpiF32>(a, b, o, args, quads, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-// Clusters of four that fit on the device at once for the quad kernels
-int umma_quad_max_clusters() {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(4, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytesPair;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = 4;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  auto kern = umma_quad_kernel<1, 1, kEpiF32>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytesPair)) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }

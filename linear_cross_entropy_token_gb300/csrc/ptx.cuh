@@ -7,6 +7,7 @@
 namespace flce {
 
 // device error word values (same numbering as flce_status)
+constexpr uint32_t kErrInvalidArg = 1;
 constexpr uint32_t kErrBadTarget = 4;
 constexpr uint32_t kErrTimeout = 5;
 
@@ -324,18 +325,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-
-// The same load delivered to every CTA in cta_mask (same shared-memory
-// offset in each); the transaction bytes are counted, for each destination,
-// on the mbarrier at bar's offset in the even CTA of that destination's pair
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                                           int32_t c0, int32_t c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
       : "memory");
 }
 

@@ -21,7 +21,8 @@ STATUS = {0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_UNSUPPORTED", 3:
           4: "FLCE_ERR_BAD_TARGET", 5: "FLCE_ERR_TIMEOUT", 6: "FLCE_ERR_CUDA"}
 DTYPE_BF16, DTYPE_FP32 = 0, 1
 DLOGITS = {"auto": 0, "inplace": 1, "recompute": 2, "slabs": 3}
-CTA = {"auto": 0, "single": 1, "pair": 2, "quad": 3, "wide": 4}
+DLOGITS_NAMES = {v: k for k, v in DLOGITS.items()}
+CTA = {"auto": 0, "single": 1, "pair": 2, "wide": 4}
 BACKWARD = {"auto": 0, "separate": 1, "one_launch": 2}
 KERNEL_KINDS = ["count_valid", "gemm_logits_lse", "lse_combine", "dlogits_inplace",
                 "gemm_dlogits_recompute", "gemm_dx", "dx_split_reduce", "gemm_dw",
@@ -48,10 +49,13 @@ class Plan(ctypes.Structure):
                 ("vocab_tiles", ctypes.c_int64), ("ldv", ctypes.c_int64),
                 ("dx_splits", ctypes.c_int64), ("workspace_bytes", ctypes.c_uint64),
                 ("logits_bytes", ctypes.c_uint64), ("tile_m", ctypes.c_int64),
-                ("tile_n", ctypes.c_int64), ("vocab_slab", ctypes.c_int64)]
+                ("tile_n", ctypes.c_int64), ("vocab_slab", ctypes.c_int64),
+                ("dlogits_mode", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
-        return {k: getattr(self, k) for k, _ in self._fields_}
+        d = {k: getattr(self, k) for k, _ in self._fields_}
+        d["dlogits"] = DLOGITS_NAMES.get(d["dlogits_mode"], str(d["dlogits_mode"]))
+        return d
 
 
 class KernelProfile(ctypes.Structure):
@@ -86,6 +90,9 @@ def load() -> ctypes.CDLL:
         "flce_forward_backward_async": (i32, [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp,
                                               vp, vp]),
         "flce_async_status": (i32, [vp, vp]),
+        "flce_count_valid": (i32, [vp, vp, i64, i64, vp, vp]),
+        "flce_forward_backward_shard": (i32, [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp,
+                                              vp, vp]),
         "flce_submit_host": (i32, [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp,
                                    ctypes.POINTER(u64)]),
         "flce_wait": (i32, [vp, u64, ctypes.POINTER(ctypes.c_float)]),
@@ -256,6 +263,53 @@ class FLCE:
                                                   _stream_ptr(dev))
         self._check(st, "flce_forward_backward_async")
         return loss, n_valid, dx, dW
+
+    def count_valid(self, t, ignore_index: int = -100, out=None):
+        """This rank's non-ignored token count as a 0-dim int32 device tensor,
+        written when the current stream gets there (no host sync)."""
+        import torch
+        dev = torch.device("cuda", self.device)
+        if t.dim() != 1 or t.dtype != torch.int64 or t.device != dev or not t.is_contiguous():
+            raise ValueError(f"t must be a contiguous 1-D int64 tensor on {dev}")
+        if out is None:
+            out = torch.empty((), dtype=torch.int32, device=dev)
+        elif out.numel() != 1 or out.dtype != torch.int32 or out.device != dev:
+            raise ValueError(f"out must be one int32 element on {dev}")
+        st = self.lib.flce_count_valid(self.h, t.data_ptr(), t.shape[0], ignore_index,
+                                       out.data_ptr(), _stream_ptr(dev))
+        self._check(st, "flce_count_valid")
+        return out
+
+    def forward_backward_shard(self, x, W, t, n_valid_total, ignore_index: int = -100,
+                               chunk: int = 0, loss=None, dx=None, dW=None):
+        """One shard of a token-sharded batch: the fused call dividing by
+        n_valid_total (a one-element int32 device tensor, the non-ignored
+        tokens of every shard). Returns device tensors (loss, this shard's
+        share of the batch mean; dx, this shard's rows; dW, this shard's
+        term), with no host synchronisation; async_status() reports
+        device-side errors."""
+        import torch
+        dev = torch.device("cuda", self.device)
+        check_call_tensors(x, W, t, dx, dW, self._torch_dtype(), dev, dev)
+        if (n_valid_total.numel() != 1 or n_valid_total.dtype != torch.int32
+                or n_valid_total.device != dev):
+            raise ValueError(f"n_valid_total must be one int32 element on {dev}")
+        if loss is not None and (loss.numel() != 1 or loss.dtype != torch.float32 or loss.device != dev):
+            raise ValueError(f"loss must be one float32 element on {dev}")
+        N, H = x.shape
+        V = W.shape[0]
+        if loss is None:
+            loss = torch.empty((), dtype=torch.float32, device=dev)
+        if dx is None:
+            dx = torch.empty_like(x)
+        if dW is None:
+            dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+        st = self.lib.flce_forward_backward_shard(self.h, x.data_ptr(), W.data_ptr(), t.data_ptr(), N,
+                                                  H, V, ignore_index, chunk, n_valid_total.data_ptr(),
+                                                  loss.data_ptr(), dx.data_ptr(), dW.data_ptr(),
+                                                  _stream_ptr(dev))
+        self._check(st, "flce_forward_backward_shard")
+        return loss, dx, dW
 
     def async_status(self) -> None:
         """Wait for the current stream; raise FlceError for a device-side

@@ -44,7 +44,7 @@ RAW_METRICS = [
 
 
 def kind_of(name: str) -> str:
-    m = re.search(r"umma_(?:gemm|pair|wide|quad)_kernel<(\d+), (\d+), (\d+)>", name)
+    m = re.search(r"umma_(?:gemm|pair|wide)_kernel<(\d+), (\d+), (\d+)>", name)
     if m:
         return _GEMM.get(tuple(int(v) for v in m.groups()), "gemm_other")
     for k, v in _PLAIN.items():

@@ -24,7 +24,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.flce_abi_version() == 3
+    assert lib.flce_abi_version() == 4
     assert lib.flce_status_string(0) == b"FLCE_OK"
     assert lib.flce_status_string(4) == b"FLCE_ERR_BAD_TARGET"
     assert lib.flce_kernel_name(1) == b"gemm_logits_lse"
@@ -186,3 +186,19 @@ def test_plan_invariants_over_extreme_shapes():
         assert p["workspace_bytes"] <= (budget or int(1.25 * GiB))
         assert p["num_chunks"] * p["chunk"] >= N > (p["num_chunks"] - 1) * p["chunk"]
         assert p["ldv"] % 64 == 0 and p["ldv"] >= vs
+        assert p["dlogits"] == mode
+
+
+def test_plan_reports_the_mode_it_runs():
+    """AUTO resolves to INPLACE; an fp32 handle runs RECOMPUTE in place."""
+    assert flce.plan(4096, 1024, 32000)["dlogits"] == "inplace"
+    assert flce.plan(4096, 1024, 32000, dlogits_mode="recompute")["dlogits"] == "recompute"
+    assert flce.plan(4096, 1024, 32000, dtype="fp32", dlogits_mode="recompute")["dlogits"] == "inplace"
+    assert flce.plan(4096, 1024, 32000, dlogits_mode="slabs")["dlogits"] == "slabs"
+
+
+def test_plan_refuses_a_tile_shape_that_does_not_exist(lib):
+    cfg = flce.make_config("bf16", 0)
+    cfg.cta_pair = 3
+    p = flce.Plan()
+    assert lib.flce_make_plan(ctypes.byref(cfg), 1024, 256, 1000, 0, 0, ctypes.byref(p)) == 1

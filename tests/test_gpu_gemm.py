@@ -9,7 +9,7 @@ import torch
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=["single", "pair", "quad", "wide"])
+@pytest.fixture(scope="module", params=["single", "pair", "wide"])
 def handle(request):
     from linear_cross_entropy_token_gb300 import FLCE
     h = FLCE("bf16", 0, cta=request.param)

@@ -14,7 +14,7 @@ from flce_testing import assert_parity, device_inputs, rel_fro, run, to_np64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=["single", "pair", "pair-one_launch", "quad", "wide"])
+@pytest.fixture(scope="module", params=["single", "pair", "pair-one_launch", "wide"])
 def bf16(request):
     """Both GEMM tile shapes: one CTA per 128 x 256 tile, and CTA pairs per
     256 x 256 tile, with the dx and dW GEMMs in one dynamically scheduled

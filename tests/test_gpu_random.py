@@ -12,7 +12,7 @@ from flce_testing import assert_parity, run
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = ("single", "pair", "quad", "wide")
+SHAPES = ("single", "pair", "wide")
 
 
 @pytest.fixture(scope="module")

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 BUDGET = 48 << 20
 
 
-@pytest.fixture(scope="module", params=["wide", "pair", "single", "quad"])
+@pytest.fixture(scope="module", params=["wide", "pair", "single"])
 def slabs(request):
     from linear_cross_entropy_token_gb300 import FLCE
     h = FLCE("bf16", 0, dlogits_mode="slabs", cta=request.param, hbm_budget_bytes=BUDGET)

@@ -1,0 +1,88 @@
+"""The 131,072-token long-context batch (H = 4096, V = 128256, uniform
+targets, none ignored) in the launch configuration bench.py times: the
+default HBM budget, 28 planned chunks of 4736 tokens, the last one ragged.
+
+Every output the method defines is checked against the fp64 oracle: the
+loss from every token's log-sum-exp (the oracle runs about 1.4e14 FLOPs of
+float64 products for it, minutes of host time, hence its own module
+collected late), sampled token losses, sampled rows of dx, and sampled rows
+of dW, including the vocabulary's last entries and rows that are targets.
+The extra device memory stays at the chunk workspace, far below the 33.6 GB
+of full bf16 logits that the chunked schedule of the FLCE page ("Fused
+Linear Cross-Entropy: LLM 학습 logits 메모리 병목 없애기", section "FLCE의 핵심
+아이디어: logits을 오래 들고 있지 않는다") never holds."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from flce_testing import LOSS_RTOL, device_inputs, rel_fro
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+GiB = 1 << 30
+
+
+def _rows(w, n=48, seed=0):
+    g = np.random.default_rng(seed)
+    rows = set(g.choice(w.N, n, replace=False).tolist()) | {0, 4735, 4736, w.N - 1}
+    return np.array(sorted(rows))
+
+
+def _vocab(w, n=40, seed=1):
+    g = np.random.default_rng(seed)
+    J = set(range(4)) | {w.V - 1, w.V - 2, w.V - 3, w.V // 2}
+    J |= set(g.choice(w.V, n, replace=False).tolist())
+    J |= set(np.unique(w.t)[:6].tolist())             # rows that are some token's target
+    return np.array(sorted(J))
+
+
+def test_long_context_against_the_full_oracle():
+    from linear_cross_entropy_token_gb300 import FLCE
+    w = workloads.make("long_bf16")
+    h = FLCE("bf16", 0)
+    try:
+        x, W, t = device_inputs(w)
+        dx = torch.empty_like(x)
+        dW = torch.empty(W.shape, dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        loss, _, _ = h.forward_backward(x, W, t, dx=dx, dW=dW)
+        free1, _ = torch.cuda.mem_get_info()
+        tl = h.token_losses(w.N)
+        plan = h.last_plan()
+        torch.cuda.synchronize()
+        # plan and memory: O(C·V) workspace, never the full logits
+        assert (plan["chunk"], plan["num_chunks"]) == (4736, 28)
+        assert plan["workspace_bytes"] <= int(1.25 * GiB)
+        assert free0 - free1 <= plan["workspace_bytes"] + (64 << 20)
+        assert plan["workspace_bytes"] * 20 < w.N * w.V * 2
+        rows, J = _rows(w), _vocab(w)
+        got_tl = tl.double().cpu().numpy()
+        got_dx = dx[torch.from_numpy(rows).cuda()].double().cpu().numpy()
+        got_dw = dW[torch.from_numpy(J).cuda()].double().cpu().numpy()
+        del x, W, t, dx, dW
+        torch.cuda.empty_cache()
+    finally:
+        h.close()
+
+    xr = workloads.F64Rows(w.x)
+    Wd = w.W_f64()
+    valid = oracle.valid_mask(w.t, w.ignore_index)
+    n_valid = int(valid.sum())
+    assert n_valid == w.N
+    lse = oracle.lse_rows(xr, Wd, np.arange(w.N), block=512)
+    zt = np.zeros(w.N)
+    for s in range(0, w.N, 4096):
+        r = np.arange(s, min(w.N, s + 4096))
+        zt[r] = np.einsum("ij,ij->i", w.x_f64(r), Wd[w.t[r]])
+    ref_tl = oracle.token_losses(lse, zt, valid)
+    ref_loss = float(ref_tl.sum()) / n_valid
+    assert abs(loss - ref_loss) / ref_loss <= LOSS_RTOL, (loss, ref_loss)
+    # every token's loss, not a sample: they come with the full log-sum-exp
+    assert rel_fro(got_tl, ref_tl) <= LOSS_RTOL
+    assert np.abs(got_tl - ref_tl).max() <= 1e-2 * np.abs(ref_tl).max()
+    assert rel_fro(got_dx, oracle.dx_rows(xr, Wd, w.t, rows, n_valid)) <= 1e-2
+    assert len(J) >= 40
+    assert rel_fro(got_dw, oracle.dW_rows(xr, Wd, w.t, J, lse, n_valid)) <= 1e-2

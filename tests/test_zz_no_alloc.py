@@ -4,11 +4,18 @@ It serves callers that cannot let a library call cudaMalloc: a framework
 whose pool allocator must account for every byte of device memory, a runtime
 on a fixed memory plan, or code that must not pay the device-wide
 synchronisation of cudaFree. Its scratch is a static device array inside the
-library, so this test checks three things through the C ABI. Its loss and
-per-token losses match those of the handle-based flce_forward_backward, on
-two calls in a row with different shapes (the shared scratch keeps the
-previous call's contents). A repeated call takes no device memory. Sizes
-beyond the scratch are refused.
+library, so this test checks, through the C ABI, on several calls in a row
+with different shapes (the shared scratch keeps the previous call's
+contents):
+
+* its loss and per-token losses against the fp64 oracle, and against those
+  of the handle-based flce_forward_backward, within the loss tolerance of
+  the other tests;
+* batches of one chunk, of several chunks with a ragged last one, and a
+  vocabulary so large that the scratch bound shortens the chunk below 4096
+  tokens;
+* that a repeated call takes no device memory, and that sizes beyond the
+  scratch are refused.
 
 This file is collected last on purpose: a run that stops at its first failure
 has then already run every other test.
@@ -19,22 +26,43 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 from flce_testing import LOSS_RTOL, device_inputs, rel_fro
 
 pytestmark = pytest.mark.gpu
 
+# (N, H, V, ignored fraction, seed)
+CASES = [
+    (1000, 256, 4099, 0.1, 21),        # one chunk, odd V
+    (3000, 512, 50257, 0.05, 22),      # one chunk, GPT-2-sized vocabulary
+    (9000, 512, 32000, 0.1, 23),       # three 4096-token chunks, the last 808 tokens
+    (1500, 64, 2_000_000, 0.1, 24),    # the scratch holds 1024-token chunks: two, the last 476
+]
 
-def test_loss_static_matches_forward_backward_on_two_calls():
+
+def _oracle_token_losses(w, block=32):
+    """Per-token losses from the oracle's definition, a few rows at a time
+    (the 2,000,000-entry vocabulary's logits do not fit host memory whole)."""
+    xr = workloads.F64Rows(w.x)
+    Wd = w.W_f64()
+    out = np.empty(w.N)
+    for s in range(0, w.N, block):
+        r = np.arange(s, min(w.N, s + block))
+        out[r] = oracle.token_loss_rows(xr, Wd, w.t, r, w.ignore_index)
+    n_valid = int(oracle.valid_mask(w.t, w.ignore_index).sum())
+    return out, float(out.sum()) / n_valid
+
+
+def test_loss_static_matches_the_oracle_and_forward_backward_on_calls_in_a_row():
     from linear_cross_entropy_token_gb300 import FLCE, flce
     h = FLCE("bf16", 0)
-    cases = [(1000, 256, 4099, 0.1, 21), (3000, 512, 50257, 0.05, 22)]
     try:
-        for i, (N, H, V, ign, seed) in enumerate(cases):
+        for i, (N, H, V, ign, seed) in enumerate(CASES):
             w = workloads.generate(workloads.custom(N, H, V, "bf16", ignore_frac=ign, seed=seed))
             x, W, t = device_inputs(w)
-            loss_ref, _, _ = h.forward_backward(x, W, t)
-            tl_ref = h.token_losses(N).double().cpu().numpy()
+            loss_fb, _, _ = h.forward_backward(x, W, t)
+            tl_fb = h.token_losses(N).double().cpu().numpy()
             out = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
             torch.cuda.synchronize()
             free0, _ = torch.cuda.mem_get_info()
@@ -45,9 +73,15 @@ def test_loss_static_matches_forward_backward_on_two_calls():
                 # the first call on a device may load the library's module that
                 # holds the static array; a later call takes nothing
                 assert free1 == free0
-            assert abs(loss - loss_ref) / abs(loss_ref) <= LOSS_RTOL, (loss, loss_ref)
-            assert rel_fro(tl.double().cpu().numpy(), tl_ref) <= LOSS_RTOL
-            assert np.isfinite(tl.cpu().numpy()).all()
+            got = tl.double().cpu().numpy()
+            assert np.isfinite(got).all()
+            ref_tl, ref_loss = _oracle_token_losses(w)
+            assert abs(loss - ref_loss) / ref_loss <= LOSS_RTOL, (N, V, loss, ref_loss)
+            assert rel_fro(got, ref_tl) <= LOSS_RTOL, (N, V)
+            assert not got[w.t == -100].any()
+            assert abs(loss - loss_fb) / abs(loss_fb) <= LOSS_RTOL, (loss, loss_fb)
+            assert rel_fro(got, tl_fb) <= LOSS_RTOL
+            del x, W, t, out
     finally:
         h.close()
 
