@@ -109,7 +109,7 @@ Layout make_layout(int64_t N, int64_t H, int64_t C, int64_t ldv, int64_t vt, int
   L.lse = take(static_cast<uint64_t>(C) * 4);
   L.dcorr = take(static_cast<uint64_t>(C) * 4);
   L.token_loss = take(static_cast<uint64_t>(std::max<int64_t>(N, 1)) * 4);
-  L.dxpart = take(static_cast<uint64_t>(splits) * C * H * 4);  // bf16 path: fp32 dx partials
+  L.dxpart = take(static_cast<uint64_t>(splits) * C * H * 4);  // fp32 partials of the dx GEMM's splits
   L.total = off;
   return L;
 }
@@ -232,8 +232,18 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   const int slots = num_sms / group;
   const int tile_m = group * kBM, tile_n = tile_cols(cfg);
   // SLABS accumulate dx over the slabs in one fp32 buffer (one split)
-  auto splits_for = [&](int64_t C) {
-    return bf16 ? (slabs ? 1 : pick_dx_splits(C, H, V, slots, tile_m, tile_n)) : 0;
+  // fp32: the CUDA-core dx GEMM splits its V reduction when its C x H output
+  // has too few tiles to fill the SMs (the count for the full V bounds that of
+  // any slab)
+  auto splits_for = [&](int64_t C) -> int64_t {
+    if (!bf16) {
+      // the partials take at most a quarter of the budget
+      const uint64_t per_split = static_cast<uint64_t>(std::max<int64_t>(C, 1)) * H * 4;
+      const int64_t cap = static_cast<int64_t>(budget / 4 / per_split);
+      const int64_t s = std::min<int64_t>(simt_split_k(std::max<int64_t>(C, 1), H, V, num_sms), cap);
+      return s > 1 ? s : 0;
+    }
+    return slabs ? 1 : pick_dx_splits(C, H, V, slots, tile_m, tile_n);
   };
   // SLABS: the widest slab (a multiple of 512 columns) whose C x slab buffer
   // fits both kSlabBytes and what the budget leaves beside the rest of the
@@ -776,8 +786,10 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
   if (st != FLCE_OK) return fail(h, st, "%s", why.c_str());
   st = ensure_workspace(h, p.workspace_bytes);
   if (st != FLCE_OK) return st;
-  const Layout L =
-      make_layout(N, H, p.chunk, p.ldv, p.vocab_tiles, bf16 ? p.dx_splits : 0, bf16 ? 2 : 4);
+  // the same split count the plan sized the workspace with (fp32 plans
+  // without a split hold no partials)
+  const int64_t part_splits = bf16 ? p.dx_splits : (p.dx_splits > 1 ? p.dx_splits : 0);
+  const Layout L = make_layout(N, H, p.chunk, p.ldv, p.vocab_tiles, part_splits, bf16 ? 2 : 4);
   uint8_t* ws = static_cast<uint8_t*>(h->ws);
   uint32_t* ctrl = reinterpret_cast<uint32_t*>(ws + L.ctrl);
   float2* partials = reinterpret_cast<float2*>(ws + L.partials);
@@ -825,6 +837,8 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     const float* Wf = static_cast<const float*>(W);
     float* dxf = static_cast<float*>(dx);
     float* logits = reinterpret_cast<float*>(ws + L.logits);
+    float* dxpart = reinterpret_cast<float*>(ws + L.dxpart);
+    const int dx_splits = static_cast<int>(p.dx_splits);
     const bool slabs = h->cfg.dlogits_mode == FLCE_DLOGITS_SLABS;
     for (int64_t c = 0; c < p.num_chunks; ++c) {
       char nvtx_name[40];
@@ -842,7 +856,8 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
           const double dvs = static_cast<double>(vs);
           const int vts = static_cast<int>(cdiv(vs, kVocabTile));
           FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dH * dvs, 4 * (dr * dH + dvs * dH + dr * dvs),
-                      launch_simt_gemm_f32(xf + off * H, H, 1, Wf + v0 * H, 1, H, logits, ldv, rows, vs, H, 0, s));
+                      launch_simt_gemm_f32(xf + off * H, H, 1, Wf + v0 * H, 1, H, logits, ldv, rows, vs, H, 0,
+                                           1, nullptr, s));
           FLCE_LAUNCH(FLCE_K_SIMT_TILE_STATS, 0.0, 4 * dr * dvs + 12 * dr * vts,
                       launch_simt_tile_stats(logits, ldv, rows, vs, vts, vt, v0, t + off, ignore_index,
                                              partials + v0 / kVocabTile, zt, s));
@@ -853,20 +868,21 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
           const int64_t v0 = sl * Vs, vs = std::min(Vs, V - v0);
           const double dvs = static_cast<double>(vs);
           FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dH * dvs, 4 * (dr * dH + dvs * dH + dr * dvs),
-                      launch_simt_gemm_f32(xf + off * H, H, 1, Wf + v0 * H, 1, H, logits, ldv, rows, vs, H, 0, s));
+                      launch_simt_gemm_f32(xf + off * H, H, 1, Wf + v0 * H, 1, H, logits, ldv, rows, vs, H, 0,
+                                           1, nullptr, s));
           FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 8 * dr * dvs,
                       launch_dlogits_f32(logits, ldv, rows, vs, v0, lse, t + off, ignore_index, ctrl, s));
           FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dvs * dH, 4 * (dr * dvs + dvs * dH + (sl > 0 ? 2 : 1) * dr * dH),
                       launch_simt_gemm_f32(logits, ldv, 1, Wf + v0 * H, H, 1, dxf + off * H, H, rows, H, vs,
-                                           sl > 0 ? 1 : 0, s));
+                                           sl > 0 ? 1 : 0, dx_splits, dxpart, s));
           FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dvs * dH, 4 * (dr * dvs + dr * dH + (c > 0 ? 2 : 1) * dvs * dH),
                       launch_simt_gemm_f32(logits, 1, ldv, xf + off * H, H, 1, dW + v0 * H, H, vs, H, rows,
-                                           c > 0 ? 1 : 0, s));
+                                           c > 0 ? 1 : 0, 1, nullptr, s));
         }
         continue;
       }
       FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dH * dV, 4 * (dr * dH + dV * dH + dr * dV),
-                  launch_simt_gemm_f32(xf + off * H, H, 1, Wf, 1, H, logits, ldv, rows, V, H, 0, s));
+                  launch_simt_gemm_f32(xf + off * H, H, 1, Wf, 1, H, logits, ldv, rows, V, H, 0, 1, nullptr, s));
       FLCE_LAUNCH(FLCE_K_SIMT_TILE_STATS, 0.0, 4 * dr * dV + 12 * dr * vt,
                   launch_simt_tile_stats(logits, ldv, rows, V, vt, vt, 0, t + off, ignore_index, partials,
                                          zt, s));
@@ -875,9 +891,11 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 8 * dr * dV,
                   launch_dlogits_f32(logits, ldv, rows, V, 0, lse, t + off, ignore_index, ctrl, s));
       FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dV * dH, 4 * (dr * dV + dV * dH + dr * dH),
-                  launch_simt_gemm_f32(logits, ldv, 1, Wf, H, 1, dxf + off * H, H, rows, H, V, 0, s));
+                  launch_simt_gemm_f32(logits, ldv, 1, Wf, H, 1, dxf + off * H, H, rows, H, V, 0, dx_splits,
+                                       dxpart, s));
       FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dV * dH, 4 * (dr * dV + dr * dH + 2 * dV * dH),
-                  launch_simt_gemm_f32(logits, 1, ldv, xf + off * H, H, 1, dW, H, V, H, rows, c > 0 ? 1 : 0, s));
+                  launch_simt_gemm_f32(logits, 1, ldv, xf + off * H, H, 1, dW, H, V, H, rows, c > 0 ? 1 : 0, 1,
+                                       nullptr, s));
     }
   } else {
     // ------------------------------------------------- bf16 tcgen05 path

@@ -127,9 +127,15 @@ cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* c
                                  cudaStream_t s);
 
 // flce_simt.cu (fp32 path)
+// C (+)= A·B over K with strided operands. splits > 1 with part != null
+// splits the reduction over that many blocks along K, writing partials to part
+// (splits x M x N fp32), and a second launch adds them in split order.
+constexpr int kMaxSimtSplits = 64;
+int simt_split_k(int64_t M, int64_t N, int64_t K, int num_sms);
 cudaError_t launch_simt_gemm_f32(const float* A, int64_t sam, int64_t sak, const float* B,
                                  int64_t sbk, int64_t sbn, float* C, int64_t ldc, int64_t M,
-                                 int64_t N, int64_t K, int accumulate, cudaStream_t s);
+                                 int64_t N, int64_t K, int accumulate, int splits, float* part,
+                                 cudaStream_t s);
 // vocab_tiles tiles of the buffer's V columns; the buffer's column 0 is
 // vocabulary column col_base, and partials rows are part_stride apart
 cudaError_t launch_simt_tile_stats(const float* logits, int64_t ldv, int rows, int64_t V,

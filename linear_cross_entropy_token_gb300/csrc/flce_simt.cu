@@ -2,49 +2,89 @@
 //
 // TF32 tensor cores cannot hold fp32 inputs to a 1e-5 gradient error, so
 // fp32 x and W take these kernels: a strided fp32 GEMM (used for x_c·Wᵀ,
-// dlogits·W and dlogitsᵀ·x_c) and the per-vocab-tile max / sum-exp of the
-// stored fp32 logits. The rest of the fp32 path shares the row kernels of the
-// bf16 path, and its chunk schedule is the same (the four steps of the FLCE
-// page, "Fused Linear Cross-Entropy: LLM 학습 logits 메모리 병목 없애기",
-// section "FLCE의 핵심 아이디어").
+// dlogits·W and dlogitsᵀ·x_c) with a fixed-order split of the reduction, and
+// the per-vocab-tile max / sum-exp of the stored fp32 logits. The rest of the
+// fp32 path shares the row kernels of the bf16 path, and its chunk schedule is
+// the same (the four steps of the FLCE page, "Fused Linear Cross-Entropy: LLM
+// 학습 logits 메모리 병목 없애기", section "FLCE의 핵심 아이디어").
+#include <algorithm>
+
 #include "flce_internal.h"
 
 namespace flce {
 namespace {
 
 constexpr int kTM = 64, kTN = 64, kTK = 16;
+constexpr int kSimtThreads = 256;
+constexpr int kLoads = kTK * kTM / kSimtThreads;  // operand elements per thread per k-tile (4)
+static_assert(kTM == kTN, "the load mapping below assumes square tiles");
+
+// Element e (0..1023) of a 64 x 16 operand tile, mapped so that consecutive
+// threads walk the operand's unit-stride dimension: `outer` indexes the 64
+// rows (m of A, n of B), `kk` the 16-deep k slice.
+__device__ __forceinline__ void tile_coords(int e, bool k_unit, int& outer, int& kk) {
+  if (k_unit) {
+    kk = e % kTK;
+    outer = e / kTK;
+  } else {
+    outer = e % kTM;
+    kk = e / kTM;
+  }
+}
 
 // C[m, n] (+)= sum_k A(m, k) B(k, n), A(m, k) = A[m*sam + k*sak],
-// B(k, n) = B[k*sbk + n*sbn]; 256 threads, 4 x 4 outputs each.
-__global__ void __launch_bounds__(256) simt_gemm_f32_kernel(
+// B(k, n) = B[k*sbk + n*sbn], over the k range of split blockIdx.z
+// ([z*kps, min(K, (z+1)*kps))). With part == nullptr the block writes C
+// (adding to it if accumulate); otherwise it writes its split's partial sums
+// to part[z][m][n] (M x N, row-major) for simt_splitk_reduce_kernel.
+// 256 threads, a 4 x 4 output block each; the next k-tile's operands are
+// loaded into registers while the current one is multiplied.
+__global__ void __launch_bounds__(kSimtThreads) simt_gemm_f32_kernel(
     const float* __restrict__ A, int64_t sam, int64_t sak, const float* __restrict__ B,
     int64_t sbk, int64_t sbn, float* __restrict__ C, int64_t ldc, int64_t M, int64_t N,
-    int64_t K, int accumulate) {
+    int64_t K, int64_t kps, int accumulate, float* __restrict__ part) {
   __shared__ float As[kTK][kTM + 1];
   __shared__ float Bs[kTK][kTN + 1];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTM;
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTN;
-  float acc[4][4] = {};
-  for (int64_t k0 = 0; k0 < K; k0 += kTK) {
-    for (int i = threadIdx.x; i < kTK * kTM; i += 256) {
-      const int kk = i / kTM, mm = i % kTM;
-      const int64_t m = m0 + mm, k = k0 + kk;
-      As[kk][mm] = (m < M && k < K) ? A[m * sam + k * sak] : 0.f;
+  const int64_t kbeg = static_cast<int64_t>(blockIdx.z) * kps;
+  const int64_t kend = min(K, kbeg + kps);
+  const bool a_k_unit = sak == 1;
+  const bool b_k_unit = sbk == 1 && sbn != 1;
+  float ra[kLoads], rb[kLoads];
+  auto fetch = [&](int64_t k0) {
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+      int o, kk;
+      tile_coords(threadIdx.x + q * kSimtThreads, a_k_unit, o, kk);
+      const int64_t m = m0 + o, k = k0 + kk;
+      ra[q] = (m < M && k < kend) ? A[m * sam + k * sak] : 0.f;
+      tile_coords(threadIdx.x + q * kSimtThreads, b_k_unit, o, kk);
+      const int64_t n = n0 + o;
+      rb[q] = (n < N && k0 + kk < kend) ? B[(k0 + kk) * sbk + n * sbn] : 0.f;
     }
-    for (int i = threadIdx.x; i < kTK * kTN; i += 256) {
-      const int kk = i / kTN, nn = i % kTN;
-      const int64_t n = n0 + nn, k = k0 + kk;
-      Bs[kk][nn] = (n < N && k < K) ? B[k * sbk + n * sbn] : 0.f;
+  };
+  float acc[4][4] = {};
+  if (kbeg < kend) fetch(kbeg);
+  for (int64_t k0 = kbeg; k0 < kend; k0 += kTK) {
+#pragma unroll
+    for (int q = 0; q < kLoads; ++q) {
+      int o, kk;
+      tile_coords(threadIdx.x + q * kSimtThreads, a_k_unit, o, kk);
+      As[kk][o] = ra[q];
+      tile_coords(threadIdx.x + q * kSimtThreads, b_k_unit, o, kk);
+      Bs[kk][o] = rb[q];
     }
     __syncthreads();
+    if (k0 + kTK < kend) fetch(k0 + kTK);
 #pragma unroll
     for (int kk = 0; kk < kTK; ++kk) {
       float a[4], b[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -52,58 +92,108 @@ __global__ void __launch_bounds__(256) simt_gemm_f32_kernel(
     }
     __syncthreads();
   }
+  // thread (tx, ty) holds rows ty*4 + i and columns tx + 16*j: a warp's stores
+  // of one (i, j) cover 16 consecutive columns of two rows
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t m = m0 + ty * 4 + i;
     if (m >= M) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int64_t n = n0 + tx * 4 + j;
+      const int64_t n = n0 + tx + 16 * j;
       if (n >= N) continue;
-      float* c = C + m * ldc + n;
-      *c = accumulate ? (*c + acc[i][j]) : acc[i][j];
+      if (part) {
+        part[(static_cast<int64_t>(blockIdx.z) * M + m) * N + n] = acc[i][j];
+      } else {
+        float* c = C + m * ldc + n;
+        *c = accumulate ? (*c + acc[i][j]) : acc[i][j];
+      }
     }
   }
 }
 
-// One block per (token row, vocab tile of 256): m = max z, l = sum exp(z - m),
-// and z_t when the target falls in the tile. The buffer's column 0 is
-// vocabulary column col_base; partials rows are part_stride apart.
+// C[m, n] (+)= sum over the splits, in split order, of part[s][m][n].
+__global__ void __launch_bounds__(256) simt_splitk_reduce_kernel(
+    const float* __restrict__ part, int splits, int64_t M, int64_t N, float* __restrict__ C,
+    int64_t ldc, int accumulate) {
+  const int64_t MN = M * N;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < MN;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float v = part[e];
+    for (int s = 1; s < splits; ++s) v += part[s * MN + e];
+    const int64_t m = e / N, n = e - m * N;
+    float* c = C + m * ldc + n;
+    *c = accumulate ? (*c + v) : v;
+  }
+}
+
+// One warp per (token row, vocab tile of 256): m = max z, l = sum exp(z - m),
+// and z_t when the target falls in the tile; each lane takes 8 columns. The
+// buffer's column 0 is vocabulary column col_base; partials rows are
+// part_stride apart.
 __global__ void __launch_bounds__(256) simt_tile_stats_kernel(
-    const float* __restrict__ logits, int64_t ldv, int64_t V, int part_stride, int64_t col_base,
-    const int64_t* __restrict__ t, int64_t ignore_index, float2* __restrict__ partials,
-    float* __restrict__ zt) {
-  __shared__ float red[256];
-  const int r = blockIdx.y, vt = blockIdx.x;
-  const int64_t j = static_cast<int64_t>(vt) * kVocabTile + threadIdx.x;
-  const bool in = j < V;
-  const float z = in ? logits[static_cast<size_t>(r) * ldv + j] : -INFINITY;
-  red[threadIdx.x] = z;
-  __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + w]);
-    __syncthreads();
-  }
-  const float m = red[0];
-  __syncthreads();
-  red[threadIdx.x] = in ? expf(z - m) : 0.f;
-  __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) partials[static_cast<size_t>(r) * part_stride + vt] = make_float2(m, red[0]);
+    const float* __restrict__ logits, int64_t ldv, int rows, int64_t V, int vocab_tiles,
+    int part_stride, int64_t col_base, const int64_t* __restrict__ t, int64_t ignore_index,
+    float2* __restrict__ partials, float* __restrict__ zt) {
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= rows * vocab_tiles) return;
+  const int r = w / vocab_tiles, vt = w - r * vocab_tiles;
+  const float* row = logits + static_cast<size_t>(r) * ldv;
   const int64_t tg = t[r];
-  if (in && tg != ignore_index && tg - col_base == j) zt[r] = z;
+  float z[8];
+  float m = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int64_t j = static_cast<int64_t>(vt) * kVocabTile + q * 32 + lane;
+    z[q] = j < V ? row[j] : -INFINITY;
+    m = fmaxf(m, z[q]);
+    if (j < V && tg != ignore_index && tg - col_base == j) zt[r] = z[q];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float l = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) l += z[q] == -INFINITY ? 0.f : expf(z[q] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  if (lane == 0) partials[static_cast<size_t>(r) * part_stride + vt] = make_float2(m, l);
 }
 
 }  // namespace
 
+int simt_split_k(int64_t M, int64_t N, int64_t K, int num_sms) {
+  // enough blocks for about two per SM, each split at least 128 deep
+  const int64_t tiles = ((M + kTM - 1) / kTM) * ((N + kTN - 1) / kTN);
+  int64_t s = (2 * static_cast<int64_t>(num_sms) + tiles - 1) / tiles;
+  s = std::min<int64_t>(s, std::max<int64_t>(1, K / 128));
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, kMaxSimtSplits)));
+}
+
 cudaError_t launch_simt_gemm_f32(const float* A, int64_t sam, int64_t sak, const float* B,
                                  int64_t sbk, int64_t sbn, float* C, int64_t ldc, int64_t M,
-                                 int64_t N, int64_t K, int accumulate, cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>((N + kTN - 1) / kTN), static_cast<unsigned>((M + kTM - 1) / kTM));
-  simt_gemm_f32_kernel<<<grid, 256, 0, s>>>(A, sam, sak, B, sbk, sbn, C, ldc, M, N, K, accumulate);
+                                 int64_t N, int64_t K, int accumulate, int splits, float* part,
+                                 cudaStream_t s) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  // k per split, a multiple of the k-tile; the last split may be shorter
+  int64_t kps = (K + splits - 1) / std::max(1, splits);
+  kps = std::max<int64_t>(kTK, (kps + kTK - 1) / kTK * kTK);
+  const int S = static_cast<int>(std::max<int64_t>(1, (K + kps - 1) / kps));
+  dim3 grid(static_cast<unsigned>((N + kTN - 1) / kTN), static_cast<unsigned>((M + kTM - 1) / kTM),
+            static_cast<unsigned>(S));
+  if (S == 1 || !part) {
+    grid.z = 1;
+    simt_gemm_f32_kernel<<<grid, kSimtThreads, 0, s>>>(A, sam, sak, B, sbk, sbn, C, ldc, M, N, K,
+                                                       std::max<int64_t>(K, 1), accumulate, nullptr);
+    return cudaGetLastError();
+  }
+  simt_gemm_f32_kernel<<<grid, kSimtThreads, 0, s>>>(A, sam, sak, B, sbk, sbn, C, ldc, M, N, K, kps,
+                                                     accumulate, part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t MN = M * N;
+  const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((MN + 255) / 256, 4096));
+  simt_splitk_reduce_kernel<<<blocks, 256, 0, s>>>(part, S, M, N, C, ldc, accumulate);
   return cudaGetLastError();
 }
 
@@ -111,9 +201,11 @@ cudaError_t launch_simt_tile_stats(const float* logits, int64_t ldv, int rows, i
                                    int vocab_tiles, int part_stride, int64_t col_base,
                                    const int64_t* t_chunk, int64_t ignore_index, float2* partials,
                                    float* zt, cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>(vocab_tiles), static_cast<unsigned>(rows));
-  simt_tile_stats_kernel<<<grid, 256, 0, s>>>(logits, ldv, V, part_stride, col_base, t_chunk,
-                                              ignore_index, partials, zt);
+  const int64_t warps = static_cast<int64_t>(rows) * vocab_tiles;
+  if (warps == 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>((warps + 7) / 8);
+  simt_tile_stats_kernel<<<blocks, 256, 0, s>>>(logits, ldv, rows, V, vocab_tiles, part_stride,
+                                                col_base, t_chunk, ignore_index, partials, zt);
   return cudaGetLastError();
 }
 
