@@ -237,9 +237,9 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   // any slab)
   auto splits_for = [&](int64_t C) -> int64_t {
     if (!bf16) {
-      // the partials take at most a quarter of the budget
+      // the partials take at most an eighth of the budget
       const uint64_t per_split = static_cast<uint64_t>(std::max<int64_t>(C, 1)) * H * 4;
-      const int64_t cap = static_cast<int64_t>(budget / 4 / per_split);
+      const int64_t cap = static_cast<int64_t>(budget / 8 / per_split);
       const int64_t s = std::min<int64_t>(simt_split_k(std::max<int64_t>(C, 1), H, V, num_sms), cap);
       return s > 1 ? s : 0;
     }

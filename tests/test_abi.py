@@ -89,8 +89,13 @@ def test_plan_long_context_stays_O_CV():
 
 def test_plan_explicit_chunk_and_budget():
     p = flce.plan(256, 128, 4096, "fp32", chunk=64)
-    assert (p["chunk"], p["num_chunks"], p["dx_splits"]) == (64, 4, 1)
+    # the fp32 dx GEMM (64 x 128 output, two 64 x 64 tiles) splits its 4096-deep
+    # reduction 32 ways to fill the SMs; its partials sit in the workspace
+    assert (p["chunk"], p["num_chunks"], p["dx_splits"]) == (64, 4, 32)
     assert p["logits_bytes"] == 64 * 4096 * 4
+    assert p["workspace_bytes"] >= p["logits_bytes"] + 32 * 64 * 128 * 4
+    # a large output needs no split
+    assert flce.plan(4096, 4096, 32000, "fp32")["dx_splits"] == 1
     p = flce.plan(16384, 4096, 151936, "bf16", chunk=8192, hbm_budget_bytes=4 * GiB)
     assert p["chunk"] == 8192 and p["num_chunks"] == 2
     with pytest.raises(flce.FlceError) as e:
