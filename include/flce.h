@@ -143,11 +143,17 @@ typedef struct flce_plan {
     uint64_t logits_bytes;       /* of which the C x ldv logits / dlogits buffer       */
     int64_t tile_m;              /* rows of a GEMM output tile: 128 (one CTA) or 256 (CTA
                                     pair, normal or wide)                               */
-    int64_t tile_n;              /* columns of a GEMM output tile: 256, or 512 (wide)   */
+    int64_t tile_n;              /* columns of the logits GEMM's output tile: 256, or 512
+                                    (wide). A FLCE_CTA_AUTO bf16 handle picks wide
+                                    (512) or pair (256) tiles per GEMM, in-place and
+                                    recompute modes, by a time model of the two:
+                                    pair tiles where the reduction per tile is short */
     int64_t vocab_slab;          /* SLABS: vocabulary columns per backward slab (the
                                     buffer is chunk x vocab_slab); other modes: V       */
     int64_t dlogits_mode;        /* the FLCE_DLOGITS_* mode the call runs (AUTO and,
                                     on fp32 handles, RECOMPUTE resolved to INPLACE)     */
+    int64_t tile_n_dx;           /* columns of the dx GEMM's output tile (256 or 512)  */
+    int64_t tile_n_dw;           /* columns of the dW GEMM's output tile (256 or 512)  */
 } flce_plan;
 
 /* Kernel kinds, for the per-kernel timing of flce_profile_read(). */
@@ -373,8 +379,9 @@ const char* flce_last_error(flce_handle_t h);
  * handle: it calls no cudaMalloc, cudaFree or allocating library routine. Its
  * scratch is one file-scope device array of 64 MiB, which every GPU that loads
  * the library holds until the process exits. That bounds V: one 128-token
- * chunk needs 128 x ceil(V/256) x 8 bytes of it, so V up to about 16.7 million.
- * Larger V returns INVALID_ARG.
+ * chunk needs 128 x ceil(V/64) x 8 bytes of it (a max and a sum of exp per
+ * 64 vocabulary columns), so V up to about 4.19 million. Larger V returns
+ * INVALID_ARG.
  *   x, W, t      device inputs as for flce_forward_backward (current device)
  *   loss         host, receives the fp32 mean loss
  *   token_loss   device, N fp32 outputs (0 for ignored tokens)

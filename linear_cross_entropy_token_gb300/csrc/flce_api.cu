@@ -104,12 +104,21 @@ Layout make_layout(int64_t N, int64_t H, int64_t C, int64_t ldv, int64_t vt, int
   };
   L.ctrl = take(kCtrlWords * 4);
   L.logits = take(static_cast<uint64_t>(C) * ldv * esize);
-  L.partials = take(static_cast<uint64_t>(C) * vt * 8);
+  // One region serves two buffers that are never live together: the
+  // log-sum-exp partials of the chunk (written by the logits GEMM or the
+  // statistics pass, last read by the dlogits pass) and the fp32 partials of
+  // the dx GEMM's splits (written by the dx GEMM, read by the dx reduction).
+  // On the call's stream every mode finishes with the first before it starts
+  // on the second, and the next chunk's logits GEMM comes after the dx
+  // reduction.
+  const uint64_t part_bytes = static_cast<uint64_t>(C) * vt * 8;
+  const uint64_t dxpart_bytes = static_cast<uint64_t>(splits) * C * H * 4;
+  L.partials = take(std::max(part_bytes, dxpart_bytes));
+  L.dxpart = L.partials;
   L.zt = take(static_cast<uint64_t>(C) * 4);
   L.lse = take(static_cast<uint64_t>(C) * 4);
   L.dcorr = take(static_cast<uint64_t>(C) * 4);
   L.token_loss = take(static_cast<uint64_t>(std::max<int64_t>(N, 1)) * 4);
-  L.dxpart = take(static_cast<uint64_t>(splits) * C * H * 4);  // fp32 partials of the dx GEMM's splits
   L.total = off;
   return L;
 }
@@ -127,6 +136,42 @@ int cta_group_size(const flce_config* cfg) {
 bool valid_cta_mode(int mode) {
   return mode == FLCE_CTA_AUTO || mode == FLCE_CTA_SINGLE || mode == FLCE_CTA_PAIR ||
          mode == FLCE_CTA_WIDE;
+}
+
+// Tile shapes of one GEMM launch
+enum Shape : int { kShapeSingle = 0, kShapePair = 1, kShapeWide = 2 };
+
+// A time model of one GEMM on CTA pairs, in SM cycles, for choosing between
+// wide (256 x 512, single-buffered accumulator) and pair (256 x 256, double-
+// buffered) tiles per launch. Fitted to launches timed on GB300 at the
+// 16384 x 4096 x 128256 and 2048 x 1024 x 32000 shapes: a 64-deep k-block of
+// a wide tile takes ~1110 cycles and of a pair tile ~610 (the wide tile does
+// twice the MMA work per k-block with less shared-memory traffic per FLOP);
+// a wide tile's epilogue holds the accumulator ~7100 cycles (log-sum-exp) or
+// ~5700 (fp32 stores) before the next tile's MMAs may start, while a pair
+// tile's epilogue (~3500 / ~2900 cycles) overlaps its successor's main loop
+// and only shows when that is shorter; each tile also pays ~1500 cycles of
+// pipeline fill. Work units run in waves of `slots` pairs.
+double gemm_cycles(int shape, int64_t M, int64_t N, int64_t K, bool lse, int64_t S, int slots) {
+  const int64_t kb = cdiv(cdiv(K, kBK), S);
+  const int64_t units = cdiv(M, 2 * kBM) * cdiv(N, shape == kShapeWide ? 2 * kBN : kBN) * S;
+  const double waves = static_cast<double>(cdiv(units, std::max(slots, 1)));
+  const double fill = 1500.0;
+  if (shape == kShapeWide) return waves * (1110.0 * kb + (lse ? 7100.0 : 5700.0) + fill);
+  return waves * (std::max(610.0 * kb, lse ? 3500.0 : 2900.0) + fill);
+}
+
+// Pair tiles replace the wide ones only where the model times them more
+// than this much faster: its error against measured launches is about 5%
+// (at 4096 x 32768 x 4096 it put pair 2% ahead; wide measured 6% faster).
+constexpr double kPairMargin = 0.95;
+
+// The tile shape (wide or pair) for one GEMM.
+int pick_shape(int64_t M, int64_t N, int64_t K, bool lse, int slots) {
+  return gemm_cycles(kShapePair, M, N, K, lse, 1, slots) <
+                 kPairMargin * gemm_cycles(kShapeWide, M, N, K, lse, 1, slots)
+             ? kShapePair
+             : kShapeWide;
 }
 
 // Output-tile columns of the handle's GEMMs: 512 for wide CTA-pair tiles
@@ -231,6 +276,33 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   const int group = cta_group_size(cfg);
   const int slots = num_sms / group;
   const int tile_m = group * kBM, tile_n = tile_cols(cfg);
+  // an AUTO bf16 handle picks wide or pair tiles per GEMM (the slab walk
+  // keeps the wide tiles its slab sizing assumes)
+  const bool mixed = bf16 && !slabs && cfg->cta_pair == FLCE_CTA_AUTO;
+  // dx on a mixed plan: the tile shape and split of the V reduction with the
+  // lowest modelled GEMM time plus the split partials' HBM round trip (about
+  // 3.6 KB per cycle)
+  struct DxChoice {
+    int shape;
+    int64_t splits;
+  };
+  auto dx_choice = [&](int64_t C) -> DxChoice {
+    const int64_t kb = cdiv(V, kBK);
+    DxChoice best[2] = {{kShapeWide, 1}, {kShapePair, 1}};
+    double best_t[2] = {-1, -1};
+    for (int i = 0; i < 2; ++i) {
+      for (int64_t sp = 1; sp <= 8; ++sp) {
+        if (sp > 1 && kb / sp < 16) break;
+        const double t = gemm_cycles(best[i].shape, C, H, V, false, sp, slots) +
+                         (4.0 * sp * C * H + 6.0 * C * H) / 3600.0;
+        if (best_t[i] < 0 || t < best_t[i] * 0.999) {  // more splits only for a gain
+          best_t[i] = t;
+          best[i].splits = sp;
+        }
+      }
+    }
+    return best_t[1] < kPairMargin * best_t[0] ? best[1] : best[0];
+  };
   // SLABS accumulate dx over the slabs in one fp32 buffer (one split)
   // fp32: the CUDA-core dx GEMM splits its V reduction when its C x H output
   // has too few tiles to fill the SMs (the count for the full V bounds that of
@@ -243,6 +315,7 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
       const int64_t s = std::min<int64_t>(simt_split_k(std::max<int64_t>(C, 1), H, V, num_sms), cap);
       return s > 1 ? s : 0;
     }
+    if (mixed) return dx_choice(std::max<int64_t>(C, 1)).splits;
     return slabs ? 1 : pick_dx_splits(C, H, V, slots, tile_m, tile_n);
   };
   // SLABS: the widest slab (a multiple of 512 columns) whose C x slab buffer
@@ -338,6 +411,14 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   out->logits_bytes = static_cast<uint64_t>(C) * out->ldv * esize;
   out->tile_m = tile_m;
   out->tile_n = tile_n;
+  out->tile_n_dx = tile_n;
+  out->tile_n_dw = tile_n;
+  if (mixed && C > 0) {
+    auto cols = [](int sh) -> int64_t { return sh == kShapeWide ? 2 * kBN : kBN; };
+    out->tile_n = cols(pick_shape(C, V, H, true, slots));
+    out->tile_n_dx = cols(dx_choice(C).shape);
+    out->tile_n_dw = cols(pick_shape(V, H, C, false, slots));
+  }
   // fp32 handles run SLABS as asked and every other mode in place
   out->dlogits_mode = slabs ? FLCE_DLOGITS_SLABS
                       : (bf16 && cfg->dlogits_mode == FLCE_DLOGITS_RECOMPUTE) ? FLCE_DLOGITS_RECOMPUTE
@@ -354,9 +435,10 @@ struct flce_handle_s {
   int device = 0;
   int num_sms = 0;
   int pair_clusters = 0;  // clusters of two the pair kernels fit at once
-  bool use_pair = false;  // GEMMs on CTA pairs (256 x 256 tiles)
   int wide_clusters = 0;  // clusters of two the wide kernels fit at once
-  bool use_wide = false;  // GEMMs on CTA pairs with 256 x 512 tiles
+  // tile shape of the handle's GEMMs; an AUTO handle (cfg.cta_pair stays
+  // FLCE_CTA_AUTO) runs each GEMM on the shape its plan names, wide or pair
+  int shape = kShapeSingle;
   uint64_t timeout_ns = 0;
   std::string err;
   // workspace
@@ -393,7 +475,7 @@ struct flce_handle_s {
   bool has_plan = false;
   int64_t launches = 0;
   Profiler prof;
-  std::map<std::array<int, 4>, int> group_cache;  // pick_group_m by (num_m, num_n, num_s, slots)
+  std::map<std::array<int, 5>, int> group_cache;  // pick_group_m by (shape, num_m, num_n, num_s, slots)
 };
 
 namespace {
@@ -586,27 +668,37 @@ flce_status read_back(flce_handle_t h, uint32_t* ctrl_dev, cudaStream_t s, float
 
 // One GEMM on the handle's tile shape; sets num_m from the M extent and the
 // grid from the work units (persistent CTAs, or CTA pairs).
-int group_for(flce_handle_t h, int num_m, int num_n, int num_s, int slots) {
-  const std::array<int, 4> key{num_m, num_n, num_s, slots};
+int group_for(flce_handle_t h, int shape, int num_m, int num_n, int num_s, int slots) {
+  const std::array<int, 5> key{shape, num_m, num_n, num_s, slots};
   auto it = h->group_cache.find(key);
   if (it != h->group_cache.end()) return it->second;
-  const int tile_m = (h->use_pair || h->use_wide) ? 2 * kBM : kBM;
-  const int g = pick_group_m(num_m, num_n, num_s, slots, tile_m, h->use_wide ? 2 * kBN : kBN);
+  const int tile_m = shape == kShapeSingle ? kBM : 2 * kBM;
+  const int g = pick_group_m(num_m, num_n, num_s, slots, tile_m, shape == kShapeWide ? 2 * kBN : kBN);
   h->group_cache.emplace(key, g);
   return g;
 }
 
-cudaError_t launch_gemm(flce_handle_t h, int kind, const CUtensorMap& a, const CUtensorMap& b,
+// The shape a GEMM with tile_n output columns (from its plan) runs on.
+int shape_for(flce_handle_t h, int64_t tile_n) {
+  if (h->cfg.cta_pair != FLCE_CTA_AUTO || h->shape == kShapeSingle) return h->shape;
+  return tile_n == 2 * kBN ? kShapeWide : kShapePair;
+}
+
+// One GEMM on tile shape `shape`; sets num_m (and, for wide tiles, num_n)
+// from the extents and the grid from the work units (persistent CTAs, or CTA
+// pairs). args.num_n counts 256-column tiles on entry.
+cudaError_t launch_gemm(flce_handle_t h, int shape, int kind, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& o, UmmaArgs args, int64_t M, cudaStream_t s) {
-  const int rows_per_unit = (h->use_pair || h->use_wide) ? 2 * kBM : kBM;
-  const int slots_max = h->use_wide ? h->wide_clusters : h->use_pair ? h->pair_clusters : h->num_sms;
+  const int rows_per_unit = shape == kShapeSingle ? kBM : 2 * kBM;
+  const int slots_max = shape == kShapeWide ? h->wide_clusters
+                        : shape == kShapePair ? h->pair_clusters : h->num_sms;
   args.num_m = static_cast<int>(cdiv(M, rows_per_unit));
-  if (h->use_wide) args.num_n = static_cast<int>(cdiv(args.cols, 2 * kBN));
+  if (shape == kShapeWide) args.num_n = static_cast<int>(cdiv(args.cols, 2 * kBN));
   const int units = args.num_m * args.num_n * args.num_s;
   const int slots = std::min(units, slots_max);
-  if (args.raster == 2) args.group_m = group_for(h, args.num_m, args.num_n, args.num_s, slots);
-  if (h->use_wide) return launch_umma_wide(kind, a, b, o, args, slots, s);
-  if (h->use_pair) return launch_umma_pair(kind, a, b, o, args, slots, s);
+  if (args.raster == 2) args.group_m = group_for(h, shape, args.num_m, args.num_n, args.num_s, slots);
+  if (shape == kShapeWide) return launch_umma_wide(kind, a, b, o, args, slots, s);
+  if (shape == kShapePair) return launch_umma_pair(kind, a, b, o, args, slots, s);
   return launch_umma(kind, a, b, o, args, slots, s);
 }
 
@@ -716,7 +808,7 @@ flce_status slab_backward(flce_handle_t h, const SlabChunk& k, cudaStream_t s, b
       if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab wait: %s", cudaGetErrorString(e));
     }
     FLCE_LAUNCH(FLCE_K_GEMM_DLOGITS, 2 * dr * dH * dvs, 2 * dr * dH + 2 * dvs * dH + 2 * dr * dvs + 12 * dr,
-                launch_gemm(h, kUmmaDlogits, *k.mX_k, mWs_k, mZs_out, g, rows, s));
+                launch_gemm(h, h->shape, kUmmaDlogits, *k.mX_k, mWs_k, mZs_out, g, rows, s));
     e = cudaEventRecord(h->slab_ready, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side, h->slab_ready, 0);
     if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab fork: %s", cudaGetErrorString(e));
@@ -731,7 +823,7 @@ flce_status slab_backward(flce_handle_t h, const SlabChunk& k, cudaStream_t s, b
     b.cols = static_cast<int>(H);
     b.reduce_add = sl > 0 ? 1 : 0;
     FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dvs * dH, 2 * dr * dvs + 2 * dvs * dH + (sl > 0 ? 8.0 : 4.0) * dr * dH,
-                launch_gemm(h, kUmmaDxF32, mZs_k, mWs_mn, mDxs, b, rows, s));
+                launch_gemm(h, h->shape, kUmmaDxF32, mZs_k, mWs_mn, mDxs, b, rows, s));
     // dW_s (+)= d_sᵀ · x_c, beside it on the side stream
     UmmaArgs d = *k.logits_args;
     d.num_n = static_cast<int>(cdiv(H, kBN));
@@ -746,7 +838,7 @@ flce_status slab_backward(flce_handle_t h, const SlabChunk& k, cudaStream_t s, b
       const cudaStream_t s = side;  // the launch and its timing events go on the side stream
       FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dvs * dH,
                   2 * dr * dvs + 2 * dr * dH + (k.chunk_index > 0 ? 8.0 : 4.0) * dvs * dH,
-                  launch_gemm(h, kUmmaDw, mZs_mn, *k.mX_mn, mDws, d, vs, s));
+                  launch_gemm(h, h->shape, kUmmaDw, mZs_mn, *k.mX_mn, mDws, d, vs, s));
     }
     e = cudaEventRecord(h->slab_freed, side);
     if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab join: %s", cudaGetErrorString(e));
@@ -906,7 +998,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     const bool recompute = h->cfg.dlogits_mode == FLCE_DLOGITS_RECOMPUTE;
     const bool slabs = h->cfg.dlogits_mode == FLCE_DLOGITS_SLABS;
     const int64_t zw = slabs ? p.vocab_slab : V;  // columns of the chunk buffer
-    const int b_box = (h->use_pair || h->use_wide) ? 128 : 256;
+    const int b_box = h->shape == kShapeSingle ? 256 : 128;
     CUtensorMap mW_k, mW_mn, mX_k, mX_mn, mZ_out, mZ_k, mZ_mn, mDx, mDw;
     // a CTA of a pair loads 128 of the tile's 256 columns of a K-major B
     if (!map_bf16_2d(&mW_k, W, H, V, H * 2, 64, b_box, &why) ||
@@ -951,7 +1043,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       a.timeout_ns = h->timeout_ns;
       FLCE_LAUNCH(FLCE_K_GEMM_LOGITS, 2 * dr * dH * dV,
                   2 * dr * dH + 2 * dV * dH + ((recompute || slabs) ? 0 : 2 * dr * dV) + 8 * dr * vt + 12 * dr,
-                  launch_gemm(h, kUmmaLogits, mX_k, mW_k, mZ_out, a, rows, s));
+                  launch_gemm(h, shape_for(h, p.tile_n), kUmmaLogits, mX_k, mW_k, mZ_out, a, rows, s));
       // 2a. cross-tile log-sum-exp and token losses
       FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
                   launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
@@ -966,7 +1058,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       // 2b. dlogits = (softmax - onehot) / n_valid over the chunk buffer
       if (recompute) {
         FLCE_LAUNCH(FLCE_K_GEMM_DLOGITS, 2 * dr * dH * dV, 2 * dr * dH + 2 * dV * dH + 2 * dr * dV + 12 * dr,
-                    launch_gemm(h, kUmmaDlogits, mX_k, mW_k, mZ_out, a, rows, s));
+                    launch_gemm(h, shape_for(h, p.tile_n), kUmmaDlogits, mX_k, mW_k, mZ_out, a, rows, s));
       } else {
         FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 4 * dr * dV,
                     launch_dlogits_bf16(logits, ldv, rows, V, partials, vt, lse, t + off, ignore_index,
@@ -1002,7 +1094,8 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       d.reduce_add = c > 0 ? 1 : 0;
       const double dx_bytes = 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH;
       const double dw_bytes = 2 * dr * dV + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dV * dH;
-      if (h->use_pair && h->cfg.backward_launch == FLCE_BACKWARD_ONE_LAUNCH) {
+      if (h->shape == kShapePair && h->cfg.cta_pair == FLCE_CTA_PAIR &&
+          h->cfg.backward_launch == FLCE_BACKWARD_ONE_LAUNCH) {
         // both read the finished dlogits buffer: one launch, dx units first,
         // handed out from a counter in the control block
         DualMaps maps;
@@ -1018,7 +1111,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
         da.p[0].num_m = static_cast<int>(cdiv(rows, 2 * kBM));
         da.p[1].num_m = static_cast<int>(cdiv(V, 2 * kBM));
         da.units0 = da.p[0].num_m * da.p[0].num_n * da.p[0].num_s;
-        da.p[0].group_m = group_for(h, da.p[0].num_m, da.p[0].num_n, da.p[0].num_s,
+        da.p[0].group_m = group_for(h, kShapePair, da.p[0].num_m, da.p[0].num_n, da.p[0].num_s,
                                     std::min(da.units0, h->pair_clusters));
         da.pad = 0;
         da.sched_ctr = reinterpret_cast<int32_t*>(ctrl + kCtrlSched);
@@ -1029,9 +1122,9 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
                     launch_umma_pair_dual(maps, da, std::min(units, h->pair_clusters), s));
       } else {
         FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, dx_bytes,
-                    launch_gemm(h, kUmmaDxF32, mZ_k, mW_mn, mDx, b, rows, s));
+                    launch_gemm(h, shape_for(h, p.tile_n_dx), kUmmaDxF32, mZ_k, mW_mn, mDx, b, rows, s));
         FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dV * dH, dw_bytes,
-                    launch_gemm(h, kUmmaDw, mZ_mn, mX_mn, mDw, d, V, s));
+                    launch_gemm(h, shape_for(h, p.tile_n_dw), kUmmaDw, mZ_mn, mX_mn, mDw, d, V, s));
       }
       FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4.0 * S * dr * dH + 4 * dr * dH,
                   launch_dx_reduce(dxpart, S, C * H, rows, H, static_cast<const __nv_bfloat16*>(W), V,
@@ -1129,24 +1222,24 @@ flce_status flce_create(flce_handle_t* out, const flce_config* cfg) {
   h->timeout_ns = static_cast<uint64_t>(cfg->timeout_ms > 0 ? cfg->timeout_ms : 2000) * 1000000ull;
   DeviceGuard g(h->device);
   if (cfg->dtype == FLCE_DTYPE_BF16) {
-    const int group = cta_group_size(cfg);
-    if (group == 2 && tile_cols(cfg) == 2 * kBN) {
-      h->wide_clusters = umma_wide_max_clusters();
-      if (h->wide_clusters <= 0) {
-        delete h;
-        return FLCE_ERR_UNSUPPORTED;
-      }
-      h->use_wide = true;
-    } else if (group == 2) {
-      h->pair_clusters = umma_pair_max_clusters();
-      if (cfg->cta_pair == FLCE_CTA_PAIR && h->pair_clusters <= 0) {
-        delete h;
-        return FLCE_ERR_UNSUPPORTED;
-      }
-      h->use_pair = h->pair_clusters > 0;
+    const int mode = cfg->cta_pair;
+    if (mode == FLCE_CTA_AUTO || mode == FLCE_CTA_WIDE) h->wide_clusters = umma_wide_max_clusters();
+    if (mode == FLCE_CTA_AUTO || mode == FLCE_CTA_PAIR) h->pair_clusters = umma_pair_max_clusters();
+    if ((mode == FLCE_CTA_WIDE && h->wide_clusters <= 0) || (mode == FLCE_CTA_PAIR && h->pair_clusters <= 0)) {
+      delete h;
+      return FLCE_ERR_UNSUPPORTED;
     }
-    // the handle's plans follow the tile shape it actually runs
-    h->cfg.cta_pair = h->use_wide ? FLCE_CTA_WIDE : h->use_pair ? FLCE_CTA_PAIR : FLCE_CTA_SINGLE;
+    if (mode == FLCE_CTA_AUTO && h->wide_clusters > 0 && h->pair_clusters > 0) {
+      h->shape = kShapeWide;   // per GEMM, the plan's choice of wide or pair
+    } else {
+      h->shape = (mode == FLCE_CTA_AUTO || mode == FLCE_CTA_WIDE) && h->wide_clusters > 0 ? kShapeWide
+                 : (mode == FLCE_CTA_AUTO || mode == FLCE_CTA_PAIR) && h->pair_clusters > 0 ? kShapePair
+                                                                                          : kShapeSingle;
+      // the handle's plans follow the one tile shape it actually runs
+      h->cfg.cta_pair = h->shape == kShapeWide   ? FLCE_CTA_WIDE
+                        : h->shape == kShapePair ? FLCE_CTA_PAIR
+                                                 : FLCE_CTA_SINGLE;
+    }
   }
   if (cudaMallocHost(&h->host_ctrl, kCtrlWords * 4) != cudaSuccess) {
     cudaGetLastError();
@@ -1429,7 +1522,7 @@ flce_status flce_check_gemm(flce_handle_t h, int32_t a_mn_major, int32_t b_mn_ma
   bool ok = a_mn_major ? map_bf16_2d(&ma, A, M, K, M * 2, 64, 64, &why)
                        : map_bf16_2d(&ma, A, K, M, K * 2, 64, 128, &why);
   ok = ok && (b_mn_major ? map_bf16_2d(&mb, B, N, K, N * 2, 64, 64, &why)
-                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, (h->use_pair || h->use_wide) ? 128 : 256, &why));
+                         : map_bf16_2d(&mb, B, K, N, K * 2, 64, h->shape == kShapeSingle ? 256 : 128, &why));
   ok = ok && map_f32_3d(&mc, C, N, M, 1, N * 4, static_cast<uint64_t>(M) * N * 4, &why);
   if (!ok) return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
   UmmaArgs a{};
@@ -1448,7 +1541,7 @@ flce_status flce_check_gemm(flce_handle_t h, int32_t a_mn_major, int32_t b_mn_ma
   const double flops = 2.0 * M * N * K;
   const int kkind = a_mn_major ? FLCE_K_GEMM_DW : (b_mn_major ? FLCE_K_GEMM_DX : FLCE_K_GEMM_LOGITS);
   FLCE_LAUNCH(kkind, flops, 2.0 * (M * K + N * K) + 4.0 * M * N,
-              launch_gemm(h, kind, ma, mb, mc, a, M, s));
+              launch_gemm(h, h->shape, kind, ma, mb, mc, a, M, s));
   return read_back(h, ctrl, s, nullptr);
 }
 

@@ -24,7 +24,10 @@ enum CtrlWord : int {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kVocabTile = kBN;   // vocab columns per log-sum-exp partial
+// Vocabulary columns per log-sum-exp partial (running max, sum of exp): one
+// 64-column group of an output tile. The bf16 chunk buffer stores each group
+// relative to its own max.
+constexpr int kVocabTile = 64;
 
 // Epilogues of the tcgen05 GEMM
 enum Epilogue : int {
@@ -60,7 +63,7 @@ struct UmmaArgs {
   int64_t ignore_index;
   int64_t col_base;              // kEpiLse / kEpiDlogits: vocabulary index of output column 0
   const int64_t* targets;        // targets of this chunk's tokens
-  float2* partials;              // [rows][vocab_tiles] (running max, sum of exp)
+  float2* partials;              // [rows][vocab_tiles] (max, sum of exp) per 64-column group
   float* zt;                     // [rows] fp32 target logit
   const float* lse;              // [rows] log-sum-exp (kEpiDlogits)
   float* dcorr;                  // [rows] rounding error of the target entry (kEpiDlogits)

@@ -127,8 +127,9 @@ __global__ void __launch_bounds__(256) simt_splitk_reduce_kernel(
   }
 }
 
-// One warp per (token row, vocab tile of 256): m = max z, l = sum exp(z - m),
-// and z_t when the target falls in the tile; each lane takes 8 columns. The
+// One warp per (token row, vocab tile of kVocabTile columns): m = max z,
+// l = sum exp(z - m), and z_t when the target falls in the tile; each lane
+// takes kVocabTile / 32 columns. The
 // buffer's column 0 is vocabulary column col_base; partials rows are
 // part_stride apart.
 __global__ void __launch_bounds__(256) simt_tile_stats_kernel(
@@ -141,10 +142,11 @@ __global__ void __launch_bounds__(256) simt_tile_stats_kernel(
   const int r = w / vocab_tiles, vt = w - r * vocab_tiles;
   const float* row = logits + static_cast<size_t>(r) * ldv;
   const int64_t tg = t[r];
-  float z[8];
+  constexpr int kPerLane = kVocabTile / 32;
+  float z[kPerLane];
   float m = -INFINITY;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < kPerLane; ++q) {
     const int64_t j = static_cast<int64_t>(vt) * kVocabTile + q * 32 + lane;
     z[q] = j < V ? row[j] : -INFINITY;
     m = fmaxf(m, z[q]);
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(256) simt_tile_stats_kernel(
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float l = 0.f;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) l += z[q] == -INFINITY ? 0.f : expf(z[q] - m);
+  for (int q = 0; q < kPerLane; ++q) l += z[q] == -INFINITY ? 0.f : expf(z[q] - m);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   if (lane == 0) partials[static_cast<size_t>(r) * part_stride + vt] = make_float2(m, l);

@@ -70,7 +70,16 @@ constexpr uint32_t kSmemBytesWide = 1024 + kStagesWide * kStageBytesWide +
                                     2 * kEpiBufsWide * kEpiBytes + (2 * kStagesWide + 3) * 8 + 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 192;
-constexpr int kThreadsWide = 320;   // producer warp, MMA warp, two epilogues of four warps
+// wide tiles: warpgroup 0 (TMA producer warp, MMA warp, two idle warps) and
+// two epilogue warpgroups; registers move from warpgroup 0 to the epilogues
+// (setmaxnreg), whose log-sum-exp pass keeps a row's 256 columns of bf16 in
+// registers. The split must fit the launch: 384 threads x kWideLaunchRegs.
+constexpr int kThreadsWide = 384;
+constexpr uint32_t kWideRegsCtl = 56;    // warpgroup 0
+constexpr uint32_t kWideRegsEpi = 224;   // each epilogue warpgroup
+constexpr int kWideLaunchRegs = 168;     // what __launch_bounds__(384, 1) leaves a thread
+static_assert(128 * kWideRegsCtl + 256 * kWideRegsEpi <= kThreadsWide * kWideLaunchRegs,
+              "register split of the wide kernel");
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kEpiBar = 1;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -144,7 +153,7 @@ __device__ __forceinline__ void stage_row(uint8_t* buf, int r, const uint32_t (&
 template <int EPI, int NBUF = 2, class Release>
 __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorMap* tmO, uint8_t* sE,
                                               uint32_t& ebuf, int row, bool leader, int m0, int n0,
-                                              int n_tile, int s_idx, uint32_t tbase,
+                                              int s_idx, uint32_t tbase,
                                               Release&& release, uint32_t bar = kEpiBar) {
   static_assert(NBUF == 1 || NBUF == 2, "staging buffers");
   const int grow = m0 + row;
@@ -166,61 +175,101 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
     if (NBUF == 2) ebuf ^= 1u;
   };
 
-  if constexpr (EPI == kEpiLse || EPI == kEpiDlogits) {
+  if constexpr (EPI == kEpiLse) {
+    // One pass over the accumulator, then the arithmetic. Per 64-column group
+    // g: read the group from TMEM, take its row max m_g (and the target logit
+    // when it falls in the group), and keep y = z - m_g packed as bf16 in
+    // registers. Once the last group is read the accumulator goes back to the
+    // MMA issuer; only then come the exponentials (the MUFU-bound part:
+    // 16 per clock per SM), s_g = sum of exp(y) over the packed values, and
+    // the stores of y. The partial of group g is (m_g, s_g). Stored relative
+    // to its group's max, every group's largest entries sit near 0, where
+    // bf16 is most precise; the dlogits pass adds m_g back from the partial,
+    // and since s_g sums the same bf16 values that pass exponentiates, the
+    // softmax it forms sums to one over the row. Columns past the output's
+    // last (a ragged vocabulary) enter as -inf: they add nothing.
+    constexpr int kGroups = kBN / 64;
+    int64_t tg = -1;
+    if (rvalid) tg = a.targets[grow];
+    const int64_t tl = (rvalid && tg != a.ignore_index) ? tg - a.col_base : -1;
+    const int tcol = (tl >= n0 && tl < n0 + kBN) ? static_cast<int>(tl - n0) : -1;
+    const int last_g = min(kGroups - 1, (a.cols - n0 - 1) / 64);  // uniform, >= 0
+    uint32_t y[kGroups][32];
+    float mg[kGroups];
+    float zt = 0.f;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      if (g > last_g) break;  // uniform across the epilogue threads
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(tbase + g * 64, r0);
+      tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
+      tmem_ld_wait();
+      tmem_regs_ready(r0);
+      tmem_regs_ready(r1);
+      if (g == last_g) release();
+      const int ncv = a.cols - (n0 + g * 64);  // valid columns in the group (uniform)
+      if (ncv < 64) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i >= ncv) r0[i] = 0xFF800000u;  // -inf
+          if (i + 32 >= ncv) r1[i] = 0xFF800000u;
+        }
+      }
+      float m8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m8[j] = fmaxf(__uint_as_float(r0[j]), __uint_as_float(r1[j]));
+#pragma unroll
+      for (int i = 8; i < 32; ++i) {
+        m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(r0[i]));
+        m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(r1[i]));
+      }
+      const float m = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                            fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      if (tcol >= g * 64 && tcol < g * 64 + 64) {
+        const int k = tcol - g * 64;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i == k) zt = __uint_as_float(r0[i]);
+          if (i + 32 == k) zt = __uint_as_float(r1[i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        y[g][i] = pack_bf16x2(__uint_as_float(r0[2 * i]) - m, __uint_as_float(r0[2 * i + 1]) - m);
+        y[g][16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]) - m, __uint_as_float(r1[2 * i + 1]) - m);
+      }
+      mg[g] = m;
+    }
+    // the accumulator is free: sums of exp and stores
+    const size_t prow = static_cast<size_t>(grow) * a.vocab_tiles + static_cast<size_t>(n0 / 64);
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      if (g > last_g) break;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        s4[i & 3] += ex2_approx(__uint_as_float(y[g][i] << 16) * kLog2e);
+        s4[(i + 2) & 3] += ex2_approx(__uint_as_float(y[g][i] & 0xFFFF0000u) * kLog2e);
+      }
+      if (rvalid) a.partials[prow + g] = make_float2(mg[g], (s4[0] + s4[1]) + (s4[2] + s4[3]));
+      if (a.store_logits) {
+        const int c0 = n0 + g * 64;
+        stage_and_store(y[g], [&](uint32_t src) { tma_store_2d(tmO, src, c0, m0); });
+      }
+    }
+    if (rvalid && tcol >= 0) a.zt[grow] = zt;
+  } else if constexpr (EPI == kEpiDlogits) {
+    // d = (exp(z - lse) - onehot) * scale, one pass over the accumulator; the
+    // fp32 rounding error of the target entry goes to dcorr for the dx
+    // reduction
     int64_t tg = -1;
     if (rvalid) tg = a.targets[grow];
     const bool tvalid = rvalid && tg != a.ignore_index;
     const int64_t tl = tg - a.col_base;  // target column in this GEMM's output
     const int tcol = (tvalid && tl >= n0 && tl < n0 + kBN) ? static_cast<int>(tl - n0) : -1;
-    float tmax = -INFINITY, tsum = 0.f, zt = 0.f;
-    float scale = 0.f, lse_l2 = 0.f;
-    if constexpr (EPI == kEpiDlogits) {
-      const uint32_t nv = a.ctrl[kCtrlNValid];
-      scale = (tvalid && nv > 0) ? 1.0f / static_cast<float>(nv) : 0.f;
-      lse_l2 = rvalid ? a.lse[grow] * kLog2e : 0.f;
-    }
-    if constexpr (EPI == kEpiLse) {
-      // pass 1 over the accumulator: the tile's row max and the target logit,
-      // 64 columns per TMEM wait; full groups take the max as eight
-      // independent chains
-#pragma unroll 1
-      for (int g = 0; g < kBN / 64; ++g) {
-        const int ncv = a.cols - (n0 + g * 64);
-        if (ncv <= 0) break;  // uniform across the epilogue threads
-        uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(tbase + g * 64, r0);
-        tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
-        tmem_ld_wait();
-        tmem_regs_ready(r0);
-        tmem_regs_ready(r1);
-        if (ncv >= 64) {
-          float m[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) m[j] = fmaxf(__uint_as_float(r0[j]), __uint_as_float(r1[j]));
-#pragma unroll
-          for (int i = 8; i < 32; ++i) {
-            m[i & 7] = fmaxf(m[i & 7], __uint_as_float(r0[i]));
-            m[i & 7] = fmaxf(m[i & 7], __uint_as_float(r1[i]));
-          }
-          tmax = fmaxf(tmax, fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])),
-                                   fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7]))));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (i < ncv) tmax = fmaxf(tmax, __uint_as_float(r0[i]));
-            if (i + 32 < ncv) tmax = fmaxf(tmax, __uint_as_float(r1[i]));
-          }
-        }
-        if (tcol >= g * 64 && tcol < g * 64 + 64) {
-          const int k = tcol - g * 64;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (i == k) zt = __uint_as_float(r0[i]);
-            if (i + 32 == k) zt = __uint_as_float(r1[i]);
-          }
-        }
-      }
-    }
+    const uint32_t nv = a.ctrl[kCtrlNValid];
+    const float scale = (tvalid && nv > 0) ? 1.0f / static_cast<float>(nv) : 0.f;
+    const float lse_l2 = rvalid ? a.lse[grow] * kLog2e : 0.f;
     // last 64-column group holding valid columns (uniform)
     const int last_g = min(kBN / 64 - 1, (a.cols - n0 - 1) / 64);
 #pragma unroll 1
@@ -233,73 +282,31 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
       tmem_regs_ready(r1);
       if (g == last_g) release();
       const int c0 = n0 + g * 64;
-      const int ncv = a.cols - c0;  // valid columns in this group, >= 1 (uniform)
-      if constexpr (EPI == kEpiLse) {
-        // pass 2: sum of exp(z - tmax), and the logits stored shifted by the
-        // tile max, y = z - tmax, so that the largest entries are stored near
-        // 0 where bf16 is most precise
-        const float ml = tmax * kLog2e;
-        if (ncv >= 64) {
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      const int k = (tcol >= g * 64 && tcol < g * 64 + 64) ? tcol - g * 64 : -1;
+      uint32_t w[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            s4[i & 3] += ex2_approx(fmaf(__uint_as_float(r0[i]), kLog2e, -ml));
-            s4[i & 3] += ex2_approx(fmaf(__uint_as_float(r1[i]), kLog2e, -ml));
-          }
-          tsum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-        } else {
+      for (int i = 0; i < 16; ++i) {
+        float v[4] = {__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]),
+                      __uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])};
+        const int ci[4] = {2 * i, 2 * i + 1, 32 + 2 * i, 33 + 2 * i};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (i < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r0[i]), kLog2e, -ml));
-            if (i + 32 < ncv) tsum += ex2_approx(fmaf(__uint_as_float(r1[i]), kLog2e, -ml));
+        for (int q = 0; q < 4; ++q) {
+          float p = ex2_approx(fmaf(v[q], kLog2e, -lse_l2));
+          if (ci[q] == k) p -= 1.0f;
+          v[q] = p * scale;
+        }
+        w[i] = pack_bf16x2(v[0], v[1]);
+        w[16 + i] = pack_bf16x2(v[2], v[3]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (ci[q] == k) {
+            const uint32_t word = q < 2 ? w[i] : w[16 + i];
+            const uint32_t bits = (q & 1) ? (word >> 16) : (word & 0xFFFFu);
+            a.dcorr[grow] = v[q] - __uint_as_float(bits << 16);
           }
         }
-        if (a.store_logits) {
-          uint32_t w[32];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            w[i] = pack_bf16x2(__uint_as_float(r0[2 * i]) - tmax, __uint_as_float(r0[2 * i + 1]) - tmax);
-            w[16 + i] =
-                pack_bf16x2(__uint_as_float(r1[2 * i]) - tmax, __uint_as_float(r1[2 * i + 1]) - tmax);
-          }
-          stage_and_store(w, [&](uint32_t src) { tma_store_2d(tmO, src, c0, m0); });
-        }
-      } else {
-        // d = (exp(z - lse) - onehot) * scale over the logits buffer; the
-        // fp32 rounding error of the target entry goes to dcorr for the dx
-        // reduction
-        const int k = (tcol >= g * 64 && tcol < g * 64 + 64) ? tcol - g * 64 : -1;
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float v[4] = {__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]),
-                        __uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1])};
-          const int ci[4] = {2 * i, 2 * i + 1, 32 + 2 * i, 33 + 2 * i};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float p = ex2_approx(fmaf(v[q], kLog2e, -lse_l2));
-            if (ci[q] == k) p -= 1.0f;
-            v[q] = p * scale;
-          }
-          w[i] = pack_bf16x2(v[0], v[1]);
-          w[16 + i] = pack_bf16x2(v[2], v[3]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (ci[q] == k) {
-              const uint32_t word = q < 2 ? w[i] : w[16 + i];
-              const uint32_t bits = (q & 1) ? (word >> 16) : (word & 0xFFFFu);
-              a.dcorr[grow] = v[q] - __uint_as_float(bits << 16);
-            }
-          }
-        }
-        stage_and_store(w, [&](uint32_t src) { tma_store_2d(tmO, src, c0, m0); });
       }
-    }
-    if constexpr (EPI == kEpiLse) {
-      if (rvalid) {
-        a.partials[static_cast<size_t>(grow) * a.vocab_tiles + n_tile] = make_float2(tmax, tsum);
-        if (tcol >= 0) a.zt[grow] = zt;
-      }
+      stage_and_store(w, [&](uint32_t src) { tma_store_2d(tmO, src, c0, m0); });
     }
   } else if constexpr (EPI == kEpiBf16) {
 #pragma unroll 1
@@ -509,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const Unit t = unit_coords(a, u);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + acc * kBN;
-      epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, t.m * kBM, t.n * kBN, t.n, t.s, tbase, [&] {
+      epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, t.m * kBM, t.n * kBN, t.s, tbase, [&] {
         tc_fence_before();
         mbar_arrive(tempty_bar(acc));
       });
@@ -689,7 +696,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const Unit t = unit_coords(a, u);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + acc * kBN;
       const int m0 = t.m * 2 * kBM + static_cast<int>(rank) * kBM;
-      epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, m0, t.n * kBN, t.n, t.s, tbase, [&] {
+      epilogue_tile<EPI>(a, &tmO, sE, ebuf, row, leader, m0, t.n * kBN, t.s, tbase, [&] {
         tc_fence_before();
         if (rank == 0)
           mbar_arrive(tempty_bar(acc));
@@ -772,115 +779,120 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int num_units = a.num_m * a.num_n * a.num_s;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------ TMA producer
-      uint32_t n_issued = 0;
-      bool failed = false;
-      for (int u = pair; u < num_units && !failed; u += npairs) {
-        const Unit t = unit_coords(a, u);
-        const int kb0 = t.s * a.kb_per_split;
-        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
-        const int mA = t.m * 2 * kBM + static_cast<int>(rank) * kBM;      // this CTA's rows of A
-        const int nB0 = t.n * 2 * kBN + static_cast<int>(rank) * (kBN / 2);  // its columns, MMA 0
-        const int nB1 = nB0 + kBN;                                          // and MMA 1
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const int stage = n_issued % kStagesWide;
-          const uint32_t phase = (n_issued / kStagesWide) & 1u;
-          if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, a.ctrl, a.timeout_ns)) {
-            failed = true;
-            break;
+  // each role's code sits inside the branch that sets its register budget
+  if (warp < 4) {
+    warpgroup_regs_dec<kWideRegsCtl>();
+    if (warp == 0) {
+      if (lane == 0) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t n_issued = 0;
+        bool failed = false;
+        for (int u = pair; u < num_units && !failed; u += npairs) {
+          const Unit t = unit_coords(a, u);
+          const int kb0 = t.s * a.kb_per_split;
+          const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+          const int mA = t.m * 2 * kBM + static_cast<int>(rank) * kBM;      // this CTA's rows of A
+          const int nB0 = t.n * 2 * kBN + static_cast<int>(rank) * (kBN / 2);  // its columns, MMA 0
+          const int nB1 = nB0 + kBN;                                          // and MMA 1
+          for (int kb = kb0; kb < kb1; ++kb) {
+            const int stage = n_issued % kStagesWide;
+            const uint32_t phase = (n_issued / kStagesWide) & 1u;
+            if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, a.ctrl, a.timeout_ns)) {
+              failed = true;
+              break;
+            }
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytesWide);
+            const uint32_t fb = mapa_shared(full_bar(stage), 0);
+            const uint32_t sa = smem_u32(sA + stage * kABytes);
+            const uint32_t sb = smem_u32(sB + stage * kBBytes);
+            const int k0 = kb * kBK;
+            if (AMN == 0) {
+              tma_load_2d_pair(sa, &tmA, fb, k0, mA);
+            } else {
+              tma_load_2d_pair(sa, &tmA, fb, mA, k0);
+              tma_load_2d_pair(sa + 8192, &tmA, fb, mA + 64, k0);
+            }
+            if (BMN == 0) {
+              tma_load_2d_pair(sb, &tmB, fb, k0, nB0);
+              tma_load_2d_pair(sb + kBHalfBytes, &tmB, fb, k0, nB1);
+            } else {
+              tma_load_2d_pair(sb, &tmB, fb, nB0, k0);
+              tma_load_2d_pair(sb + 8192, &tmB, fb, nB0 + 64, k0);
+              tma_load_2d_pair(sb + kBHalfBytes, &tmB, fb, nB1, k0);
+              tma_load_2d_pair(sb + kBHalfBytes + 8192, &tmB, fb, nB1 + 64, k0);
+            }
+            ++n_issued;
           }
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytesWide);
-          const uint32_t fb = mapa_shared(full_bar(stage), 0);
-          const uint32_t sa = smem_u32(sA + stage * kABytes);
-          const uint32_t sb = smem_u32(sB + stage * kBBytes);
-          const int k0 = kb * kBK;
-          if (AMN == 0) {
-            tma_load_2d_pair(sa, &tmA, fb, k0, mA);
-          } else {
-            tma_load_2d_pair(sa, &tmA, fb, mA, k0);
-            tma_load_2d_pair(sa + 8192, &tmA, fb, mA + 64, k0);
-          }
-          if (BMN == 0) {
-            tma_load_2d_pair(sb, &tmB, fb, k0, nB0);
-            tma_load_2d_pair(sb + kBHalfBytes, &tmB, fb, k0, nB1);
-          } else {
-            tma_load_2d_pair(sb, &tmB, fb, nB0, k0);
-            tma_load_2d_pair(sb + 8192, &tmB, fb, nB0 + 64, k0);
-            tma_load_2d_pair(sb + kBHalfBytes, &tmB, fb, nB1, k0);
-            tma_load_2d_pair(sb + kBHalfBytes + 8192, &tmB, fb, nB1 + 64, k0);
-          }
-          ++n_issued;
+        }
+        if (failed && rank == 0) {
+          const uint32_t first = n_issued > kStagesWide ? n_issued - kStagesWide : 0;
+          for (uint32_t i = first; i < n_issued; ++i)
+            mbar_drain_wait(full_bar(i % kStagesWide), (i / kStagesWide) & 1u, a.timeout_ns);
         }
       }
-      if (failed && rank == 0) {
-        const uint32_t first = n_issued > kStagesWide ? n_issued - kStagesWide : 0;
-        for (uint32_t i = first; i < n_issued; ++i)
-          mbar_drain_wait(full_bar(i % kStagesWide), (i / kStagesWide) & 1u, a.timeout_ns);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
-      // ------------------------------------- MMA issuer (CTA 0 of the pair)
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, AMN, BMN);
-      uint32_t n_consumed = 0;
-      bool issued = false, failed = false;
-      int it = 0;
-      for (int u = pair; u < num_units && !failed; u += npairs, ++it) {
-        const Unit t = unit_coords(a, u);
-        const int kb0 = t.s * a.kb_per_split;
-        const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
-        if (!mbar_wait_bounded_cluster(tempty_bar, (it & 1) ^ 1u, a.ctrl, a.timeout_ns)) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const int stage = n_consumed % kStagesWide;
-          const uint32_t phase = (n_consumed / kStagesWide) & 1u;
-          if (!mbar_wait_bounded_cluster(full_bar(stage), phase, a.ctrl, a.timeout_ns)) {
+    } else if (warp == 1) {
+      if (lane == 0 && rank == 0) {
+        // ------------------------------------- MMA issuer (CTA 0 of the pair)
+        constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, AMN, BMN);
+        uint32_t n_consumed = 0;
+        bool issued = false, failed = false;
+        int it = 0;
+        for (int u = pair; u < num_units && !failed; u += npairs, ++it) {
+          const Unit t = unit_coords(a, u);
+          const int kb0 = t.s * a.kb_per_split;
+          const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+          if (!mbar_wait_bounded_cluster(tempty_bar, (it & 1) ^ 1u, a.ctrl, a.timeout_ns)) {
             failed = true;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(sA + stage * kABytes);
-          const uint32_t sb = smem_u32(sB + stage * kBBytes);
-#pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t ad = AMN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
-                                    : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-            const uint32_t ko = BMN ? 2048u * k : 32u * k;
-            const uint64_t bd0 = BMN ? smem_desc_sw128(sb + ko, 8192u, 1024u)
-                                     : smem_desc_sw128(sb + ko, 16u, 1024u);
-            const uint64_t bd1 = BMN ? smem_desc_sw128(sb + kBHalfBytes + ko, 8192u, 1024u)
-                                     : smem_desc_sw128(sb + kBHalfBytes + ko, 16u, 1024u);
-            const uint32_t acc_in = (kb > kb0 || k > 0) ? 1u : 0u;
-            tc_mma_bf16_pair_a_fill(tmem_base, ad, bd0, idesc, acc_in);
-            tc_mma_bf16_pair_a_lastuse(tmem_base + kBN, ad, bd1, idesc, acc_in);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            const int stage = n_consumed % kStagesWide;
+            const uint32_t phase = (n_consumed / kStagesWide) & 1u;
+            if (!mbar_wait_bounded_cluster(full_bar(stage), phase, a.ctrl, a.timeout_ns)) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(sA + stage * kABytes);
+            const uint32_t sb = smem_u32(sB + stage * kBBytes);
+  #pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t ad = AMN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                      : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+              const uint32_t ko = BMN ? 2048u * k : 32u * k;
+              const uint64_t bd0 = BMN ? smem_desc_sw128(sb + ko, 8192u, 1024u)
+                                       : smem_desc_sw128(sb + ko, 16u, 1024u);
+              const uint64_t bd1 = BMN ? smem_desc_sw128(sb + kBHalfBytes + ko, 8192u, 1024u)
+                                       : smem_desc_sw128(sb + kBHalfBytes + ko, 16u, 1024u);
+              const uint32_t acc_in = (kb > kb0 || k > 0) ? 1u : 0u;
+              tc_mma_bf16_pair_a_fill(tmem_base, ad, bd0, idesc, acc_in);
+              tc_mma_bf16_pair_a_lastuse(tmem_base + kBN, ad, bd1, idesc, acc_in);
+            }
+            issued = true;
+            tc_commit_pair_multicast(empty_bar(stage), 0x3);
+            ++n_consumed;
           }
-          issued = true;
-          tc_commit_pair_multicast(empty_bar(stage), 0x3);
-          ++n_consumed;
+          if (failed) break;
+          tc_commit_pair_multicast(tfull_bar, 0x3);
         }
-        if (failed) break;
-        tc_commit_pair_multicast(tfull_bar, 0x3);
-      }
-      if (failed && issued) {
-        tc_commit_pair(drain_bar);
-        mbar_drain_wait(drain_bar, 0, a.timeout_ns);
+        if (failed && issued) {
+          tc_commit_pair(drain_bar);
+          mbar_drain_wait(drain_bar, 0, a.timeout_ns);
+        }
       }
     }
   } else {
+    warpgroup_regs_inc<kWideRegsEpi>();
     // ------------------------------------------------------------ epilogue
-    // two epilogues of four warps, one per 256-column half of the tile, each
+    // two epilogue warpgroups, one per 256-column half of the tile, each
     // with its own staging buffer and named barrier; every thread of both
-    // hands the accumulator back after its last TMEM read
-    const int grp = (warp - 2) >> 2;
+    // hands the accumulator back after its last TMEM read. Warp w reads TMEM
+    // lanes 32 (w % 4) .. 32 (w % 4) + 31.
+    const int grp = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
-    const bool leader = threadIdx.x == 64 + grp * kEpiThreads;
+    const bool leader = threadIdx.x == (grp + 1) * kEpiThreads;
     const uint32_t bar = kEpiBar + static_cast<uint32_t>(grp);
     uint8_t* sEg = sE + grp * kEpiBufsWide * kEpiBytes;
     uint32_t ebuf = 0;
@@ -901,7 +913,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
           mbar_arrive_cluster(mapa_shared(tempty_bar, 0));
       };
       if (n0 < a.cols)
-        epilogue_tile<EPI, kEpiBufsWide>(a, &tmO, sEg, ebuf, row, leader, m0, n0, 2 * t.n + grp, t.s, tbase,
+        epilogue_tile<EPI, kEpiBufsWide>(a, &tmO, sEg, ebuf, row, leader, m0, n0, t.s, tbase,
                               release, bar);
       else
         release();   // the second half lies beyond the last column
@@ -1176,7 +1188,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       locate(u, q, t);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + acc * kBN;
       const int m0 = t.m * 2 * kBM + static_cast<int>(rank) * kBM;
-      epilogue_tile<kEpiF32>(d.p[q], &maps.o[q], sE, ebuf, row, leader, m0, t.n * kBN, t.n, t.s, tbase,
+      epilogue_tile<kEpiF32>(d.p[q], &maps.o[q], sE, ebuf, row, leader, m0, t.n * kBN, t.s, tbase,
                              [&] {
                                tc_fence_before();
                                if (rank == 0)
@@ -1236,10 +1248,25 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   return cudaGetLastError();
 }
 
+// The registers a wide kernel is launched with must cover its warpgroups'
+// split (setmaxnreg.inc would otherwise wait forever): checked once per
+// instantiation from the compiled register count.
+template <class Kernel>
+cudaError_t check_wide_regs(Kernel kern) {
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  return attr.numRegs * kThreadsWide >= static_cast<int>(128 * kWideRegsCtl + 256 * kWideRegsEpi)
+             ? cudaSuccess
+             : cudaErrorInvalidConfiguration;
+}
+
 template <int AMN, int BMN, int EPI>
 cudaError_t launch_wide_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
                           const UmmaArgs& args, int pairs, cudaStream_t s) {
   auto kern = umma_wide_kernel<AMN, BMN, EPI>;
+  static const cudaError_t regs_ok = check_wide_regs(kern);
+  if (regs_ok != cudaSuccess) return regs_ok;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytesWide));
   if (e != cudaSuccess) return e;

@@ -334,6 +334,19 @@ __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncol
                : "memory");
 }
 
+// Register re-allocation between warpgroups (all four warps of a warpgroup
+// execute it together). The registers a warpgroup gives up return to the
+// CTA's pool; an increase waits until the pool holds them, so the split must
+// not exceed what the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void warpgroup_regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void warpgroup_regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tmem_relinquish_pair() {
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }

@@ -70,10 +70,11 @@ GiB = 1 << 30
 def test_plan_llama3_default_budget():
     p = flce.plan(16384, 4096, 128256, "bf16")
     assert p["chunk"] == 4096 and p["num_chunks"] == 4
-    assert p["vocab_tiles"] == 501 and p["ldv"] == 128256
+    assert p["vocab_tiles"] == 2004 and p["ldv"] == 128256   # a partial per 64 columns
     assert p["logits_bytes"] == 4096 * 128256 * 2
     assert p["workspace_bytes"] <= int(1.25 * GiB)
-    assert p["tile_m"] == 256 and p["tile_n"] == 512   # wide CTA-pair tiles by default
+    # wide CTA-pair tiles for all three GEMMs at this shape (long reductions)
+    assert (p["tile_m"], p["tile_n"], p["tile_n_dx"], p["tile_n_dw"]) == (256, 512, 512, 512)
     assert p["dx_splits"] == 4          # 128 wide dx tiles on 76 SM pairs: 4 splits fill the waves
     q = flce.plan(16384, 4096, 128256, "bf16", cta="pair")
     assert (q["tile_n"], q["dx_splits"]) == (256, 2)   # 256 tiles of 256 x 256: 2 splits
@@ -110,7 +111,7 @@ def test_plan_small_and_ragged():
     p = flce.plan(2048, 1024, 32000, "bf16")
     assert p["chunk"] == 2048 and p["num_chunks"] == 1
     p = flce.plan(1000, 64, 4099, "bf16", chunk=300)
-    assert (p["chunk"], p["num_chunks"], p["ldv"], p["vocab_tiles"]) == (300, 4, 4160, 17)
+    assert (p["chunk"], p["num_chunks"], p["ldv"], p["vocab_tiles"]) == (300, 4, 4160, 65)
     p = flce.plan(50, 64, 100, "bf16")
     assert p["chunk"] == 50 and p["num_chunks"] == 1
     p = flce.plan(0, 64, 100, "bf16")
@@ -146,7 +147,7 @@ def test_plan_slabs_bounded_in_V():
     assert q["vocab_slab"] == vs
     assert q["workspace_bytes"] - p["workspace_bytes"] <= p["chunk"] * 8 * (q["vocab_tiles"] - p["vocab_tiles"]) + 4096
     # small budgets shorten the chunk before they narrow the slab below 8192
-    for mib, chunk, slab in ((128, 3328, 8704), (64, 1664, 9728), (24, 640, 9216)):
+    for mib, chunk, slab in ((128, 3328, 11776), (64, 1920, 9216), (24, 640, 11264)):
         r = flce.plan(16384, 4096, 128256, "bf16", dlogits_mode="slabs", hbm_budget_bytes=mib << 20)
         assert (r["chunk"], r["vocab_slab"]) == (chunk, slab)
         assert r["workspace_bytes"] <= mib << 20
@@ -207,3 +208,20 @@ def test_plan_refuses_a_tile_shape_that_does_not_exist(lib):
     cfg.cta_pair = 3
     p = flce.Plan()
     assert lib.flce_make_plan(ctypes.byref(cfg), 1024, 256, 1000, 0, 0, ctypes.byref(p)) == 1
+
+
+def test_plan_picks_tile_shapes_per_gemm():
+    """The default handle times wide (256 x 512) against pair (256 x 256)
+    tiles per GEMM with a model and takes pair tiles only where they win by
+    more than 5%: the short reductions of a 2048 x 1024 x 32000 call (logits
+    K = 1024, dW K = 2048); the long ones of the Llama-3 shape stay wide.
+    An explicit tile shape applies to every GEMM."""
+    p = flce.plan(2048, 1024, 32000)
+    assert (p["tile_n"], p["tile_n_dx"], p["tile_n_dw"]) == (256, 512, 256)
+    q = flce.plan(2048, 1024, 32000, cta="wide")
+    assert (q["tile_n"], q["tile_n_dx"], q["tile_n_dw"]) == (512, 512, 512)
+    r = flce.plan(2048, 1024, 32000, cta="pair")
+    assert (r["tile_n"], r["tile_n_dx"], r["tile_n_dw"]) == (256, 256, 256)
+    # the slab walk keeps the wide tiles its slab sizing assumes
+    s = flce.plan(16384, 4096, 128256, dlogits_mode="slabs")
+    assert (s["tile_n"], s["tile_n_dx"], s["tile_n_dw"]) == (512, 512, 512)

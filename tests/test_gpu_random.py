@@ -1,6 +1,7 @@
 """Parity with the fp64 oracle on seeded random shapes: token counts, hidden
 sizes (multiples of 8), vocabulary sizes, ignore fractions, target
-distributions and chunk sizes drawn per case, on all four tile shapes, one
+distributions and chunk sizes drawn per case, rotating over the tile shapes (the
+default picks wide or pair tiles per GEMM), one
 handle per shape reused across the cases (workspace growth, cached tile
 orders, changing tensor maps)."""
 import numpy as np
@@ -12,7 +13,7 @@ from flce_testing import assert_parity, run
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = ("single", "pair", "wide")
+SHAPES = ("single", "pair", "wide", "auto")
 
 
 @pytest.fixture(scope="module")

@@ -37,7 +37,7 @@ CASES = [
     (1000, 256, 4099, 0.1, 21),        # one chunk, odd V
     (3000, 512, 50257, 0.05, 22),      # one chunk, GPT-2-sized vocabulary
     (9000, 512, 32000, 0.1, 23),       # three 4096-token chunks, the last 808 tokens
-    (1500, 64, 2_000_000, 0.1, 24),    # the scratch holds 1024-token chunks: two, the last 476
+    (1500, 64, 2_000_000, 0.1, 24),    # the scratch holds 256-token chunks: six, the last 220
 ]
 
 
