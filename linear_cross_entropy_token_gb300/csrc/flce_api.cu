@@ -684,16 +684,16 @@ int shape_for(flce_handle_t h, int64_t tile_n) {
   return tile_n == 2 * kBN ? kShapeWide : kShapePair;
 }
 
-// One GEMM on tile shape `shape`; sets num_m (and, for wide tiles, num_n)
-// from the extents and the grid from the work units (persistent CTAs, or CTA
-// pairs). args.num_n counts 256-column tiles on entry.
+// One GEMM on tile shape `shape`; sets num_m and num_n from the extents (M
+// rows, args.cols columns) and the grid from the work units (persistent
+// CTAs, or CTA pairs).
 cudaError_t launch_gemm(flce_handle_t h, int shape, int kind, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& o, UmmaArgs args, int64_t M, cudaStream_t s) {
   const int rows_per_unit = shape == kShapeSingle ? kBM : 2 * kBM;
   const int slots_max = shape == kShapeWide ? h->wide_clusters
                         : shape == kShapePair ? h->pair_clusters : h->num_sms;
   args.num_m = static_cast<int>(cdiv(M, rows_per_unit));
-  if (shape == kShapeWide) args.num_n = static_cast<int>(cdiv(args.cols, 2 * kBN));
+  args.num_n = static_cast<int>(cdiv(args.cols, shape == kShapeWide ? 2 * kBN : kBN));
   const int units = args.num_m * args.num_n * args.num_s;
   const int slots = std::min(units, slots_max);
   if (args.raster == 2) args.group_m = group_for(h, shape, args.num_m, args.num_n, args.num_s, slots);
@@ -1024,7 +1024,7 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
 
       // 1. projection with the online max / sum-exp epilogue
       UmmaArgs a{};
-      a.num_n = vt;
+      a.num_n = static_cast<int>(cdiv(V, kBN));
       a.num_s = 1;
       a.kb_total = kb_h;
       a.kb_per_split = kb_h;

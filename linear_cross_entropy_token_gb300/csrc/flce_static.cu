@@ -130,7 +130,7 @@ extern "C" flce_status flce_loss_static(const void* x, const void* W, const int6
       if (!encode_bf16_2d(&mX, xb + off * H, H, rows, H * 2, 64, 128)) return FLCE_ERR_INVALID_ARG;
       UmmaArgs a{};
       a.num_m = (rows + kBM - 1) / kBM;
-      a.num_n = static_cast<int>(vt);
+      a.num_n = static_cast<int>((V + kBN - 1) / kBN);
       a.num_s = 1;
       a.kb_total = static_cast<int>((H + kBK - 1) / kBK);
       a.kb_per_split = a.kb_total;

@@ -156,6 +156,10 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
                                               int s_idx, uint32_t tbase,
                                               Release&& release, uint32_t bar = kEpiBar) {
   static_assert(NBUF == 1 || NBUF == 2, "staging buffers");
+  if (n0 >= a.cols) {  // a tile past the last column (uniform): nothing to read
+    release();
+    return;
+  }
   const int grow = m0 + row;
   const bool rvalid = grow < a.rows;
 

@@ -93,8 +93,9 @@ def test_loss_static_refuses_sizes_beyond_its_scratch():
     t = torch.zeros(1, dtype=torch.int64, device="cuda")
     tl = torch.zeros(1, dtype=torch.float32, device="cuda")
     loss = ctypes.c_float()
-    # V = 20 million needs 128 x 78125 x 8 bytes = 80 MB of scratch for one
-    # 128-token chunk, beyond the 64 MiB array: refused before any launch
+    # V = 20 million needs 128 x 312500 x 8 bytes = 320 MB of scratch for one
+    # 128-token chunk (a partial per 64 vocabulary columns), beyond the 64 MiB
+    # array: refused before any launch
     st = lib.flce_loss_static(buf.data_ptr(), buf.data_ptr(), t.data_ptr(), 1, 8, 20_000_000, -100,
                               ctypes.byref(loss), tl.data_ptr(), None)
     assert st == 1  # FLCE_ERR_INVALID_ARG
