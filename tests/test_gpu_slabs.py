@@ -241,7 +241,7 @@ def test_autograd_with_a_slab_handle():
 @pytest.mark.parametrize("N,H,V,chunk,budget,min_slabs", [
     (256, 128, 4096, 64, 0, 1),            # the tiny fp32 config: one slab
     (256, 128, 4096, 64, 300 << 10, 4),    # four slabs of 1024
-    (300, 100, 2999, 128, 300 << 10, 6),   # ragged chunks, a ragged last slab, odd H
+    (300, 100, 2999, 128, 320 << 10, 6),   # ragged chunks, a ragged last slab, odd H
 ])
 def test_fp32_slabs(N, H, V, chunk, budget, min_slabs):
     """The slab walk on the fp32 CUDA-core path, at the fp32 tolerance."""
