@@ -91,7 +91,25 @@ __global__ void count_only_kernel(const int64_t* __restrict__ t, int64_t N, int6
 }
 
 // One warp per token row: lse = M + log sum_s l_s exp(m_s - M) over the vocab
-// tiles' (m_s, l_s); token loss = lse - z_t (0 for an ignored token).
+// tiles' (m_s, l_s); token loss = lse - z_t (0 for an ignored token). One
+// pass over the partials: each lane keeps a running (max, sum) and rescales
+// its sum when the max grows; the lanes' pairs then merge the same way, in a
+// fixed order.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  if (m2 > m) {
+    s = s * ex2_approx((m - m2) * kLog2e) + s2;
+    m = m2;
+  } else {
+    s += s2 * ex2_approx((m2 - m) * kLog2e);
+  }
+}
+
 __global__ void lse_combine_kernel(const float2* __restrict__ partials, int vocab_tiles,
                                    const float* __restrict__ zt, const int64_t* __restrict__ t,
                                    int rows, int64_t ignore_index, float* __restrict__ lse,
@@ -101,18 +119,17 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partials, int voca
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
   const float2* p = partials + static_cast<size_t>(r) * vocab_tiles;
-  float M = -INFINITY;
-  for (int s = lane; s < vocab_tiles; s += 32) M = fmaxf(M, p[s].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float S = 0.f;
-  const float Ml = M * kLog2e;
+  float M = -INFINITY, S = 0.f;
   for (int s = lane; s < vocab_tiles; s += 32) {
     const float2 q = p[s];
-    S += q.y * ex2_approx(fmaf(q.x, kLog2e, -Ml));
+    lse_merge(M, S, q.x, q.y);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+    lse_merge(M, S, m2, s2);
+  }
   if (lane == 0) {
     const float l = M + logf(S);
     lse[r] = l;
@@ -137,8 +154,10 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partials, int voca
 // common to all rows. Its exact fp32 rounding error goes to dcorr[row] so the
 // dx reduction can add dcorr·W[t] back. Ignored rows and padding columns get 0.
 constexpr int kDlogitsVecs = 4;
+constexpr int kDlogitsThreads = 256;
+constexpr int kDlogitsCols = kDlogitsThreads * 8 * kDlogitsVecs;  // columns per block
 
-__global__ void __launch_bounds__(256) dlogits_bf16_kernel(
+__global__ void __launch_bounds__(kDlogitsThreads) dlogits_bf16_kernel(
     __nv_bfloat16* __restrict__ buf, int64_t ldv, int64_t V, const float2* __restrict__ partials,
     int vocab_tiles, const float* __restrict__ lse, const int64_t* __restrict__ t,
     int64_t ignore_index, const uint32_t* __restrict__ ctrl, float* __restrict__ dcorr) {
@@ -166,12 +185,21 @@ __global__ void __launch_bounds__(256) dlogits_bf16_kernel(
     const int64_t c0 = base + (static_cast<int64_t>(i) * blockDim.x + threadIdx.x) * 8;
     if (c0 < ldv) v[i] = *reinterpret_cast<const uint4*>(row + c0);
   }
+  // the block's per-group exponent offsets (lse - m_g)·log2 e, staged once in
+  // shared memory while the vectors above are in flight
+  __shared__ float s_ll[kDlogitsCols / kVocabTile];
+  {
+    const int64_t g0 = base / kVocabTile;
+    for (int q = threadIdx.x; q < kDlogitsCols / kVocabTile; q += blockDim.x)
+      if (g0 + q < vocab_tiles) s_ll[q] = (l - prow[g0 + q].x) * kLog2e;
+    __syncthreads();
+  }
 #pragma unroll
   for (int i = 0; i < kDlogitsVecs; ++i) {
     const int64_t c0 = base + (static_cast<int64_t>(i) * blockDim.x + threadIdx.x) * 8;
     if (c0 >= ldv) continue;
     // 8 columns never straddle a vocab tile
-    const float ll = (l - prow[c0 / kVocabTile].x) * kLog2e;
+    const float ll = s_ll[(c0 - base) / kVocabTile];
     uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     if (c0 + 8 <= V && (tg < c0 || tg >= c0 + 8)) {
       const float nl = ll + lg_nv;
@@ -333,10 +361,8 @@ cudaError_t launch_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int rows, int64
                                 const float2* partials, int vocab_tiles, const float* lse,
                                 const int64_t* t_chunk, int64_t ignore_index,
                                 const uint32_t* ctrl, float* dcorr, cudaStream_t s) {
-  const int threads = 256;
-  const int64_t per_block = threads * 8 * kDlogitsVecs;
-  dim3 grid(static_cast<unsigned>((ldv + per_block - 1) / per_block), static_cast<unsigned>(rows));
-  dlogits_bf16_kernel<<<grid, threads, 0, s>>>(buf, ldv, V, partials, vocab_tiles, lse, t_chunk,
+  dim3 grid(static_cast<unsigned>((ldv + kDlogitsCols - 1) / kDlogitsCols), static_cast<unsigned>(rows));
+  dlogits_bf16_kernel<<<grid, kDlogitsThreads, 0, s>>>(buf, ldv, V, partials, vocab_tiles, lse, t_chunk,
                                                ignore_index, ctrl, dcorr);
   return cudaGetLastError();
 }

@@ -337,7 +337,8 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
     // kG - kAhead store rounds rather than kG - 1, and the last rounds' stores
     // overlap the next tile's MMAs.
     constexpr int kG = kBN / 32;
-    constexpr int kAhead = 4;
+    constexpr int kAhead = 6;   // 192 registers of look-ahead: the wide kernel's
+                                // epilogue warpgroups hold 224 (setmaxnreg)
     static_assert(kAhead <= kG, "look-ahead");
     uint32_t r[kAhead][32];
 #pragma unroll
