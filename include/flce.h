@@ -170,7 +170,8 @@ enum {
     FLCE_K_SIMT_GEMM = 9,        /* fp32 path: CUDA-core GEMMs                         */
     FLCE_K_SIMT_TILE_STATS = 10, /* fp32 path: per-vocab-tile max/sum-exp              */
     FLCE_K_GEMM_DX_DW = 11,      /* CTA pairs: the dx and dW GEMMs of a chunk in one launch */
-    FLCE_K_DEVICE_RESULT = 12,   /* loss and n_valid into caller device memory         */
+    FLCE_K_DEVICE_RESULT = 12,   /* loss and n_valid into caller device memory (an
+                                    empty batch; otherwise the loss reduction writes them) */
     FLCE_K_NUM_KINDS = 13
 };
 

@@ -852,12 +852,20 @@ flce_status slab_backward(flce_handle_t h, const SlabChunk& k, cudaStream_t s, b
 
 // Everything of one call up to its control words on the device (*ctrl_out):
 // the result is read from them once the stream gets there.
+// The sync-free entry points' result in caller device memory (either may be
+// null): the loss (NaN after a recorded error) and n_valid.
+struct DeviceResult {
+  float* loss = nullptr;
+  int32_t* n_valid = nullptr;
+};
+
 // nv_total: the divisor of a token-sharded batch (device, one int32), or
-// null to divide by this call's own n_valid.
+// null to divide by this call's own n_valid. dres: where the loss reduction
+// also writes the device result, or null.
 flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int64_t* t, int64_t N,
                        int64_t H, int64_t V, int64_t ignore_index, int64_t chunk, void* dx,
                        float* dW, cudaStream_t s, uint32_t** ctrl_out,
-                       const int32_t* nv_total = nullptr) {
+                       const int32_t* nv_total = nullptr, const DeviceResult* dres = nullptr) {
   NvtxRange nvtx_call("flce_forward_backward");
   if (!W || !dW || (N > 0 && (!x || !t || !dx)))
     return fail(h, FLCE_ERR_INVALID_ARG, "null pointer argument");
@@ -901,6 +909,8 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
   if (N == 0) {
     e = cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * 4, s);
     if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+    if (dres)
+      FLCE_LAUNCH(FLCE_K_DEVICE_RESULT, 0.0, 16.0, launch_device_result(ctrl, dres->loss, dres->n_valid, s));
     *ctrl_out = ctrl;
     return FLCE_OK;
   }
@@ -1131,13 +1141,16 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
                                    t + off, ignore_index, ctrl, dcorr, dxb + off * H, s));
     }
   }
-  FLCE_LAUNCH(FLCE_K_LOSS_FINALIZE, 0.0, 4.0 * N, launch_loss_finalize(token_loss, N, ctrl, s));
   if (side_pending) {
-    // the call ends on its stream only once the side stream's dW GEMMs are done
+    // the call ends on its stream only once the side stream's dW GEMMs are
+    // done; the loss reduction below reads the error word they may have set
     side_pending = false;
     e = cudaStreamWaitEvent(s, h->slab_freed, 0);
     if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab join: %s", cudaGetErrorString(e));
   }
+  FLCE_LAUNCH(FLCE_K_LOSS_FINALIZE, 0.0, 4.0 * N,
+              launch_loss_finalize(token_loss, N, ctrl, dres ? 1 : 0, dres ? dres->loss : nullptr,
+                                   dres ? dres->n_valid : nullptr, s));
   *ctrl_out = ctrl;
   return FLCE_OK;
 }
@@ -1315,10 +1328,10 @@ flce_status flce_forward_backward_async(flce_handle_t h, const void* x, const vo
   DeviceGuard g(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t* ctrl = nullptr;
-  const flce_status st = enqueue_fb(h, x, W, t, N, H, V, ignore_index, chunk, dx, dW, s, &ctrl);
-  if (st != FLCE_OK) return st;
-  FLCE_LAUNCH(FLCE_K_DEVICE_RESULT, 0.0, 16.0, launch_device_result(ctrl, loss_dev, n_valid_dev, s));
-  return FLCE_OK;
+  DeviceResult dres;
+  dres.loss = loss_dev;
+  dres.n_valid = n_valid_dev;
+  return enqueue_fb(h, x, W, t, N, H, V, ignore_index, chunk, dx, dW, s, &ctrl, nullptr, &dres);
 }
 
 flce_status flce_async_status(flce_handle_t h, void* stream) {
@@ -1364,11 +1377,10 @@ flce_status flce_forward_backward_shard(flce_handle_t h, const void* x, const vo
   DeviceGuard g(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t* ctrl = nullptr;
-  const flce_status st =
-      enqueue_fb(h, x, W, t, N, H, V, ignore_index, chunk, dx, dW, s, &ctrl, n_valid_total_dev);
-  if (st != FLCE_OK) return st;
-  FLCE_LAUNCH(FLCE_K_DEVICE_RESULT, 0.0, 16.0, launch_device_result(ctrl, loss_dev, nullptr, s));
-  return FLCE_OK;
+  DeviceResult dres;
+  dres.loss = loss_dev;
+  return enqueue_fb(h, x, W, t, N, H, V, ignore_index, chunk, dx, dW, s, &ctrl, n_valid_total_dev,
+                    &dres);
 }
 
 flce_status flce_forward_backward_host(flce_handle_t h, const void* x_host, const void* W_host,

@@ -126,8 +126,10 @@ cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_st
                              int64_t ignore_index, const uint32_t* ctrl, const float* dcorr,
                              __nv_bfloat16* dx, cudaStream_t s);
 cudaError_t launch_device_result(uint32_t* ctrl, float* loss_dev, int32_t* n_valid_dev, cudaStream_t s);
-cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* ctrl,
-                                 cudaStream_t s);
+// result != 0: also write the sync-free entry points' device result (loss,
+// NaN after a recorded error; n_valid; the sticky error word)
+cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* ctrl, int result,
+                                 float* loss_dev, int32_t* n_valid_dev, cudaStream_t s);
 
 // flce_simt.cu (fp32 path)
 // C (+)= A·B over K with strided operands. splits > 1 with part != null

@@ -120,7 +120,17 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partials, int voca
   if (r >= rows) return;
   const float2* p = partials + static_cast<size_t>(r) * vocab_tiles;
   float M = -INFINITY, S = 0.f;
-  for (int s = lane; s < vocab_tiles; s += 32) {
+  // a lane takes partials lane, lane + 32, ... in blocks of four loads in
+  // flight (the row's partials are one contiguous run)
+  int s = lane;
+  for (; s + 96 < vocab_tiles; s += 128) {
+    float2 q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = p[s + 32 * j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) lse_merge(M, S, q[j].x, q[j].y);
+  }
+  for (; s < vocab_tiles; s += 32) {
     const float2 q = p[s];
     lse_merge(M, S, q.x, q.y);
   }
@@ -275,12 +285,21 @@ __global__ void dx_reduce_kernel(const float* __restrict__ part, int splits, int
   const bool corr = tg != ignore_index && tg >= 0 && tg < V && ctrl[kCtrlNValid] > 0;
   const int64_t i = static_cast<int64_t>(r) * H + h;
   float4 acc = *reinterpret_cast<const float4*>(part + i);
-  for (int s = 1; s < splits; ++s) {
-    const float4 v = *reinterpret_cast<const float4*>(part + s * split_stride + i);
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
+  // up to eight splits' loads in flight, then added in split order
+  for (int s0 = 1; s0 < splits; s0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (s0 + j < splits) v[j] = *reinterpret_cast<const float4*>(part + (s0 + j) * split_stride + i);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (s0 + j < splits) {
+        acc.x += v[j].x;
+        acc.y += v[j].y;
+        acc.z += v[j].z;
+        acc.w += v[j].w;
+      }
+    }
   }
   if (corr) {
     const float c = dcorr[r];
@@ -300,22 +319,35 @@ __global__ void dx_reduce_kernel(const float* __restrict__ part, int splits, int
   *reinterpret_cast<uint2*>(dx + i) = o;
 }
 
-// loss = (sum of token losses) / n_valid, the sum in float64 and fixed order
-__global__ void loss_finalize_kernel(const float* __restrict__ token_loss, int64_t N,
-                                     uint32_t* ctrl) {
-  __shared__ double part[1024];
+// loss = (sum of token losses) / n_valid, the sum in float64 and fixed order:
+// each thread sums a fixed strided set, then warp shuffles and one warp merge
+// the partial sums in a fixed tree. With `result` set it also writes the
+// device result of the sync-free entry points (as device_result_kernel).
+__global__ void __launch_bounds__(1024) loss_finalize_kernel(const float* __restrict__ token_loss,
+                                                             int64_t N, uint32_t* ctrl, int result,
+                                                             float* loss_dev, int32_t* n_valid_dev) {
+  __shared__ double warp_sum[32];
   double s = 0.0;
   for (int64_t i = threadIdx.x; i < N; i += blockDim.x) s += static_cast<double>(token_loss[i]);
-  part[threadIdx.x] = s;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = s;
   __syncthreads();
-  for (int w = blockDim.x >> 1; w > 0; w >>= 1) {
-    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    const uint32_t nv = ctrl[kCtrlNValid];
-    const float loss = nv > 0 ? static_cast<float>(part[0] / static_cast<double>(nv)) : 0.f;
-    ctrl[kCtrlLoss] = __float_as_uint(loss);
+  if (threadIdx.x < 32) {
+    double w = threadIdx.x < (blockDim.x >> 5) ? warp_sum[threadIdx.x] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w += __shfl_down_sync(0xffffffffu, w, o);
+    if (threadIdx.x == 0) {
+      const uint32_t nv = ctrl[kCtrlNValid];
+      const float loss = nv > 0 ? static_cast<float>(w / static_cast<double>(nv)) : 0.f;
+      ctrl[kCtrlLoss] = __float_as_uint(loss);
+      if (result) {
+        const uint32_t err = ctrl[kCtrlError];
+        if (loss_dev) *loss_dev = err ? __uint_as_float(0x7fc00000u) : loss;
+        if (n_valid_dev) *n_valid_dev = static_cast<int32_t>(nv);
+        if (err && ctrl[kCtrlSticky] == 0u) ctrl[kCtrlSticky] = err;
+      }
+    }
   }
 }
 
@@ -388,9 +420,9 @@ cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_st
   return cudaGetLastError();
 }
 
-cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* ctrl,
-                                 cudaStream_t s) {
-  loss_finalize_kernel<<<1, 1024, 0, s>>>(token_loss, N, ctrl);
+cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* ctrl, int result,
+                                 float* loss_dev, int32_t* n_valid_dev, cudaStream_t s) {
+  loss_finalize_kernel<<<1, 1024, 0, s>>>(token_loss, N, ctrl, result, loss_dev, n_valid_dev);
   return cudaGetLastError();
 }
 

@@ -153,7 +153,8 @@ extern "C" flce_status flce_loss_static(const void* x, const void* W, const int6
                              token_loss + off, s) != cudaSuccess)
         return FLCE_ERR_CUDA;
     }
-    if (launch_loss_finalize(token_loss, N, ctrl, s) != cudaSuccess) return FLCE_ERR_CUDA;
+    if (launch_loss_finalize(token_loss, N, ctrl, 0, nullptr, nullptr, s) != cudaSuccess)
+      return FLCE_ERR_CUDA;
   }
   uint32_t host_ctrl[4] = {0, 0, 0, 0};
   if (cudaMemcpyAsync(host_ctrl, ctrl, sizeof host_ctrl, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
