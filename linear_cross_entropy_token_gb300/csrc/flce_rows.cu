@@ -90,11 +90,11 @@ __global__ void count_only_kernel(const int64_t* __restrict__ t, int64_t N, int6
   }
 }
 
-// One warp per token row: lse = M + log sum_s l_s exp(m_s - M) over the vocab
-// tiles' (m_s, l_s); token loss = lse - z_t (0 for an ignored token). One
-// pass over the partials: each lane keeps a running (max, sum) and rescales
-// its sum when the max grows; the lanes' pairs then merge the same way, in a
-// fixed order.
+// Per token row: lse = M + log sum_s l_s exp(m_s - M) over the vocab tiles'
+// (m_s, l_s); token loss = lse - z_t (0 for an ignored token). One pass over
+// the partials: each thread keeps a running (max, sum) and rescales its sum
+// when the max grows; the threads' pairs then merge the same way, in a fixed
+// order.
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
   if (m2 == -INFINITY) return;
   if (m == -INFINITY) {
@@ -110,27 +110,29 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   }
 }
 
-__global__ void lse_combine_kernel(const float2* __restrict__ partials, int vocab_tiles,
-                                   const float* __restrict__ zt, const int64_t* __restrict__ t,
-                                   int rows, int64_t ignore_index, float* __restrict__ lse,
-                                   float* __restrict__ token_loss) {
-  const int warps = blockDim.x >> 5;
-  const int r = blockIdx.x * warps + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
+constexpr int kCombineThreads = 128;
+
+// One block of kCombineThreads per token row: each thread merges a strided
+// share of the row's partials (four loads in flight), then the warps and the
+// block merge their pairs in a fixed order.
+__global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(
+    const float2* __restrict__ partials, int vocab_tiles, const float* __restrict__ zt,
+    const int64_t* __restrict__ t, int rows, int64_t ignore_index, float* __restrict__ lse,
+    float* __restrict__ token_loss) {
+  __shared__ float2 warp_ms[kCombineThreads / 32];
+  const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float2* p = partials + static_cast<size_t>(r) * vocab_tiles;
   float M = -INFINITY, S = 0.f;
-  // a lane takes partials lane, lane + 32, ... in blocks of four loads in
-  // flight (the row's partials are one contiguous run)
-  int s = lane;
-  for (; s + 96 < vocab_tiles; s += 128) {
+  int s = threadIdx.x;
+  for (; s + 3 * kCombineThreads < vocab_tiles; s += 4 * kCombineThreads) {
     float2 q[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) q[j] = p[s + 32 * j];
+    for (int j = 0; j < 4; ++j) q[j] = p[s + j * kCombineThreads];
 #pragma unroll
     for (int j = 0; j < 4; ++j) lse_merge(M, S, q[j].x, q[j].y);
   }
-  for (; s < vocab_tiles; s += 32) {
+  for (; s < vocab_tiles; s += kCombineThreads) {
     const float2 q = p[s];
     lse_merge(M, S, q.x, q.y);
   }
@@ -140,7 +142,13 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partials, int voca
     const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
     lse_merge(M, S, m2, s2);
   }
-  if (lane == 0) {
+  if (lane == 0) warp_ms[warp] = make_float2(M, S);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    M = warp_ms[0].x;
+    S = warp_ms[0].y;
+#pragma unroll
+    for (int w = 1; w < kCombineThreads / 32; ++w) lse_merge(M, S, warp_ms[w].x, warp_ms[w].y);
     const float l = M + logf(S);
     lse[r] = l;
     const int64_t tg = t[r];
@@ -285,21 +293,12 @@ __global__ void dx_reduce_kernel(const float* __restrict__ part, int splits, int
   const bool corr = tg != ignore_index && tg >= 0 && tg < V && ctrl[kCtrlNValid] > 0;
   const int64_t i = static_cast<int64_t>(r) * H + h;
   float4 acc = *reinterpret_cast<const float4*>(part + i);
-  // up to eight splits' loads in flight, then added in split order
-  for (int s0 = 1; s0 < splits; s0 += 8) {
-    float4 v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (s0 + j < splits) v[j] = *reinterpret_cast<const float4*>(part + (s0 + j) * split_stride + i);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (s0 + j < splits) {
-        acc.x += v[j].x;
-        acc.y += v[j].y;
-        acc.z += v[j].z;
-        acc.w += v[j].w;
-      }
-    }
+  for (int s = 1; s < splits; ++s) {
+    const float4 v = *reinterpret_cast<const float4*>(part + s * split_stride + i);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
   }
   if (corr) {
     const float c = dcorr[r];
@@ -383,9 +382,9 @@ cudaError_t launch_count_only(const int64_t* t, int64_t N, int64_t ignore_index,
 cudaError_t launch_lse_combine(const float2* partials, int vocab_tiles, const float* zt,
                                const int64_t* t_chunk, int rows, int64_t ignore_index, float* lse,
                                float* token_loss_chunk, cudaStream_t s) {
-  const int warps = 8;
-  lse_combine_kernel<<<(rows + warps - 1) / warps, warps * 32, 0, s>>>(
-      partials, vocab_tiles, zt, t_chunk, rows, ignore_index, lse, token_loss_chunk);
+  if (rows <= 0) return cudaSuccess;
+  lse_combine_kernel<<<rows, kCombineThreads, 0, s>>>(partials, vocab_tiles, zt, t_chunk, rows,
+                                                      ignore_index, lse, token_loss_chunk);
   return cudaGetLastError();
 }
 
