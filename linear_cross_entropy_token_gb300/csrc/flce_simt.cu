@@ -119,8 +119,17 @@ __global__ void __launch_bounds__(256) simt_splitk_reduce_kernel(
   const int64_t MN = M * N;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < MN;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    // eight splits' loads in flight at a time, added in split order
     float v = part[e];
-    for (int s = 1; s < splits; ++s) v += part[s * MN + e];
+    int s = 1;
+    for (; s + 8 <= splits; s += 8) {
+      float q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) q[j] = part[(s + j) * MN + e];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v += q[j];
+    }
+    for (; s < splits; ++s) v += part[s * MN + e];
     const int64_t m = e / N, n = e - m * N;
     float* c = C + m * ldc + n;
     *c = accumulate ? (*c + v) : v;

@@ -8,7 +8,9 @@
       utilisation, warp stalls (from `ncu -i <rep> --page raw --csv
       --print-units base`)
   python -m linear_cross_entropy_token_gb300.ncu_summary traffic <report.ncu-rep>
-      DRAM bytes per launch per kernel kind, as JSON
+        [--workload NAME --chunk C --chunks K]
+      DRAM bytes per launch per kernel kind, as JSON (K: chunks of the call
+      whose first launches were captured; weights dW's store against its adds)
 """
 from __future__ import annotations
 
@@ -27,6 +29,7 @@ _PLAIN = {"count_valid_kernel": "count_valid", "lse_combine_kernel": "lse_combin
           "dlogits_bf16_kernel": "dlogits_inplace", "dlogits_f32_kernel": "dlogits_inplace_f32",
           "dx_reduce_kernel": "dx_split_reduce", "loss_finalize_kernel": "loss_finalize",
           "simt_gemm_f32_kernel": "simt_gemm_f32", "simt_tile_stats_kernel": "simt_tile_stats_f32",
+          "simt_splitk_reduce_kernel": "simt_splitk_reduce_f32",
           "wait_check_kernel": "wait_check", "umma_pair_dual_kernel": "gemm_dx_dw",
           "device_result_kernel": "device_result"}
 
@@ -99,15 +102,24 @@ def raw(rep_path: str):
     return res
 
 
-def traffic(rep_path: str):
+def traffic(rep_path: str, chunks: int = 0):
+    """DRAM bytes per launch per kernel kind. With chunks = K > 0 the capture
+    holds the first chunks of one call: the dW GEMM's first launch stores dW
+    and its later ones add into it, so its per-launch figure is the mean over
+    a K-chunk call, (first + (K - 1) x mean of the others) / K."""
     per = collections.OrderedDict()
     for d in raw(rep_path):
         if d.get("dram_read_MB") is None:
             continue
-        a = per.setdefault(d["kernel"], [0, 0.0])
-        a[0] += 1
-        a[1] += (d["dram_read_MB"] + d["dram_write_MB"]) * 1e6
-    return {k: {"launches": n, "dram_bytes_per_launch": b / n} for k, (n, b) in per.items()}
+        per.setdefault(d["kernel"], []).append((d["dram_read_MB"] + d["dram_write_MB"]) * 1e6)
+    out = {}
+    for k, v in per.items():
+        if chunks > 0 and k == "gemm_dw" and len(v) > 1:
+            per_launch = (v[0] + (chunks - 1) * sum(v[1:]) / len(v[1:])) / chunks
+        else:
+            per_launch = sum(v) / len(v)
+        out[k] = {"launches": len(v), "dram_bytes_per_launch": per_launch}
+    return out
 
 
 def _md_table(header, rows) -> str:
@@ -135,7 +147,8 @@ def main(argv=None):
         opts = dict(zip(argv[2::2], argv[3::2]))
         from .build import source_hash
         out = {"workload": opts.get("--workload"), "chunk": int(opts.get("--chunk", 0)),
-               "source_hash": source_hash(), "kernels": traffic(path)}
+               "source_hash": source_hash(),
+               "kernels": traffic(path, int(opts.get("--chunks", 0)))}
         print(json.dumps(out, indent=1))
     else:
         print(__doc__)
