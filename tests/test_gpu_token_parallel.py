@@ -61,6 +61,27 @@ def test_shards_sum_to_the_whole_batch(dtype, N, H, V, ign, chunk, k):
     assert rel_fro(dW.cpu().numpy(), ref.dW) <= GRAD_RTOL[dtype]
 
 
+@pytest.mark.parametrize("mode,budget", [("slabs", 4 << 20), ("recompute", 48 << 20)])
+def test_shards_in_the_other_dlogits_modes(mode, budget):
+    """The batch's divisor reaches the dlogits epilogue of the recomputing
+    GEMM too (slab walk: several slabs per chunk)."""
+    from linear_cross_entropy_token_gb300 import FLCE
+    w = workloads.generate(workloads.custom(900, 128, 20011, "bf16", ignore_frac=0.1, seed=31))
+    x, W, t = device_inputs(w)
+    h = FLCE("bf16", 0, dlogits_mode=mode, hbm_budget_bytes=budget)   # slabs: four of 6656
+    try:
+        loss, dx, dW, counts, total = _sharded(h, x, W, t, _shards(900, 2), chunk=256)
+        if mode == "slabs":
+            assert h.last_plan()["vocab_slab"] < w.V
+    finally:
+        h.close()
+    ref = oracle.flce_reference(w.x_f64(), w.W_f64(), w.t, w.ignore_index)
+    assert total == ref.n_valid
+    assert abs(loss - ref.loss) / ref.loss <= LOSS_RTOL
+    assert rel_fro(to_np64(dx), ref.dx) <= 1e-2
+    assert rel_fro(dW.cpu().numpy(), ref.dW) <= 1e-2
+
+
 def test_shard_with_every_token_ignored():
     """A shard with no valid token adds nothing but still counts; a batch
     with none at all gives zeros."""
