@@ -186,9 +186,10 @@ def kernel_source_hash() -> str:
     return source_hash()
 
 
-def traffic_for(kernel: str, workload: str, chunk: int):
+def traffic_for(kernel: str, workload: str, chunk: int, dlogits: str):
     """DRAM bytes per launch of a kernel from the committed ncu summary, or
-    None if there is none for this workload or the kernels changed since."""
+    None if there is none for this workload, chunk and dlogits mode, or the
+    kernels changed since."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
@@ -196,7 +197,8 @@ def traffic_for(kernel: str, workload: str, chunk: int):
     if d.get("source_hash") != kernel_source_hash():
         return None
     k = d.get("kernels", {}).get(kernel)
-    if not k or d.get("workload") != workload or d.get("chunk") != chunk:
+    if (not k or d.get("workload") != workload or d.get("chunk") != chunk
+            or d.get("dlogits", "inplace") != dlogits):
         return None
     return k.get("dram_bytes_per_launch")
 
@@ -424,7 +426,7 @@ def run_ours(args, ws, rank, local):
         roof = {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
                 "peak_sustained": sustained, "frac_sustained": achieved / sustained}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_for(name, args.config, plan["chunk"])
+    roof["traffic"] = traffic_for(name, args.config, plan["chunk"], plan["dlogits"])
     roof["kernel"] = name
     roof["timing"] = ("per-launch CUDA events on each kernel's stream over a second run of the "
                       "timed steps (the headline run records none)")

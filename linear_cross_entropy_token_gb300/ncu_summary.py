@@ -8,7 +8,7 @@
       utilisation, warp stalls (from `ncu -i <rep> --page raw --csv
       --print-units base`)
   python -m linear_cross_entropy_token_gb300.ncu_summary traffic <report.ncu-rep>
-        [--workload NAME --chunk C --chunks K]
+        [--workload NAME --chunk C --chunks K --dlogits MODE]
       DRAM bytes per launch per kernel kind, as JSON (K: chunks of the call
       whose first launches were captured; weights dW's store against its adds)
 """
@@ -147,6 +147,7 @@ def main(argv=None):
         opts = dict(zip(argv[2::2], argv[3::2]))
         from .build import source_hash
         out = {"workload": opts.get("--workload"), "chunk": int(opts.get("--chunk", 0)),
+               "dlogits": opts.get("--dlogits", "inplace"),
                "source_hash": source_hash(),
                "kernels": traffic(path, int(opts.get("--chunks", 0)))}
         print(json.dumps(out, indent=1))
