@@ -49,6 +49,13 @@ constexpr int64_t kMinSlab = 8192;
 constexpr int64_t kSlabMaxChunk = 4096;
 constexpr int64_t kMaxDim = (1ll << 31) - 1;
 constexpr uint64_t kAlign = 1024;
+// in-place and recompute modes run the dW GEMM beside the dx GEMM on a second
+// stream when the dx launch has fewer work units than this many waves of CTA
+// pairs (small problems, where dx leaves SMs idle)
+#ifndef FLCE_OVERLAP_WAVES
+#define FLCE_OVERLAP_WAVES 2
+#endif
+constexpr int kOverlapWaves = FLCE_OVERLAP_WAVES;
 
 uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -768,14 +775,22 @@ struct SlabChunk {
   int b_box;                    // rows of a K-major B box for the handle's tile shape
 };
 
+// The handle's second stream and its two events (created on first use).
+flce_status ensure_side_stream(flce_handle_t h) {
+  if (h->side_stream) return FLCE_OK;
+  cudaError_t e = cudaStreamCreateWithFlags(&h->side_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slab_ready, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slab_freed, cudaEventDisableTiming);
+  if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
+  return FLCE_OK;
+}
+
 flce_status slab_backward(flce_handle_t h, const SlabChunk& k, cudaStream_t s, bool* side_pending) {
   std::string why;
   cudaError_t e = cudaSuccess;
-  if (!h->side_stream) {
-    e = cudaStreamCreateWithFlags(&h->side_stream, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slab_ready, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->slab_freed, cudaEventDisableTiming);
-    if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
+  {
+    const flce_status st = ensure_side_stream(h);
+    if (st != FLCE_OK) return st;
   }
   const cudaStream_t side = h->side_stream;
   const int64_t H = k.H, V = k.V, Vs = k.plan->vocab_slab, ldv = k.plan->ldv;
@@ -1032,6 +1047,12 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
           !map_bf16_2d(&mZ_mn, logits, zw, rows, ldv * 2, 64, 64, &why))
         return fail(h, FLCE_ERR_INVALID_ARG, "%s", why.c_str());
 
+      // the previous chunk's dW GEMM, if it ran on the side stream, must have
+      // read the buffer before this chunk's logits GEMM overwrites it
+      if (side_pending && !slabs) {
+        e = cudaStreamWaitEvent(s, h->slab_freed, 0);
+        if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "dW wait: %s", cudaGetErrorString(e));
+      }
       // 1. projection with the online max / sum-exp epilogue
       UmmaArgs a{};
       a.num_n = static_cast<int>(cdiv(V, kBN));
@@ -1102,6 +1123,14 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       d.rows = static_cast<int>(V);
       d.cols = static_cast<int>(H);
       d.reduce_add = c > 0 ? 1 : 0;
+      // dW beside dx when the dx launch is short of kOverlapWaves waves
+      const int64_t dx_units = cdiv(rows, 2 * kBM) * cdiv(H, p.tile_n_dx) * S;
+      const bool overlap_dw = h->shape != kShapeSingle &&
+                              dx_units < static_cast<int64_t>(kOverlapWaves) * (h->num_sms / 2);
+      if (overlap_dw) {
+        st = ensure_side_stream(h);
+        if (st != FLCE_OK) return st;
+      }
       const double dx_bytes = 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH;
       const double dw_bytes = 2 * dr * dV + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dV * dH;
       if (h->shape == kShapePair && h->cfg.cta_pair == FLCE_CTA_PAIR &&
@@ -1130,6 +1159,24 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
         const int units = da.units0 + da.p[1].num_m * da.p[1].num_n;
         FLCE_LAUNCH(FLCE_K_GEMM_DX_DW, 4 * dr * dV * dH, dx_bytes + dw_bytes,
                     launch_umma_pair_dual(maps, da, std::min(units, h->pair_clusters), s));
+      } else if (overlap_dw) {
+        // the dx GEMM fills less than kOverlapWaves waves of the GPU: the dW
+        // GEMM runs beside it on the side stream (both only read the finished
+        // buffer); the next chunk's logits GEMM waits for it before it
+        // overwrites the buffer, and the call's end joins the side stream
+        e = cudaEventRecord(h->slab_ready, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->side_stream, h->slab_ready, 0);
+        if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "dW fork: %s", cudaGetErrorString(e));
+        {
+          const cudaStream_t s = h->side_stream;  // the launch and its timing events go there
+          FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dV * dH, dw_bytes,
+                      launch_gemm(h, shape_for(h, p.tile_n_dw), kUmmaDw, mZ_mn, mX_mn, mDw, d, V, s));
+        }
+        e = cudaEventRecord(h->slab_freed, h->side_stream);
+        if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "dW join: %s", cudaGetErrorString(e));
+        side_pending = true;
+        FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, dx_bytes,
+                    launch_gemm(h, shape_for(h, p.tile_n_dx), kUmmaDxF32, mZ_k, mW_mn, mDx, b, rows, s));
       } else {
         FLCE_LAUNCH(FLCE_K_GEMM_DX, 2 * dr * dV * dH, dx_bytes,
                     launch_gemm(h, shape_for(h, p.tile_n_dx), kUmmaDxF32, mZ_k, mW_mn, mDx, b, rows, s));
