@@ -154,6 +154,10 @@ typedef struct flce_plan {
                                     on fp32 handles, RECOMPUTE resolved to INPLACE)     */
     int64_t tile_n_dx;           /* columns of the dx GEMM's output tile (256 or 512)  */
     int64_t tile_n_dw;           /* columns of the dW GEMM's output tile (256 or 512)  */
+    int64_t dw_beside_dx;        /* 1: the dW GEMM runs beside the dx GEMM on the
+                                    handle's second stream (in-place and recompute
+                                    modes on CTA pairs, when the dx launch fills less
+                                    than two waves of SM pairs); 0: one after the other */
 } flce_plan;
 
 /* Kernel kinds, for the per-kernel timing of flce_profile_read(). */

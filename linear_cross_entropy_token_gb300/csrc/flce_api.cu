@@ -426,6 +426,17 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
     out->tile_n_dx = cols(dx_choice(C).shape);
     out->tile_n_dw = cols(pick_shape(V, H, C, false, slots));
   }
+  // in-place and recompute modes on CTA pairs: the dW GEMM runs beside a dx
+  // launch that fills less than kOverlapWaves waves (the one-launch pair
+  // backward, when asked for, takes precedence)
+  if (bf16 && !slabs && C > 0 && group == 2 &&
+      !(cfg->cta_pair == FLCE_CTA_PAIR && cfg->backward_launch == FLCE_BACKWARD_ONE_LAUNCH)) {
+    const int64_t kb = cdiv(V, kBK);
+    const int64_t kbps = cdiv(kb, std::max<int64_t>(out->dx_splits, 1));
+    const int64_t S = cdiv(kb, kbps);
+    const int64_t dx_units = cdiv(C, 2 * kBM) * cdiv(H, out->tile_n_dx) * S;
+    out->dw_beside_dx = dx_units < static_cast<int64_t>(kOverlapWaves) * slots ? 1 : 0;
+  }
   // fp32 handles run SLABS as asked and every other mode in place
   out->dlogits_mode = slabs ? FLCE_DLOGITS_SLABS
                       : (bf16 && cfg->dlogits_mode == FLCE_DLOGITS_RECOMPUTE) ? FLCE_DLOGITS_RECOMPUTE
@@ -1123,10 +1134,9 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       d.rows = static_cast<int>(V);
       d.cols = static_cast<int>(H);
       d.reduce_add = c > 0 ? 1 : 0;
-      // dW beside dx when the dx launch is short of kOverlapWaves waves
-      const int64_t dx_units = cdiv(rows, 2 * kBM) * cdiv(H, p.tile_n_dx) * S;
-      const bool overlap_dw = h->shape != kShapeSingle &&
-                              dx_units < static_cast<int64_t>(kOverlapWaves) * (h->num_sms / 2);
+      // dW beside dx when the plan says so (the dx launch is short of
+      // kOverlapWaves waves)
+      const bool overlap_dw = p.dw_beside_dx != 0;
       if (overlap_dw) {
         st = ensure_side_stream(h);
         if (st != FLCE_OK) return st;

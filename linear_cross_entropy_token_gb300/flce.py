@@ -51,7 +51,7 @@ class Plan(ctypes.Structure):
                 ("logits_bytes", ctypes.c_uint64), ("tile_m", ctypes.c_int64),
                 ("tile_n", ctypes.c_int64), ("vocab_slab", ctypes.c_int64),
                 ("dlogits_mode", ctypes.c_int64), ("tile_n_dx", ctypes.c_int64),
-                ("tile_n_dw", ctypes.c_int64)]
+                ("tile_n_dw", ctypes.c_int64), ("dw_beside_dx", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         d = {k: getattr(self, k) for k, _ in self._fields_}

@@ -225,3 +225,8 @@ def test_plan_picks_tile_shapes_per_gemm():
     # the slab walk keeps the wide tiles its slab sizing assumes
     s = flce.plan(16384, 4096, 128256, dlogits_mode="slabs")
     assert (s["tile_n"], s["tile_n_dx"], s["tile_n_dw"]) == (512, 512, 512)
+    # the 64-unit dx launch of the small shape runs with dW beside it; the
+    # 512-unit one of the Llama-3 shape does not; single-CTA tiles never do
+    assert p["dw_beside_dx"] == 1
+    assert flce.plan(16384, 4096, 128256)["dw_beside_dx"] == 0
+    assert flce.plan(2048, 1024, 32000, cta="single")["dw_beside_dx"] == 0
