@@ -310,10 +310,11 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
     }
     return best_t[1] < kPairMargin * best_t[0] ? best[1] : best[0];
   };
-  // SLABS accumulate dx over the slabs in one fp32 buffer (one split)
-  // fp32: the CUDA-core dx GEMM splits its V reduction when its C x H output
-  // has too few tiles to fill the SMs (the count for the full V bounds that of
-  // any slab)
+  // splits of the dx GEMM's V reduction. fp32: the CUDA-core dx GEMM splits
+  // when its C x H output has too few tiles to fill the SMs (the count for the
+  // full V bounds that of any slab). bf16: the mixed plan's choice, one split
+  // for SLABS (dx accumulates over the slabs in one fp32 buffer), else the
+  // count that fills the waves of the handle's tile shape.
   auto splits_for = [&](int64_t C) -> int64_t {
     if (!bf16) {
       // the partials take at most an eighth of the budget
@@ -494,6 +495,9 @@ struct flce_handle_s {
   int64_t launches = 0;
   Profiler prof;
   std::map<std::array<int, 5>, int> group_cache;  // pick_group_m by (shape, num_m, num_n, num_s, slots)
+  // the plan of the last sizes planned (a training loop repeats them)
+  std::array<int64_t, 4> plan_key{-1, -1, -1, -1};
+  flce_plan plan_cached{};
 };
 
 namespace {
@@ -907,9 +911,17 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     return fail(h, FLCE_ERR_INVALID_ARG, "x, W, dx and dW must be 4-byte aligned");
   }
   flce_plan p;
+  flce_status st = FLCE_OK;
   std::string why;
-  flce_status st = plan_impl(&h->cfg, N, H, V, chunk, h->num_sms, &p, &why);
-  if (st != FLCE_OK) return fail(h, st, "%s", why.c_str());
+  const std::array<int64_t, 4> key{N, H, V, chunk};
+  if (key == h->plan_key) {
+    p = h->plan_cached;
+  } else {
+    st = plan_impl(&h->cfg, N, H, V, chunk, h->num_sms, &p, &why);
+    if (st != FLCE_OK) return fail(h, st, "%s", why.c_str());
+    h->plan_key = key;
+    h->plan_cached = p;
+  }
   st = ensure_workspace(h, p.workspace_bytes);
   if (st != FLCE_OK) return st;
   // the same split count the plan sized the workspace with (fp32 plans
