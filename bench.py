@@ -52,6 +52,10 @@ def parse():
                         "or CTA pairs per 256x512 sharing A (wide)")
     p.add_argument("--backward", choices=["auto", "separate", "one_launch"], default="auto",
                    help="dx and dW GEMMs of a chunk in two launches or one (CTA pairs)")
+    p.add_argument("--token-parallel", action="store_true",
+                   help="shard the batch's tokens over the ranks (NEXT-3): each step all-reduces "
+                        "the non-ignored token count, then dW and the loss; strong scaling. "
+                        "Default: independent replicas")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -528,11 +532,134 @@ def run_ours(args, ws, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def aggregate_sharded(ws, batch_tokens: int, ms_local: float, device=None):
+    """Whole-job throughput of one token-sharded batch: the batch's tokens
+    once, over the slowest rank's time."""
+    ms_max = max_over_ranks(ws, ms_local, device)
+    return ms_max, batch_tokens / (ms_max / 1e3)
+
+
+def run_token_parallel(args, ws, rank, local):
+    """--token-parallel: one batch split by tokens over the ranks; every step
+    is the token_parallel wrapper's count all-reduce, the rank's fused call
+    with the batch's divisor, and the all-reduces of dW and the loss."""
+    import socket
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+    from linear_cross_entropy_token_gb300 import FLCE
+    from linear_cross_entropy_token_gb300.token_parallel import (shard_bounds,
+                                                                 token_parallel_forward_backward)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    own_group = not dist.is_initialized()
+    if own_group:   # one process: the collectives run over a one-rank NCCL group
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                                device_id=dev)
+    w = workloads.make(args.config)
+    if args.chunk == 0 and w.spec.chunk:
+        args.chunk = w.spec.chunk
+    a, b = shard_bounds(w.N, ws, rank)
+    bf16 = w.x.dtype == np.uint16
+    xs = w.x[a:b]
+    if bf16:
+        x = torch.from_numpy(np.ascontiguousarray(xs).view(np.int16)).view(torch.bfloat16).to(dev)
+        W = torch.from_numpy(w.W.view(np.int16)).view(torch.bfloat16).to(dev)
+    else:
+        x = torch.from_numpy(np.ascontiguousarray(xs)).to(dev)
+        W = torch.from_numpy(w.W).to(dev)
+    t = torch.from_numpy(np.ascontiguousarray(w.t[a:b])).to(dev)
+    dx = torch.empty_like(x)
+    dW = torch.empty((w.V, w.H), dtype=torch.float32, device=dev)
+    h = FLCE("bf16" if bf16 else "fp32", local, hbm_budget_bytes=int(args.budget_gib * (1 << 30)),
+             dlogits_mode=args.dlogits, cta=args.cta, backward=args.backward)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return token_parallel_forward_backward(h, x, W, t, chunk=args.chunk, dx=dx, dW=dW)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    h.async_status()
+    plan = h.last_plan()
+
+    def timed():
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            loss = step()[0]
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(ws)
+        return e0.elapsed_time(e1) / args.steps, loss
+
+    launches0 = h.launch_count()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms, loss = timed()
+    clk = clocks.stop()
+    h.async_status()
+    launches = h.launch_count() - launches0
+    h.set_profiling(True)
+    h.profile_reset()
+    ms_events, _ = timed()
+    prof = h.profile()
+    h.set_profiling(False)
+    ms_max, value = aggregate_sharded(ws, w.N, ms, dev)
+    flops = 6.0 * w.N * w.H * w.V
+    tflops = flops / (ms_max / 1e3) / 1e12
+    peaks, peaks_kind = load_peaks()
+    name, pk = max(((k, v) for k, v in prof.items() if k != "gemm_dw" or not plan["dw_beside_dx"]),
+                   key=lambda kv: kv[1]["total_ms"])
+    achieved = pk["flops"] / pk["total_ms"] / 1e9 if name not in HBM_BOUND else pk["bytes"] / pk["total_ms"] / 1e6
+    roof_peak = peaks["hbm_gbs"] if name in HBM_BOUND else peaks["bf16_tflops"]
+    loss_v = float(loss.item())
+    h.close()
+    if own_group:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
+        "ms_per_step_with_kernel_events": ms_events,
+        "config": {"workload": args.config, "N": w.N, "H": w.H, "V": w.V, "tokens_per_rank": b - a,
+                   "chunk": plan["chunk"], "num_chunks": plan["num_chunks"], "dlogits": plan["dlogits"],
+                   "l2": l2_note(w.V * w.H * x.element_size(), plan["logits_bytes"]),
+                   "parallelism": f"token-parallel over {ws} rank(s): all-reduce of n_valid, then of "
+                                  "dW and the loss shares (NCCL)"},
+        "tflops": tflops, "frac_of_bf16_peak": tflops / peaks["bf16_tflops"], "peak_source": peaks_kind,
+        "loss": loss_v, "gpu_launches": launches,
+        "roofline": {"bound": "hbm" if name in HBM_BOUND else "tensor", "achieved": achieved,
+                     "peak": roof_peak, "unit": "GB/s" if name in HBM_BOUND else "TFLOP/s",
+                     "frac": achieved / roof_peak, "traffic": None, "kernel": name,
+                     "timing": "per-launch CUDA events over a second run of the timed steps"},
+        "clocks": clk,
+        "e2e": None,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.token_parallel:
+        run_token_parallel(args, ws, rank, local)
     else:
         run_ours(args, ws, rank, local)
     if ws > 1:

@@ -1,6 +1,6 @@
-"""The multi-rank logic of bench.py (independent replicas): with two gloo
-ranks on the CPU, the job time is the slowest rank's and the throughput counts
-every rank's tokens."""
+"""The multi-rank logic of bench.py: with two gloo ranks on the CPU, the job
+time is the slowest rank's; independent replicas count every rank's tokens,
+a token-sharded batch (--token-parallel) counts the batch's tokens once."""
 import os
 import socket
 
@@ -24,7 +24,9 @@ def _rank_main(rank, ws, port, out):
     dist.init_process_group("gloo", rank=rank, world_size=ws)
     bench.barrier(ws)
     ms_max, value = bench.aggregate(ws, 16384, 10.0 * (rank + 1))
-    out[rank] = (ms_max, value)
+    # --token-parallel: one batch of 16384 tokens split over the ranks
+    ms_sh, value_sh = bench.aggregate_sharded(ws, 16384, 10.0 * (rank + 1))
+    out[rank] = (ms_max, value, ms_sh, value_sh)
     bench.barrier(ws)
     dist.destroy_process_group()
 
@@ -41,9 +43,12 @@ def test_two_rank_replica_aggregation():
         p.join(120)
         assert p.exitcode == 0
     for r in range(2):
-        ms_max, value = out[r]
+        ms_max, value, ms_sh, value_sh = out[r]
         assert ms_max == pytest.approx(20.0)
         assert value == pytest.approx(2 * 16384 / 0.020)
+        # a sharded batch counts its tokens once, over the slowest rank
+        assert ms_sh == pytest.approx(20.0)
+        assert value_sh == pytest.approx(16384 / 0.020)
 
 
 def test_single_rank_aggregation():
