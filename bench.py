@@ -69,7 +69,10 @@ def dist_setup(args):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if ws > 1:
+    # under torchrun the token-parallel mode joins its rendezvous even with one
+    # rank (an explicit tcp:// group there would wait on the launcher's store)
+    launched = "MASTER_PORT" in os.environ and "RANK" in os.environ
+    if ws > 1 or (args.impl == "ours" and args.token_parallel and launched):
         import torch
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
@@ -557,7 +560,7 @@ def run_token_parallel(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     own_group = not dist.is_initialized()
-    if own_group:   # one process: the collectives run over a one-rank NCCL group
+    if own_group:   # one plain process: the collectives run over a one-rank NCCL group
         with socket.socket() as sk:
             sk.bind(("127.0.0.1", 0))
             port = sk.getsockname()[1]
@@ -662,8 +665,8 @@ def main():
         run_token_parallel(args, ws, rank, local)
     else:
         run_ours(args, ws, rank, local)
-    if ws > 1:
-        import torch.distributed as dist
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
         dist.destroy_process_group()
 
 
