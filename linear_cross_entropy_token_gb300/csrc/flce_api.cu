@@ -150,27 +150,30 @@ enum Shape : int { kShapeSingle = 0, kShapePair = 1, kShapeWide = 2 };
 
 // A time model of one GEMM on CTA pairs, in SM cycles, for choosing between
 // wide (256 x 512, single-buffered accumulator) and pair (256 x 256, double-
-// buffered) tiles per launch. Fitted to launches timed on GB300 at the
-// 16384 x 4096 x 128256 and 2048 x 1024 x 32000 shapes: a 64-deep k-block of
-// a wide tile takes ~1110 cycles and of a pair tile ~610 (the wide tile does
-// twice the MMA work per k-block with less shared-memory traffic per FLOP);
-// a wide tile's epilogue holds the accumulator ~7100 cycles (log-sum-exp) or
-// ~5700 (fp32 stores) before the next tile's MMAs may start, while a pair
-// tile's epilogue (~3500 / ~2900 cycles) overlaps its successor's main loop
-// and only shows when that is shorter; each tile also pays ~1500 cycles of
-// pipeline fill. Work units run in waves of `slots` pairs.
+// buffered) tiles per launch. Fitted to 27 launches timed on GB300 (logits, dx
+// and dW GEMMs at N x H x V from 1024 x 1024 x 32000 to 4096 x 4096 x 32768,
+// both shapes, run one after the other): a 64-deep k-block of a wide tile
+// takes ~1110 cycles and of a pair tile ~720 (the wide tile does twice the MMA
+// work per k-block with less shared-memory traffic per FLOP); a wide tile's
+// epilogue holds the accumulator ~4000 cycles (log-sum-exp: one pass over
+// TMEM, the exponentials after the release) or ~5700 (fp32 stores) before the
+// next tile's MMAs may start, while a pair tile's epilogue (~5000 / ~4150
+// cycles) overlaps its successor's main loop and only shows when that is
+// shorter; each tile also pays ~1500 cycles of pipeline fill. Work units run
+// in waves of `slots` pairs. The model gets every measured wide-or-pair
+// decision right that differs by more than 3%, its pair/wide ratios within
+// about 7% on average.
 double gemm_cycles(int shape, int64_t M, int64_t N, int64_t K, bool lse, int64_t S, int slots) {
   const int64_t kb = cdiv(cdiv(K, kBK), S);
   const int64_t units = cdiv(M, 2 * kBM) * cdiv(N, shape == kShapeWide ? 2 * kBN : kBN) * S;
   const double waves = static_cast<double>(cdiv(units, std::max(slots, 1)));
   const double fill = 1500.0;
-  if (shape == kShapeWide) return waves * (1110.0 * kb + (lse ? 7100.0 : 5700.0) + fill);
-  return waves * (std::max(610.0 * kb, lse ? 3500.0 : 2900.0) + fill);
+  if (shape == kShapeWide) return waves * (1110.0 * kb + (lse ? 4000.0 : 5700.0) + fill);
+  return waves * (std::max(720.0 * kb, lse ? 5000.0 : 4150.0) + fill);
 }
 
 // Pair tiles replace the wide ones only where the model times them more
-// than this much faster: its error against measured launches is about 5%
-// (at 4096 x 32768 x 4096 it put pair 2% ahead; wide measured 6% faster).
+// than this much faster (its error against measured launches is 5-7%).
 constexpr double kPairMargin = 0.95;
 
 // The tile shape (wide or pair) for one GEMM.
