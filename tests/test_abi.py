@@ -213,11 +213,13 @@ def test_plan_refuses_a_tile_shape_that_does_not_exist(lib):
 def test_plan_picks_tile_shapes_per_gemm():
     """The default handle times wide (256 x 512) against pair (256 x 256)
     tiles per GEMM with a model and takes pair tiles only where they win by
-    more than 5%: the short reductions of a 2048 x 1024 x 32000 call (logits
-    K = 1024, dW K = 2048); the long ones of the Llama-3 shape stay wide.
-    An explicit tile shape applies to every GEMM."""
+    more than 5%: where a wide tile would waste half its columns (H = 256:
+    dx and dW), or leave a short dx launch with too few units; the logits
+    GEMM stays wide. An explicit tile shape applies to every GEMM."""
     p = flce.plan(2048, 1024, 32000)
-    assert (p["tile_n"], p["tile_n_dx"], p["tile_n_dw"]) == (256, 512, 256)
+    assert (p["tile_n"], p["tile_n_dx"], p["tile_n_dw"]) == (512, 512, 512)
+    n = flce.plan(2048, 256, 32000)
+    assert (n["tile_n"], n["tile_n_dx"], n["tile_n_dw"], n["dx_splits"]) == (512, 256, 256, 8)
     q = flce.plan(2048, 1024, 32000, cta="wide")
     assert (q["tile_n"], q["tile_n_dx"], q["tile_n_dw"]) == (512, 512, 512)
     r = flce.plan(2048, 1024, 32000, cta="pair")
