@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define FLCE_ABI_VERSION 4
+#define FLCE_ABI_VERSION 5
 
 typedef struct flce_handle_s* flce_handle_t;
 
@@ -123,13 +123,18 @@ typedef struct flce_config {
 } flce_config;
 
 /* How the dx and dW GEMMs of a chunk are launched (CTA pairs only).
- *  SEPARATE:   one launch each.
- *  ONE_LAUNCH: one launch; its work units (dx first, then dW) are handed out
- *              dynamically, so the short dW units fill the time the long dx
- *              units leave idle at the end.
- *  AUTO:       SEPARATE (measured faster on GB300: 5.56 against 5.92 ms per
- *              4096-token chunk of the 128256-vocabulary step; running dx and
- *              dW units side by side costs more than the dx tail it fills). */
+ *  SEPARATE:   one launch each (the dW GEMM on a second stream beside a dx
+ *              launch that fills less than two waves of SM pairs).
+ *  ONE_LAUNCH: one launch on one tile shape; its work units (dx first, then
+ *              dW) are handed out dynamically, so the short dW units fill the
+ *              time the long dx units leave idle at the end, and the dx
+ *              reduction over V needs few or no splits.
+ *  AUTO:       ONE_LAUNCH where the dW GEMM runs on wide tiles (measured on
+ *              GB300: 29.6 against 30.8 ms for the 16384-token,
+ *              128256-vocabulary step, 35.0 against 37.2 ms at V = 151936,
+ *              0.33 against 0.34 ms for 2048 tokens at V = 32000), else
+ *              SEPARATE (on 256 x 256 pair tiles one launch measured slower:
+ *              5.92 against 5.56 ms per 4096-token chunk at V = 128256). */
 enum { FLCE_BACKWARD_AUTO = 0, FLCE_BACKWARD_SEPARATE = 1, FLCE_BACKWARD_ONE_LAUNCH = 2 };
 
 /* The chunk plan of one call (token-chunk scheduler). */
@@ -138,7 +143,8 @@ typedef struct flce_plan {
     int64_t num_chunks;          /* ceil(N / C)                                        */
     int64_t vocab_tiles;         /* ceil(V / 256): log-sum-exp partials per token      */
     int64_t ldv;                 /* row stride, in elements, of the chunk logits buffer */
-    int64_t dx_splits;           /* split of the V reduction of the dx GEMM            */
+    int64_t dx_splits;           /* split of the V reduction of the dx GEMM (fp32
+                                    partials summed in split order by the reduction) */
     uint64_t workspace_bytes;    /* device bytes one call needs                        */
     uint64_t logits_bytes;       /* of which the C x ldv logits / dlogits buffer       */
     int64_t tile_m;              /* rows of a GEMM output tile: 128 (one CTA) or 256 (CTA
@@ -158,6 +164,10 @@ typedef struct flce_plan {
                                     handle's second stream (in-place and recompute
                                     modes on CTA pairs, when the dx launch fills less
                                     than two waves of SM pairs); 0: one after the other */
+    int64_t backward_one_launch; /* 1: the dx and dW GEMMs of a chunk share one launch
+                                    (FLCE_BACKWARD_ONE_LAUNCH on CTA pairs, in-place
+                                    and recompute modes), on the dx GEMM's tile shape,
+                                    so tile_n_dw == tile_n_dx; 0: separate launches */
 } flce_plan;
 
 /* Kernel kinds, for the per-kernel timing of flce_profile_read(). */

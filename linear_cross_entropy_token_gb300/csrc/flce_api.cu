@@ -163,13 +163,53 @@ enum Shape : int { kShapeSingle = 0, kShapePair = 1, kShapeWide = 2 };
 // in waves of `slots` pairs. The model gets every measured wide-or-pair
 // decision right that differs by more than 3%, its pair/wide ratios within
 // about 7% on average.
+// One work unit of kb k-blocks in that model: what it occupies its pair for.
+double unit_cycles(int shape, int64_t kb, bool lse) {
+  const double fill = 1500.0;
+  if (shape == kShapeWide) return 1110.0 * kb + (lse ? 4000.0 : 5700.0) + fill;
+  return std::max(720.0 * kb, lse ? 5000.0 : 4150.0) + fill;
+}
+
 double gemm_cycles(int shape, int64_t M, int64_t N, int64_t K, bool lse, int64_t S, int slots) {
   const int64_t kb = cdiv(cdiv(K, kBK), S);
   const int64_t units = cdiv(M, 2 * kBM) * cdiv(N, shape == kShapeWide ? 2 * kBN : kBN) * S;
   const double waves = static_cast<double>(cdiv(units, std::max(slots, 1)));
-  const double fill = 1500.0;
-  if (shape == kShapeWide) return waves * (1110.0 * kb + (lse ? 4000.0 : 5700.0) + fill);
-  return waves * (std::max(720.0 * kb, lse ? 5000.0 : 4150.0) + fill);
+  return waves * unit_cycles(shape, kb, lse);
+}
+
+// HBM round trip of the dx GEMM's fp32 split partials (written, then read by
+// the reduction, which also writes dx), in SM cycles at about 3.6 KB per cycle
+double dx_partials_cycles(int64_t S, int64_t C, int64_t H) {
+  return (4.0 * S * C * H + 6.0 * C * H) / 3600.0;
+}
+
+// Splits of the dx GEMM's V reduction when dx and dW share one dynamically
+// scheduled launch on tile shape `shape`: the pairs hand units out until none
+// is left, so the launch takes about the longer of its longest unit and its
+// whole work spread over the pairs. Fewer splits mean longer dx units but
+// less partial traffic; with long dx units the short dW units fill in
+// behind them. Measured with one launch on GB300: one split at the Llama-3
+// and Qwen3 shapes (29.6 and 35.0 ms per step against 30.2 and 35.4 with four
+// and five), two to four at 2048 x 1024 x 32000 (within 1%).
+int64_t one_launch_splits(int shape, int64_t C, int64_t H, int64_t V, int slots) {
+  const int64_t kb = cdiv(V, kBK);
+  const int64_t tiles_dx = cdiv(C, 2 * kBM) * cdiv(H, shape == kShapeWide ? 2 * kBN : kBN);
+  const int64_t units_dw = cdiv(V, 2 * kBM) * cdiv(H, shape == kShapeWide ? 2 * kBN : kBN);
+  const double dw = static_cast<double>(units_dw) * unit_cycles(shape, cdiv(C, kBK), false);
+  int64_t best = 1;
+  double best_t = -1;
+  for (int64_t sp = 1; sp <= 8; ++sp) {
+    if (sp > 1 && kb / sp < 16) break;
+    const int64_t kbps = cdiv(kb, sp), S = cdiv(kb, kbps);
+    const double unit = unit_cycles(shape, kbps, false);
+    const double t = std::max(unit, (static_cast<double>(tiles_dx * S) * unit + dw) / std::max(slots, 1)) +
+                     dx_partials_cycles(S, C, H);
+    if (best_t < 0 || t < best_t * 0.999) {  // more splits only for a gain
+      best_t = t;
+      best = sp;
+    }
+  }
+  return best;
 }
 
 // Pair tiles replace the wide ones only where the model times them more
@@ -304,7 +344,7 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
       for (int64_t sp = 1; sp <= 8; ++sp) {
         if (sp > 1 && kb / sp < 16) break;
         const double t = gemm_cycles(best[i].shape, C, H, V, false, sp, slots) +
-                         (4.0 * sp * C * H + 6.0 * C * H) / 3600.0;
+                         dx_partials_cycles(sp, C, H);
         if (best_t[i] < 0 || t < best_t[i] * 0.999) {  // more splits only for a gain
           best_t[i] = t;
           best[i].splits = sp;
@@ -313,11 +353,43 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
     }
     return best_t[1] < kPairMargin * best_t[0] ? best[1] : best[0];
   };
+  // The backward GEMMs of a chunk of C tokens (bf16 in-place and recompute
+  // modes on CTA pairs): their tile shapes, and whether they share one
+  // dynamically scheduled launch. A mixed plan picks dW's shape with the time
+  // model; by default the two share a launch when dW runs on wide tiles, dx
+  // joining it there (with units handed out dynamically, the wave count that
+  // can favour pair tiles for a dx launch of its own no longer matters). An
+  // explicit one-launch request takes the wide tiles too when dW has them,
+  // else dx's own choice. Handles with one tile shape share a launch when
+  // asked to, or by default on wide tiles.
+  struct Backward {
+    int dx_shape, dw_shape;
+    bool one_launch;
+  };
+  const int handle_shape = group == 1 ? kShapeSingle : (tile_n == 2 * kBN ? kShapeWide : kShapePair);
+  auto backward_for = [&](int64_t C) -> Backward {
+    const int bl = cfg->backward_launch;
+    if (!bf16 || slabs || group == 1) return {handle_shape, handle_shape, false};
+    if (!mixed) {
+      const bool one = bl == FLCE_BACKWARD_ONE_LAUNCH ||
+                       (bl == FLCE_BACKWARD_AUTO && handle_shape == kShapeWide);
+      return {handle_shape, handle_shape, one};
+    }
+    const int64_t c = std::max<int64_t>(C, 1);
+    const int dws = pick_shape(V, H, c, false, slots);
+    if (bl == FLCE_BACKWARD_ONE_LAUNCH) {
+      const int sh = dws == kShapeWide ? kShapeWide : dx_choice(c).shape;
+      return {sh, sh, true};
+    }
+    if (bl == FLCE_BACKWARD_AUTO && dws == kShapeWide) return {kShapeWide, kShapeWide, true};
+    return {dx_choice(c).shape, dws, false};
+  };
   // splits of the dx GEMM's V reduction. fp32: the CUDA-core dx GEMM splits
   // when its C x H output has too few tiles to fill the SMs (the count for the
-  // full V bounds that of any slab). bf16: the mixed plan's choice, one split
-  // for SLABS (dx accumulates over the slabs in one fp32 buffer), else the
-  // count that fills the waves of the handle's tile shape.
+  // full V bounds that of any slab). bf16: one split for SLABS (dx accumulates
+  // over the slabs in one fp32 buffer); the one-launch model when dx and dW
+  // share a launch; else the mixed plan's choice, or the count that fills the
+  // waves of the handle's tile shape.
   auto splits_for = [&](int64_t C) -> int64_t {
     if (!bf16) {
       // the partials take at most an eighth of the budget
@@ -326,8 +398,11 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
       const int64_t s = std::min<int64_t>(simt_split_k(std::max<int64_t>(C, 1), H, V, num_sms), cap);
       return s > 1 ? s : 0;
     }
+    if (slabs) return 1;
+    const Backward bw = backward_for(C);
+    if (bw.one_launch) return one_launch_splits(bw.dx_shape, std::max<int64_t>(C, 1), H, V, slots);
     if (mixed) return dx_choice(std::max<int64_t>(C, 1)).splits;
-    return slabs ? 1 : pick_dx_splits(C, H, V, slots, tile_m, tile_n);
+    return pick_dx_splits(C, H, V, slots, tile_m, tile_n);
   };
   // SLABS: the widest slab (a multiple of 512 columns) whose C x slab buffer
   // fits both kSlabBytes and what the budget leaves beside the rest of the
@@ -424,22 +499,24 @@ flce_status plan_impl(const flce_config* cfg, int64_t N, int64_t H, int64_t V, i
   out->tile_n = tile_n;
   out->tile_n_dx = tile_n;
   out->tile_n_dw = tile_n;
-  if (mixed && C > 0) {
-    auto cols = [](int sh) -> int64_t { return sh == kShapeWide ? 2 * kBN : kBN; };
-    out->tile_n = cols(pick_shape(C, V, H, true, slots));
-    out->tile_n_dx = cols(dx_choice(C).shape);
-    out->tile_n_dw = cols(pick_shape(V, H, C, false, slots));
-  }
-  // in-place and recompute modes on CTA pairs: the dW GEMM runs beside a dx
-  // launch that fills less than kOverlapWaves waves (the one-launch pair
-  // backward, when asked for, takes precedence)
-  if (bf16 && !slabs && C > 0 && group == 2 &&
-      !(cfg->cta_pair == FLCE_CTA_PAIR && cfg->backward_launch == FLCE_BACKWARD_ONE_LAUNCH)) {
-    const int64_t kb = cdiv(V, kBK);
-    const int64_t kbps = cdiv(kb, std::max<int64_t>(out->dx_splits, 1));
-    const int64_t S = cdiv(kb, kbps);
-    const int64_t dx_units = cdiv(C, 2 * kBM) * cdiv(H, out->tile_n_dx) * S;
-    out->dw_beside_dx = dx_units < static_cast<int64_t>(kOverlapWaves) * slots ? 1 : 0;
+  auto cols = [](int sh) -> int64_t { return sh == kShapeWide ? 2 * kBN : kBN; };
+  if (mixed && C > 0) out->tile_n = cols(pick_shape(C, V, H, true, slots));
+  // in-place and recompute modes on CTA pairs: the dx and dW GEMMs of a chunk
+  // share one dynamically scheduled launch (measured faster than separate
+  // launches at every workload shape on wide tiles), or the dW GEMM runs
+  // beside a dx launch that fills less than kOverlapWaves waves
+  if (bf16 && !slabs && C > 0 && group == 2) {
+    const Backward bw = backward_for(C);
+    out->tile_n_dx = cols(bw.dx_shape);
+    out->tile_n_dw = cols(bw.dw_shape);
+    out->backward_one_launch = bw.one_launch ? 1 : 0;
+    if (!bw.one_launch) {
+      const int64_t kb = cdiv(V, kBK);
+      const int64_t kbps = cdiv(kb, std::max<int64_t>(out->dx_splits, 1));
+      const int64_t S = cdiv(kb, kbps);
+      const int64_t dx_units = cdiv(C, 2 * kBM) * cdiv(H, out->tile_n_dx) * S;
+      out->dw_beside_dx = dx_units < static_cast<int64_t>(kOverlapWaves) * slots ? 1 : 0;
+    }
   }
   // fp32 handles run SLABS as asked and every other mode in place
   out->dlogits_mode = slabs ? FLCE_DLOGITS_SLABS
@@ -1158,10 +1235,14 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       }
       const double dx_bytes = 2 * dr * dV + 2 * dV * dH + 4.0 * S * dr * dH;
       const double dw_bytes = 2 * dr * dV + 2 * dr * dH + (c > 0 ? 8.0 : 4.0) * dV * dH;
-      if (h->shape == kShapePair && h->cfg.cta_pair == FLCE_CTA_PAIR &&
-          h->cfg.backward_launch == FLCE_BACKWARD_ONE_LAUNCH) {
-        // both read the finished dlogits buffer: one launch, dx units first,
-        // handed out from a counter in the control block
+      if (p.backward_one_launch) {
+        // both read the finished dlogits buffer: one launch on the dx GEMM's
+        // tile shape, dx units first, handed out from a counter in the
+        // control block
+        const int shape = shape_for(h, p.tile_n_dx);
+        const bool wide = shape == kShapeWide;
+        const int64_t tile_cols = wide ? 2 * kBN : kBN;
+        const int slots_max = wide ? h->wide_clusters : h->pair_clusters;
         DualMaps maps;
         maps.a[0] = mZ_k;
         maps.b[0] = mW_mn;
@@ -1174,16 +1255,19 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
         da.p[1] = d;
         da.p[0].num_m = static_cast<int>(cdiv(rows, 2 * kBM));
         da.p[1].num_m = static_cast<int>(cdiv(V, 2 * kBM));
+        da.p[0].num_n = da.p[1].num_n = static_cast<int>(cdiv(H, tile_cols));
         da.units0 = da.p[0].num_m * da.p[0].num_n * da.p[0].num_s;
-        da.p[0].group_m = group_for(h, kShapePair, da.p[0].num_m, da.p[0].num_n, da.p[0].num_s,
-                                    std::min(da.units0, h->pair_clusters));
+        da.p[0].group_m = group_for(h, shape, da.p[0].num_m, da.p[0].num_n, da.p[0].num_s,
+                                    std::min(da.units0, slots_max));
         da.pad = 0;
         da.sched_ctr = reinterpret_cast<int32_t*>(ctrl + kCtrlSched);
         e = cudaMemsetAsync(da.sched_ctr, 0, 4, s);
         if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
         const int units = da.units0 + da.p[1].num_m * da.p[1].num_n;
+        const int pairs = std::min(units, slots_max);
         FLCE_LAUNCH(FLCE_K_GEMM_DX_DW, 4 * dr * dV * dH, dx_bytes + dw_bytes,
-                    launch_umma_pair_dual(maps, da, std::min(units, h->pair_clusters), s));
+                    wide ? launch_umma_wide_dual(maps, da, pairs, s)
+                         : launch_umma_pair_dual(maps, da, pairs, s));
       } else if (overlap_dw) {
         // the dx GEMM fills less than kOverlapWaves waves of the GPU: the dW
         // GEMM runs beside it on the side stream (both only read the finished

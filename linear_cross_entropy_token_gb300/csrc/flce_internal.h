@@ -101,6 +101,10 @@ struct DualArgs {
 };
 cudaError_t launch_umma_pair_dual(const DualMaps& maps, const DualArgs& args, int pairs,
                                   cudaStream_t s);
+// The same on wide tiles (256 x 512; num_n counts 512-column tiles), launched
+// on at most umma_wide_max_clusters() pairs.
+cudaError_t launch_umma_wide_dual(const DualMaps& maps, const DualArgs& args, int pairs,
+                                  cudaStream_t s);
 cudaError_t launch_wait_check(uint32_t* ctrl, uint64_t timeout_ns, cudaStream_t s);
 
 // flce_rows.cu

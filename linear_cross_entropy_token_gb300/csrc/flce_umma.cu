@@ -1214,6 +1214,289 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// ================================ dx and dW GEMMs in one launch, wide tiles
+//
+// The same dynamically scheduled backward on the wide tiles: 256 x 512 output
+// tiles, two MMAs per k-step sharing A through the collector, the single-
+// buffered 512-column accumulator and the two epilogue warpgroups of
+// umma_wide_kernel. Each ring slot now has six consumers: the even CTA's MMA
+// issuer, the odd CTA's producer, and the leader of each of the four epilogue
+// warpgroups (two per CTA), each after its whole warpgroup has read the slot.
+// With separate launches the dx GEMM's last wave of long units leaves pairs
+// idle, and a dW launch beside it on another stream only starts its
+// statically assigned units once dx units retire; here a pair that runs out
+// of dx units takes the next dW unit at once.
+constexpr int kSchedConsumersWide = 6;
+constexpr uint32_t kSmemBytesWideDual =
+    kSmemBytesWide + 2 * kSchedDepth * 8 + kSchedDepth * 4 + 16;
+static_assert(kSmemBytesWideDual <= 232448, "shared memory per CTA");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
+    umma_wide_dual_kernel(const __grid_constant__ DualMaps maps, const __grid_constant__ DualArgs d) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStagesWide * kABytes;
+  uint8_t* sE = sB + kStagesWide * kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBufsWide * kEpiBytes);
+  uint64_t* sbars = bars + 2 * kStagesWide + 3;  // unit ring: full[kSchedDepth], empty[kSchedDepth]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbars + 2 * kSchedDepth);
+  int32_t* sched_u = reinterpret_cast<int32_t*>(tmem_slot + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStagesWide + s); };
+  const uint32_t tfull_bar = bar0 + 8u * (2 * kStagesWide);
+  const uint32_t tempty_bar = bar0 + 8u * (2 * kStagesWide + 1);
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStagesWide + 2);
+  const uint32_t sbar0 = smem_u32(sbars);
+  auto sfull_bar = [&](int i) { return sbar0 + 8u * i; };
+  auto sempty_bar = [&](int i) { return sbar0 + 8u * (kSchedDepth + i); };
+  const uint32_t su0 = smem_u32(sched_u);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0: the CTA that claims units and issues the MMAs
+  uint32_t* ctrl = d.p[0].ctrl;
+  const uint64_t timeout_ns = d.p[0].timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesWide; ++s) {
+      mbar_init(full_bar(s), 1);     // used in CTA 0 only: both CTAs' loads land here
+      mbar_init(empty_bar(s), 1);    // each CTA's own, released by the pair's MMA commit
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, 2 * 2 * kEpiThreads);  // used in CTA 0: both CTAs' two epilogues arrive
+    mbar_init(drain_bar, 1);
+    for (int i = 0; i < kSchedDepth; ++i) {
+      mbar_init(sfull_bar(i), 1);                     // the even CTA's producer publishes
+      mbar_init(sempty_bar(i), kSchedConsumersWide);  // used in CTA 0
+    }
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    for (int q = 0; q < 2; ++q) {
+      tma_prefetch_map(&maps.a[q]);
+      tma_prefetch_map(&maps.b[q]);
+      tma_prefetch_map(&maps.o[q]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int units1 = d.p[1].num_m * d.p[1].num_n * d.p[1].num_s;
+  const int num_units = d.units0 + units1;
+  // problem (0: dx, 1: dW) and its own unit of a unit of the combined schedule
+  auto locate = [&](int u, int& q, Unit& t) {
+    q = u >= d.units0 ? 1 : 0;
+    t = unit_coords(d.p[q], q ? u - d.units0 : u);
+  };
+  // the unit of step i (-1: no more), optionally releasing the slot; false
+  // if the wait ran out
+  auto next_unit = [&](int i, int& u, bool release) {
+    const int slot = i % kSchedDepth;
+    if (!mbar_wait_bounded_cluster(sfull_bar(slot), (i / kSchedDepth) & 1u, ctrl, timeout_ns))
+      return false;
+    u = ld_shared_s32(su0 + 4u * slot);
+    if (release) {
+      if (rank == 0)
+        mbar_arrive(sempty_bar(slot));
+      else
+        mbar_arrive_cluster(mapa_shared(sempty_bar(slot), 0));
+    }
+    return true;
+  };
+
+  // each role's code sits inside the branch that sets its register budget
+  if (warp < 4) {
+    warpgroup_regs_dec<kWideRegsCtl>();
+    if (warp == 0) {
+      if (lane == 0) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t n_issued = 0;
+        bool failed = false;
+        for (int i = 0; !failed; ++i) {
+          int u;
+          if (rank == 0) {
+            // claim the next unit and publish it to both CTAs
+            const int slot = i % kSchedDepth;
+            if (!mbar_wait_bounded_cluster(sempty_bar(slot), ((i / kSchedDepth) & 1u) ^ 1u, ctrl,
+                                           timeout_ns)) {
+              failed = true;
+              break;
+            }
+            u = atomicAdd(d.sched_ctr, 1);
+            if (u >= num_units) u = -1;
+            sched_u[slot] = u;
+            st_shared_cluster_u32(mapa_shared(su0 + 4u * slot, 1), static_cast<uint32_t>(u));
+            mbar_arrive(sfull_bar(slot));
+            mbar_arrive_cluster(mapa_shared(sfull_bar(slot), 1));
+          } else if (!next_unit(i, u, true)) {
+            failed = true;
+            break;
+          }
+          if (u < 0) break;
+          int q;
+          Unit t;
+          locate(u, q, t);
+          const UmmaArgs& a = d.p[q];
+          const int kb0 = t.s * a.kb_per_split;
+          const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+          const int mA = t.m * 2 * kBM + static_cast<int>(rank) * kBM;      // this CTA's rows of A
+          const int nB0 = t.n * 2 * kBN + static_cast<int>(rank) * (kBN / 2);  // its columns, MMA 0
+          const int nB1 = nB0 + kBN;                                          // and MMA 1
+          for (int kb = kb0; kb < kb1; ++kb) {
+            const int stage = n_issued % kStagesWide;
+            const uint32_t phase = (n_issued / kStagesWide) & 1u;
+            if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, ctrl, timeout_ns)) {
+              failed = true;
+              break;
+            }
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytesWide);
+            const uint32_t fb = mapa_shared(full_bar(stage), 0);
+            const uint32_t sa = smem_u32(sA + stage * kABytes);
+            const uint32_t sb = smem_u32(sB + stage * kBBytes);
+            const int k0 = kb * kBK;
+            if (q == 0)
+              load_a_pair<0>(sa, &maps.a[0], fb, k0, mA);
+            else
+              load_a_pair<1>(sa, &maps.a[1], fb, k0, mA);
+            // B is MN-major in both problems
+            tma_load_2d_pair(sb, &maps.b[q], fb, nB0, k0);
+            tma_load_2d_pair(sb + 8192, &maps.b[q], fb, nB0 + 64, k0);
+            tma_load_2d_pair(sb + kBHalfBytes, &maps.b[q], fb, nB1, k0);
+            tma_load_2d_pair(sb + kBHalfBytes + 8192, &maps.b[q], fb, nB1 + 64, k0);
+            ++n_issued;
+          }
+        }
+        if (failed && rank == 0) {
+          const uint32_t first = n_issued > kStagesWide ? n_issued - kStagesWide : 0;
+          for (uint32_t i = first; i < n_issued; ++i)
+            mbar_drain_wait(full_bar(i % kStagesWide), (i / kStagesWide) & 1u, timeout_ns);
+        }
+      }
+    } else if (warp == 1) {
+      if (lane == 0 && rank == 0) {
+        // ------------------------------------- MMA issuer (CTA 0 of the pair)
+        constexpr uint32_t idesc_k = idesc_bf16_f32(2 * kBM, kBN, 0, 1);
+        constexpr uint32_t idesc_mn = idesc_bf16_f32(2 * kBM, kBN, 1, 1);
+        uint32_t n_consumed = 0;
+        bool issued = false, failed = false;
+        for (int it = 0; !failed; ++it) {
+          int u;
+          if (!next_unit(it, u, true)) {
+            failed = true;
+            break;
+          }
+          if (u < 0) break;
+          int q;
+          Unit t;
+          locate(u, q, t);
+          const UmmaArgs& a = d.p[q];
+          const int kb0 = t.s * a.kb_per_split;
+          const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
+          if (!mbar_wait_bounded_cluster(tempty_bar, (it & 1) ^ 1u, ctrl, timeout_ns)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t idesc = q ? idesc_mn : idesc_k;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            const int stage = n_consumed % kStagesWide;
+            const uint32_t phase = (n_consumed / kStagesWide) & 1u;
+            if (!mbar_wait_bounded_cluster(full_bar(stage), phase, ctrl, timeout_ns)) {
+              failed = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(sA + stage * kABytes);
+            const uint32_t sb = smem_u32(sB + stage * kBBytes);
+  #pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t ad = q ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                    : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+              const uint64_t bd0 = smem_desc_sw128(sb + 2048u * k, 8192u, 1024u);
+              const uint64_t bd1 = smem_desc_sw128(sb + kBHalfBytes + 2048u * k, 8192u, 1024u);
+              const uint32_t acc_in = (kb > kb0 || k > 0) ? 1u : 0u;
+              tc_mma_bf16_pair_a_fill(tmem_base, ad, bd0, idesc, acc_in);
+              tc_mma_bf16_pair_a_lastuse(tmem_base + kBN, ad, bd1, idesc, acc_in);
+            }
+            issued = true;
+            tc_commit_pair_multicast(empty_bar(stage), 0x3);
+            ++n_consumed;
+          }
+          if (failed) break;
+          tc_commit_pair_multicast(tfull_bar, 0x3);
+        }
+        if (failed && issued) {
+          tc_commit_pair(drain_bar);
+          mbar_drain_wait(drain_bar, 0, timeout_ns);
+        }
+      }
+    }
+  } else {
+    warpgroup_regs_inc<kWideRegsEpi>();
+    // ------------------------------------------------------------ epilogue
+    // one warpgroup per 256-column half of the tile, as in umma_wide_kernel
+    const int grp = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const bool leader = threadIdx.x == (grp + 1) * kEpiThreads;
+    const uint32_t bar = kEpiBar + static_cast<uint32_t>(grp);
+    uint8_t* sEg = sE + grp * kEpiBufsWide * kEpiBytes;
+    uint32_t ebuf = 0;
+    for (int it = 0;; ++it) {
+      int u = -1;
+      const bool got = next_unit(it, u, false);
+      // the whole warpgroup has read the slot (or given up) before its leader releases it
+      if (named_bar_or(bar, kEpiThreads, !got)) break;
+      if (leader) {
+        const int slot = it % kSchedDepth;
+        if (rank == 0)
+          mbar_arrive(sempty_bar(slot));
+        else
+          mbar_arrive_cluster(mapa_shared(sempty_bar(slot), 0));
+      }
+      if (u < 0) break;
+      const bool ok = mbar_wait_bounded_cluster(tfull_bar, it & 1, ctrl, timeout_ns);
+      if (named_bar_or(bar, kEpiThreads, !ok)) break;
+      tc_fence_after();
+      int q;
+      Unit t;
+      locate(u, q, t);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + grp * kBN;
+      const int m0 = t.m * 2 * kBM + static_cast<int>(rank) * kBM;
+      const int n0 = t.n * 2 * kBN + grp * kBN;
+      // a half past the last column only releases the accumulator
+      epilogue_tile<kEpiF32, kEpiBufsWide>(d.p[q], &maps.o[q], sEg, ebuf, row, leader, m0, n0, t.s,
+                                           tbase,
+                                           [&] {
+                                             tc_fence_before();
+                                             if (rank == 0)
+                                               mbar_arrive(tempty_bar);
+                                             else
+                                               mbar_arrive_cluster(mapa_shared(tempty_bar, 0));
+                                           },
+                                           bar);
+    }
+    if (leader) bulk_wait_group<0>();
+  }
+
+  __syncwarp();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair's MMAs may touch its memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 // One bounded wait on a barrier that nothing completes: checks that a wait
 // which runs out reports FLCE_ERR_TIMEOUT and returns.
 __global__ void wait_check_kernel(uint32_t* ctrl, uint64_t timeout_ns) {
@@ -1349,6 +1632,17 @@ int umma_wide_max_clusters() {
     return 0;
   }
   return n;
+}
+
+cudaError_t launch_umma_wide_dual(const DualMaps& maps, const DualArgs& args, int pairs,
+                                  cudaStream_t s) {
+  static const cudaError_t regs_ok = check_wide_regs(umma_wide_dual_kernel);
+  if (regs_ok != cudaSuccess) return regs_ok;
+  cudaError_t e = cudaFuncSetAttribute(umma_wide_dual_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytesWideDual));
+  if (e != cudaSuccess) return e;
+  umma_wide_dual_kernel<<<2 * pairs, kThreadsWide, kSmemBytesWideDual, s>>>(maps, args);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_umma_pair_dual(const DualMaps& maps, const DualArgs& args, int pairs,

@@ -51,7 +51,8 @@ class Plan(ctypes.Structure):
                 ("logits_bytes", ctypes.c_uint64), ("tile_m", ctypes.c_int64),
                 ("tile_n", ctypes.c_int64), ("vocab_slab", ctypes.c_int64),
                 ("dlogits_mode", ctypes.c_int64), ("tile_n_dx", ctypes.c_int64),
-                ("tile_n_dw", ctypes.c_int64), ("dw_beside_dx", ctypes.c_int64)]
+                ("tile_n_dw", ctypes.c_int64), ("dw_beside_dx", ctypes.c_int64),
+                ("backward_one_launch", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         d = {k: getattr(self, k) for k, _ in self._fields_}
@@ -134,10 +135,11 @@ def make_config(dtype: str = "bf16", device: int = 0, hbm_budget_bytes: int = 0,
 
 
 def plan(N: int, H: int, V: int, dtype: str = "bf16", chunk: int = 0, hbm_budget_bytes: int = 0,
-         num_sms: int = 0, cta: str = "auto", dlogits_mode: str = "auto") -> dict:
+         num_sms: int = 0, cta: str = "auto", dlogits_mode: str = "auto",
+         backward: str = "auto") -> dict:
     """The token-chunk plan for one call (host only; no device needed)."""
     lib = load()
-    cfg = make_config(dtype, 0, hbm_budget_bytes, dlogits_mode, cta=cta)
+    cfg = make_config(dtype, 0, hbm_budget_bytes, dlogits_mode, cta=cta, backward=backward)
     p = Plan()
     st = lib.flce_make_plan(ctypes.byref(cfg), N, H, V, chunk, num_sms, ctypes.byref(p))
     if st != FLCE_OK:

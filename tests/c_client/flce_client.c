@@ -64,12 +64,12 @@ static int plan(int argc, char** argv) {
   }
   printf("chunk %lld num_chunks %lld vocab_tiles %lld ldv %lld dx_splits %lld workspace_bytes %llu "
          "logits_bytes %llu tile_m %lld tile_n %lld vocab_slab %lld dlogits_mode %lld tile_n_dx %lld "
-         "tile_n_dw %lld dw_beside_dx %lld\n",
+         "tile_n_dw %lld dw_beside_dx %lld backward_one_launch %lld\n",
          (long long)p.chunk, (long long)p.num_chunks, (long long)p.vocab_tiles, (long long)p.ldv,
          (long long)p.dx_splits, (unsigned long long)p.workspace_bytes,
          (unsigned long long)p.logits_bytes, (long long)p.tile_m, (long long)p.tile_n,
          (long long)p.vocab_slab, (long long)p.dlogits_mode, (long long)p.tile_n_dx,
-         (long long)p.tile_n_dw, (long long)p.dw_beside_dx);
+         (long long)p.tile_n_dw, (long long)p.dw_beside_dx, (long long)p.backward_one_launch);
   return 0;
 }
 

@@ -24,7 +24,7 @@ def test_exports_every_declared_function(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.flce_abi_version() == 4
+    assert lib.flce_abi_version() == 5
     assert lib.flce_status_string(0) == b"FLCE_OK"
     assert lib.flce_status_string(4) == b"FLCE_ERR_BAD_TARGET"
     assert lib.flce_kernel_name(1) == b"gemm_logits_lse"
@@ -75,7 +75,11 @@ def test_plan_llama3_default_budget():
     assert p["workspace_bytes"] <= int(1.25 * GiB)
     # wide CTA-pair tiles for all three GEMMs at this shape (long reductions)
     assert (p["tile_m"], p["tile_n"], p["tile_n_dx"], p["tile_n_dw"]) == (256, 512, 512, 512)
-    assert p["dx_splits"] == 4          # 128 wide dx tiles on 76 SM pairs: 4 splits fill the waves
+    # dx and dW in one dynamically scheduled launch: the long dx units need
+    # no split, the short dW units fill in behind them
+    assert (p["backward_one_launch"], p["dx_splits"]) == (1, 1)
+    sep = flce.plan(16384, 4096, 128256, "bf16", backward="separate")
+    assert sep["dx_splits"] == 4        # 128 wide dx tiles on 76 SM pairs: 4 splits fill the waves
     q = flce.plan(16384, 4096, 128256, "bf16", cta="pair")
     assert (q["tile_n"], q["dx_splits"]) == (256, 2)   # 256 tiles of 256 x 256: 2 splits
 
@@ -141,7 +145,7 @@ def test_plan_slabs_bounded_in_V():
     # dW GEMM (114 x 8 tiles) both run 912 units, 12 full waves of 76
     assert (p["chunk"], vs) == (4096, 29184)
     inplace = flce.plan(16384, 4096, 128256, "bf16")
-    assert p["workspace_bytes"] < inplace["workspace_bytes"] / 4
+    assert p["workspace_bytes"] < inplace["workspace_bytes"] / 3
     # doubling V changes only the per-token log-sum-exp partials
     q = flce.plan(16384, 4096, 256512, "bf16", dlogits_mode="slabs", chunk=p["chunk"])
     assert q["vocab_slab"] == vs
@@ -227,8 +231,17 @@ def test_plan_picks_tile_shapes_per_gemm():
     # the slab walk keeps the wide tiles its slab sizing assumes
     s = flce.plan(16384, 4096, 128256, dlogits_mode="slabs")
     assert (s["tile_n"], s["tile_n_dx"], s["tile_n_dw"]) == (512, 512, 512)
-    # the 64-unit dx launch of the small shape runs with dW beside it; the
-    # 512-unit one of the Llama-3 shape does not; single-CTA tiles never do
-    assert p["dw_beside_dx"] == 1
-    assert flce.plan(16384, 4096, 128256)["dw_beside_dx"] == 0
-    assert flce.plan(2048, 1024, 32000, cta="single")["dw_beside_dx"] == 0
+    # wide dx and dW GEMMs share one dynamically scheduled launch by default;
+    # separate launches put the small shape's 64-unit dx launch beside dW,
+    # not the Llama-3 shape's 512-unit one; single-CTA tiles do neither
+    assert (p["backward_one_launch"], p["dw_beside_dx"]) == (1, 0)
+    assert (q["backward_one_launch"], r["backward_one_launch"], n["backward_one_launch"]) == (1, 0, 0)
+    sep = flce.plan(2048, 1024, 32000, backward="separate")
+    assert (sep["backward_one_launch"], sep["dw_beside_dx"]) == (0, 1)
+    assert flce.plan(16384, 4096, 128256, backward="separate")["dw_beside_dx"] == 0
+    assert flce.plan(16384, 4096, 128256)["backward_one_launch"] == 1
+    one = flce.plan(2048, 256, 32000, backward="one_launch")   # one launch on dx's pair tiles
+    assert (one["backward_one_launch"], one["tile_n_dx"], one["tile_n_dw"]) == (1, 256, 256)
+    single = flce.plan(2048, 1024, 32000, cta="single", backward="one_launch")
+    assert (single["backward_one_launch"], single["dw_beside_dx"]) == (0, 0)
+    assert flce.plan(16384, 4096, 128256, dlogits_mode="slabs")["backward_one_launch"] == 0

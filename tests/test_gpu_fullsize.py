@@ -2,8 +2,10 @@
 times (default HBM budget, planned chunk), on outputs the fp64 oracle computes
 one by one: the loss (from every token's log-sum-exp), sampled token losses,
 sampled rows of dx, sampled rows of dW; plus properties that hold at any
-size. The Qwen3-shaped batch runs its default-budget plan (C = 3328, a
-ragged last chunk) and the chunk sweep C in {1024, 2048, 4096, 8192}. The
+size. The Qwen3-shaped batch runs its default-budget plan (C = 4096, the
+backward GEMMs in one launch), the same budget with separate backward
+launches (C = 3328, a ragged last chunk) and the chunk sweep
+C in {1024, 2048, 4096, 8192}. The
 131,072-token batch has a module of its own (test_zy_long_context.py)."""
 import numpy as np
 import pytest
@@ -127,8 +129,9 @@ def test_qwen3_chunk_sweep(qwen3, chunk):
 
 
 def test_qwen3_bench_configuration(qwen3):
-    """The default HBM budget, as bench.py runs it: the planner takes
-    C = 3328, five chunks, the last one ragged (3072 tokens)."""
+    """The default HBM budget, as bench.py runs it: the dx and dW GEMMs share
+    one launch with an unsplit dx reduction, which leaves room for C = 4096,
+    four chunks."""
     from linear_cross_entropy_token_gb300 import FLCE
     w, ref = qwen3
     h = FLCE("bf16", 0)
@@ -136,7 +139,22 @@ def test_qwen3_bench_configuration(qwen3):
         plan = _check(h, w, ref)
     finally:
         h.close()
-    assert plan["chunk"] == 3328 and plan["num_chunks"] == 5
+    assert (plan["chunk"], plan["num_chunks"], plan["dx_splits"]) == (4096, 4, 1)
+    assert plan["backward_one_launch"] == 1
+
+
+def test_qwen3_separate_backward_launches(qwen3):
+    """The default budget with the dx and dW GEMMs in launches of their own:
+    five dx splits leave room for C = 3328, five chunks, the last one ragged
+    (3072 tokens)."""
+    from linear_cross_entropy_token_gb300 import FLCE
+    w, ref = qwen3
+    h = FLCE("bf16", 0, backward="separate")
+    try:
+        plan = _check(h, w, ref)
+    finally:
+        h.close()
+    assert (plan["chunk"], plan["num_chunks"], plan["backward_one_launch"]) == (3328, 5, 0)
     assert w.N - 4 * plan["chunk"] == 3072
 
 

@@ -14,12 +14,14 @@ from flce_testing import assert_parity, device_inputs, rel_fro, run, to_np64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=["single", "pair", "pair-one_launch", "wide", "auto"])
+@pytest.fixture(scope="module", params=["single", "pair", "pair-one_launch", "wide", "wide-one_launch",
+                                        "auto", "auto-one_launch"])
 def bf16(request):
     """Every GEMM tile shape: one CTA per 128 x 256 tile; CTA pairs per
-    256 x 256 tile, with the dx and dW GEMMs in one dynamically scheduled
-    launch or in two launches; CTA pairs per 256 x 512 tile; and the default,
-    which picks wide or pair tiles per GEMM."""
+    256 x 256 tile and per 256 x 512 tile, each with the dx and dW GEMMs in
+    one dynamically scheduled launch or in two launches; and the default,
+    which picks wide or pair tiles per GEMM (one launch then runs on the dx
+    GEMM's tile shape)."""
     from linear_cross_entropy_token_gb300 import FLCE
     cta, _, sep = request.param.partition("-")
     h = FLCE("bf16", 0, hbm_budget_bytes=4 << 30, cta=cta,

@@ -1,7 +1,8 @@
 """Parity with the fp64 oracle on seeded random shapes: token counts, hidden
 sizes (multiples of 8), vocabulary sizes, ignore fractions, target
 distributions and chunk sizes drawn per case, rotating over the tile shapes (the
-default picks wide or pair tiles per GEMM), one
+default picks wide or pair tiles per GEMM; wide tiles also with the dx and dW
+GEMMs in one dynamically scheduled launch), one
 handle per shape reused across the cases (workspace growth, cached tile
 orders, changing tensor maps)."""
 import numpy as np
@@ -13,13 +14,16 @@ from flce_testing import assert_parity, run
 
 pytestmark = pytest.mark.gpu
 
-SHAPES = ("single", "pair", "wide", "auto")
+SHAPES = ("single", "pair", "wide", "auto", "wide-one_launch")
 
 
 @pytest.fixture(scope="module")
 def handles():
     from linear_cross_entropy_token_gb300 import FLCE
-    hs = {c: FLCE("bf16", 0, hbm_budget_bytes=2 << 30, cta=c) for c in SHAPES}
+    hs = {}
+    for c in SHAPES:
+        cta, _, backward = c.partition("-")
+        hs[c] = FLCE("bf16", 0, hbm_budget_bytes=2 << 30, cta=cta, backward=backward or "auto")
     yield hs
     for h in hs.values():
         h.close()
