@@ -509,7 +509,8 @@ def run_ours(args, ws, rank, local):
                                    (256, 512): "256x512, CTA pairs sharing A through the collector"}[
                                       (plan["tile_m"], plan["tile_n"])]
                                   if bf16 else "fp32 CUDA-core GEMMs"),
-                   "backward_gemms": "one launch" if args.backward == "one_launch" else "two launches",
+                   "backward_gemms": ("one launch, work units handed out dynamically (dx first)"
+                                      if plan["backward_one_launch"] else "two launches"),
                    "targets": w.spec.targets, "ignore_frac": float(w.spec.ignore_frac),
                    "l2": l2_note(V * H * esize, plan["logits_bytes"]),
                    "parallelism": "replicas" if ws > 1 else "single"},

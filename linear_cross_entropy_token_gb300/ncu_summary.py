@@ -31,6 +31,7 @@ _PLAIN = {"count_valid_kernel": "count_valid", "lse_combine_kernel": "lse_combin
           "simt_gemm_f32_kernel": "simt_gemm_f32", "simt_tile_stats_kernel": "simt_tile_stats_f32",
           "simt_splitk_reduce_kernel": "simt_splitk_reduce_f32",
           "wait_check_kernel": "wait_check", "umma_pair_dual_kernel": "gemm_dx_dw",
+          "umma_wide_dual_kernel": "gemm_dx_dw",
           "device_result_kernel": "device_result"}
 
 RAW_METRICS = [
@@ -106,7 +107,8 @@ def traffic(rep_path: str, chunks: int = 0):
     """DRAM bytes per launch per kernel kind. With chunks = K > 0 the capture
     holds the first chunks of one call: the dW GEMM's first launch stores dW
     and its later ones add into it, so its per-launch figure is the mean over
-    a K-chunk call, (first + (K - 1) x mean of the others) / K."""
+    a K-chunk call, (first + (K - 1) x mean of the others) / K; the same for
+    the launch that runs the dx and dW GEMMs together."""
     per = collections.OrderedDict()
     for d in raw(rep_path):
         if d.get("dram_read_MB") is None:
@@ -114,7 +116,7 @@ def traffic(rep_path: str, chunks: int = 0):
         per.setdefault(d["kernel"], []).append((d["dram_read_MB"] + d["dram_write_MB"]) * 1e6)
     out = {}
     for k, v in per.items():
-        if chunks > 0 and k == "gemm_dw" and len(v) > 1:
+        if chunks > 0 and k in ("gemm_dw", "gemm_dx_dw") and len(v) > 1:
             per_launch = (v[0] + (chunks - 1) * sum(v[1:]) / len(v[1:])) / chunks
         else:
             per_launch = sum(v) / len(v)
