@@ -32,8 +32,8 @@ UNIT = "tokens/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-HBM_BOUND = {"dlogits_inplace", "lse_combine", "dx_split_reduce", "count_valid", "loss_finalize",
-             "device_result"}
+HBM_BOUND = {"dlogits_inplace", "lse_combine", "combine_dlogits", "dx_split_reduce", "count_valid",
+             "loss_finalize", "device_result"}
 ALU_BOUND = {"simt_gemm_f32"}
 
 

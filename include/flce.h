@@ -180,13 +180,18 @@ enum {
     FLCE_K_GEMM_DX = 5,          /* dx_c = dlogits·W on tcgen05                        */
     FLCE_K_DX_REDUCE = 6,        /* sums the dx split partials into bf16 dx            */
     FLCE_K_GEMM_DW = 7,          /* dW (+)= dlogitsᵀ·x_c on tcgen05, fp32              */
-    FLCE_K_LOSS_FINALIZE = 8,    /* fixed-order sum of token losses / n_valid          */
+    FLCE_K_LOSS_FINALIZE = 8,    /* fixed-order sum of token losses / n_valid (bf16
+                                    calls run it in their last DX_REDUCE launch unless
+                                    dW work on the second stream is still to join)    */
     FLCE_K_SIMT_GEMM = 9,        /* fp32 path: CUDA-core GEMMs                         */
     FLCE_K_SIMT_TILE_STATS = 10, /* fp32 path: per-vocab-tile max/sum-exp              */
     FLCE_K_GEMM_DX_DW = 11,      /* CTA pairs: the dx and dW GEMMs of a chunk in one launch */
     FLCE_K_DEVICE_RESULT = 12,   /* loss and n_valid into caller device memory (an
                                     empty batch; otherwise the loss reduction writes them) */
-    FLCE_K_NUM_KINDS = 13
+    FLCE_K_COMBINE_DLOGITS = 13, /* LSE_COMBINE and DLOGITS in one launch, one block per
+                                    token row (in-place mode, chunk rows of at most
+                                    32768 columns)                                    */
+    FLCE_K_NUM_KINDS = 14
 };
 
 typedef struct flce_kernel_profile {

@@ -1020,8 +1020,12 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
   h->token_loss_off = L.token_loss;
   h->has_plan = true;
 
-  // per-call words; the sticky error word only when the block is new
-  cudaError_t e = cudaMemsetAsync(ctrl, 0, (h->ws_fresh ? kCtrlWords : kCtrlSticky) * 4, s);
+  // per-call words: count_valid, the call's first kernel, clears them; a
+  // memset only for an empty batch (no count_valid) and, once, to clear the
+  // sticky error word of a new block
+  cudaError_t e = cudaSuccess;
+  if (h->ws_fresh || N == 0)
+    e = cudaMemsetAsync(ctrl, 0, (h->ws_fresh ? kCtrlWords : kCtrlSticky) * 4, s);
   if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
   h->ws_fresh = false;
   if (N == 0) {
@@ -1050,6 +1054,8 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     }
   } side_join{h, s, side_pending};
   const double dV = static_cast<double>(V), dH = static_cast<double>(H);
+  int32_t sched_claims = 0;  // work-unit claims of this call's dynamically scheduled launches
+  bool loss_done = false;    // the last dx reduction has taken the loss reduction
 
   if (!bf16) {
     // ---------------------------------------------------------- fp32 path
@@ -1178,9 +1184,12 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       FLCE_LAUNCH(FLCE_K_GEMM_LOGITS, 2 * dr * dH * dV,
                   2 * dr * dH + 2 * dV * dH + ((recompute || slabs) ? 0 : 2 * dr * dV) + 8 * dr * vt + 12 * dr,
                   launch_gemm(h, shape_for(h, p.tile_n), kUmmaLogits, mX_k, mW_k, mZ_out, a, rows, s));
-      // 2a. cross-tile log-sum-exp and token losses
-      FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
-                  launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
+      // 2a. cross-tile log-sum-exp and token losses (for short rows in one
+      // launch with the dlogits pass, 2b)
+      const bool fused_rows = !recompute && !slabs && ldv <= combine_dlogits_max_cols();
+      if (!fused_rows)
+        FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
+                    launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
       if (slabs) {
         const SlabChunk k{&p, &a, &mX_k, &mX_mn, static_cast<const __nv_bfloat16*>(W), dW, logits,
                           dxpart, dxb + off * H, t + off, dcorr, ctrl, H, V, C, c, ignore_index, rows,
@@ -1193,6 +1202,10 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       if (recompute) {
         FLCE_LAUNCH(FLCE_K_GEMM_DLOGITS, 2 * dr * dH * dV, 2 * dr * dH + 2 * dV * dH + 2 * dr * dV + 12 * dr,
                     launch_gemm(h, shape_for(h, p.tile_n), kUmmaDlogits, mX_k, mW_k, mZ_out, a, rows, s));
+      } else if (fused_rows) {
+        FLCE_LAUNCH(FLCE_K_COMBINE_DLOGITS, 0.0, 4 * dr * dV + 8 * dr * vt + 24 * dr,
+                    launch_combine_dlogits_bf16(logits, ldv, rows, V, partials, vt, zt, t + off, ignore_index,
+                                                ctrl, lse, token_loss + off, dcorr, s));
       } else {
         FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 4 * dr * dV,
                     launch_dlogits_bf16(logits, ldv, rows, V, partials, vt, lse, t + off, ignore_index,
@@ -1259,15 +1272,15 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
         da.units0 = da.p[0].num_m * da.p[0].num_n * da.p[0].num_s;
         da.p[0].group_m = group_for(h, shape, da.p[0].num_m, da.p[0].num_n, da.p[0].num_s,
                                     std::min(da.units0, slots_max));
-        da.pad = 0;
+        // the counter (cleared by count_valid) runs on across the call's launches
         da.sched_ctr = reinterpret_cast<int32_t*>(ctrl + kCtrlSched);
-        e = cudaMemsetAsync(da.sched_ctr, 0, 4, s);
-        if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+        da.sched_base = sched_claims;
         const int units = da.units0 + da.p[1].num_m * da.p[1].num_n;
         const int pairs = std::min(units, slots_max);
         FLCE_LAUNCH(FLCE_K_GEMM_DX_DW, 4 * dr * dV * dH, dx_bytes + dw_bytes,
                     wide ? launch_umma_wide_dual(maps, da, pairs, s)
                          : launch_umma_pair_dual(maps, da, pairs, s));
+        sched_claims += units + pairs;
       } else if (overlap_dw) {
         // the dx GEMM fills less than kOverlapWaves waves of the GPU: the dW
         // GEMM runs beside it on the side stream (both only read the finished
@@ -1292,9 +1305,15 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
         FLCE_LAUNCH(FLCE_K_GEMM_DW, 2 * dr * dV * dH, dw_bytes,
                     launch_gemm(h, shape_for(h, p.tile_n_dw), kUmmaDw, mZ_mn, mX_mn, mDw, d, V, s));
       }
-      FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4.0 * S * dr * dH + 4 * dr * dH,
+      // the last chunk's reduction also takes the loss reduction, unless dW
+      // work on the side stream (which may record an error) is still to join
+      const bool finish = c == p.num_chunks - 1 && !side_pending;
+      FLCE_LAUNCH(FLCE_K_DX_REDUCE, 0.0, 4.0 * S * dr * dH + 4 * dr * dH + (finish ? 4.0 * N : 0.0),
                   launch_dx_reduce(dxpart, S, C * H, rows, H, static_cast<const __nv_bfloat16*>(W), V,
-                                   t + off, ignore_index, ctrl, dcorr, dxb + off * H, s));
+                                   t + off, ignore_index, ctrl, dcorr, dxb + off * H, s,
+                                   finish ? token_loss : nullptr, N, dres ? 1 : 0,
+                                   dres ? dres->loss : nullptr, dres ? dres->n_valid : nullptr));
+      loss_done = finish;
     }
   }
   if (side_pending) {
@@ -1304,9 +1323,10 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
     e = cudaStreamWaitEvent(s, h->slab_freed, 0);
     if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "slab join: %s", cudaGetErrorString(e));
   }
-  FLCE_LAUNCH(FLCE_K_LOSS_FINALIZE, 0.0, 4.0 * N,
-              launch_loss_finalize(token_loss, N, ctrl, dres ? 1 : 0, dres ? dres->loss : nullptr,
-                                   dres ? dres->n_valid : nullptr, s));
+  if (!loss_done)
+    FLCE_LAUNCH(FLCE_K_LOSS_FINALIZE, 0.0, 4.0 * N,
+                launch_loss_finalize(token_loss, N, ctrl, dres ? 1 : 0, dres ? dres->loss : nullptr,
+                                     dres ? dres->n_valid : nullptr, s));
   *ctrl_out = ctrl;
   return FLCE_OK;
 }
@@ -1357,6 +1377,7 @@ const char* flce_kernel_name(int32_t kind) {
     case FLCE_K_SIMT_TILE_STATS: return "simt_tile_stats_f32";
     case FLCE_K_GEMM_DX_DW: return "gemm_dx_dw";
     case FLCE_K_DEVICE_RESULT: return "device_result";
+    case FLCE_K_COMBINE_DLOGITS: return "combine_dlogits";
     default: return "?";
   }
 }

@@ -96,8 +96,10 @@ struct DualMaps {
 struct DualArgs {
   UmmaArgs p[2];
   int32_t units0;       // work units of problem 0
-  int32_t pad;
-  int32_t* sched_ctr;   // next unit to hand out; zero before each launch
+  int32_t sched_base;   // the counter's value when this launch starts
+  int32_t* sched_ctr;   // claims so far: each pair claims its units and then one
+                        // past the last, so a launch of U units on P pairs leaves
+                        // it at sched_base + U + P for the next launch of the call
 };
 cudaError_t launch_umma_pair_dual(const DualMaps& maps, const DualArgs& args, int pairs,
                                   cudaStream_t s);
@@ -125,10 +127,23 @@ cudaError_t launch_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int rows, int64
 cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, int64_t col_base,
                                const float* lse, const int64_t* t_chunk, int64_t ignore_index,
                                const uint32_t* ctrl, cudaStream_t s);
+// token_loss non-null: this is the call's last dx reduction, and it also
+// runs the loss reduction of launch_loss_finalize (same arguments)
 cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_stride, int rows,
                              int64_t H, const __nv_bfloat16* W, int64_t V, const int64_t* t_chunk,
-                             int64_t ignore_index, const uint32_t* ctrl, const float* dcorr,
-                             __nv_bfloat16* dx, cudaStream_t s);
+                             int64_t ignore_index, uint32_t* ctrl, const float* dcorr,
+                             __nv_bfloat16* dx, cudaStream_t s, const float* token_loss = nullptr,
+                             int64_t N = 0, int result = 0, float* loss_dev = nullptr,
+                             int32_t* n_valid_dev = nullptr);
+// The log-sum-exp combine and the in-place dlogits pass in one launch (one
+// block per token row), for buffers of at most combine_dlogits_max_cols()
+// columns (ldv); arguments as for the two launches it replaces.
+cudaError_t launch_combine_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int rows, int64_t V,
+                                        const float2* partials, int vocab_tiles, const float* zt,
+                                        const int64_t* t_chunk, int64_t ignore_index,
+                                        const uint32_t* ctrl, float* lse, float* token_loss_chunk,
+                                        float* dcorr, cudaStream_t s);
+int64_t combine_dlogits_max_cols();
 cudaError_t launch_device_result(uint32_t* ctrl, float* loss_dev, int32_t* n_valid_dev, cudaStream_t s);
 // result != 0: also write the sync-free entry points' device result (loss,
 // NaN after a recorded error; n_valid; the sticky error word)

@@ -27,7 +27,8 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // n_valid = #{i : t_i != ignore_index}; any other target outside [0, V)
-// records FLCE_ERR_BAD_TARGET. One block; fixed-order integer sum.
+// records FLCE_ERR_BAD_TARGET. One block; fixed-order integer sum. It first
+// clears the call's control words, so the call needs no memset of them.
 // nv_total (device, may be null) is the divisor of a token-sharded batch:
 // the number of non-ignored tokens over every shard. When given, it becomes
 // the n_valid word that every later step of the call divides by, and the
@@ -37,6 +38,10 @@ __global__ void count_valid_kernel(const int64_t* __restrict__ t, int64_t N, int
                                    int64_t ignore_index, const int32_t* __restrict__ nv_total,
                                    uint32_t* ctrl) {
   __shared__ uint32_t warp_cnt[32];
+  // the call's first kernel: its control words start at zero here (the
+  // sticky error word, kept across calls, excepted)
+  if (threadIdx.x < kCtrlSticky) ctrl[threadIdx.x] = 0u;
+  __syncthreads();
   uint32_t cnt = 0;
   bool bad = false;
   for (int64_t i = threadIdx.x; i < N; i += blockDim.x) {
@@ -110,29 +115,24 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   }
 }
 
-constexpr int kCombineThreads = 128;
-
-// One block of kCombineThreads per token row: each thread merges a strided
-// share of the row's partials (four loads in flight), then the warps and the
-// block merge their pairs in a fixed order.
-__global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(
-    const float2* __restrict__ partials, int vocab_tiles, const float* __restrict__ zt,
-    const int64_t* __restrict__ t, int rows, int64_t ignore_index, float* __restrict__ lse,
-    float* __restrict__ token_loss) {
-  __shared__ float2 warp_ms[kCombineThreads / 32];
-  const int r = blockIdx.x;
+// The log-sum-exp of one token row from its partials, on a block of
+// THREADS threads: each thread merges a strided share of the row's partials
+// (four loads in flight), then the warps and the block merge their pairs in
+// a fixed order. The result is valid in thread 0; warp_ms holds THREADS / 32
+// entries of shared memory.
+template <int THREADS>
+__device__ __forceinline__ float row_lse(const float2* __restrict__ p, int vocab_tiles, float2* warp_ms) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const float2* p = partials + static_cast<size_t>(r) * vocab_tiles;
   float M = -INFINITY, S = 0.f;
   int s = threadIdx.x;
-  for (; s + 3 * kCombineThreads < vocab_tiles; s += 4 * kCombineThreads) {
+  for (; s + 3 * THREADS < vocab_tiles; s += 4 * THREADS) {
     float2 q[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) q[j] = p[s + j * kCombineThreads];
+    for (int j = 0; j < 4; ++j) q[j] = p[s + j * THREADS];
 #pragma unroll
     for (int j = 0; j < 4; ++j) lse_merge(M, S, q[j].x, q[j].y);
   }
-  for (; s < vocab_tiles; s += kCombineThreads) {
+  for (; s < vocab_tiles; s += THREADS) {
     const float2 q = p[s];
     lse_merge(M, S, q.x, q.y);
   }
@@ -148,8 +148,23 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(
     M = warp_ms[0].x;
     S = warp_ms[0].y;
 #pragma unroll
-    for (int w = 1; w < kCombineThreads / 32; ++w) lse_merge(M, S, warp_ms[w].x, warp_ms[w].y);
-    const float l = M + logf(S);
+    for (int w = 1; w < THREADS / 32; ++w) lse_merge(M, S, warp_ms[w].x, warp_ms[w].y);
+  }
+  return M + logf(S);
+}
+
+constexpr int kCombineThreads = 128;
+
+// One block of kCombineThreads per token row.
+__global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(
+    const float2* __restrict__ partials, int vocab_tiles, const float* __restrict__ zt,
+    const int64_t* __restrict__ t, int rows, int64_t ignore_index, float* __restrict__ lse,
+    float* __restrict__ token_loss) {
+  __shared__ float2 warp_ms[kCombineThreads / 32];
+  const int r = blockIdx.x;
+  const float l = row_lse<kCombineThreads>(partials + static_cast<size_t>(r) * vocab_tiles, vocab_tiles,
+                                           warp_ms);
+  if (threadIdx.x == 0) {
     lse[r] = l;
     const int64_t tg = t[r];
     token_loss[r] = (tg == ignore_index) ? 0.f : (l - zt[r]);
@@ -175,28 +190,24 @@ constexpr int kDlogitsVecs = 4;
 constexpr int kDlogitsThreads = 256;
 constexpr int kDlogitsCols = kDlogitsThreads * 8 * kDlogitsVecs;  // columns per block
 
-__global__ void __launch_bounds__(kDlogitsThreads) dlogits_bf16_kernel(
-    __nv_bfloat16* __restrict__ buf, int64_t ldv, int64_t V, const float2* __restrict__ partials,
-    int vocab_tiles, const float* __restrict__ lse, const int64_t* __restrict__ t,
-    int64_t ignore_index, const uint32_t* __restrict__ ctrl, float* __restrict__ dcorr) {
-  const int r = blockIdx.y;
-  const int64_t tg = t[r];
-  const uint32_t nv = ctrl[kCtrlNValid];
-  const bool live = tg != ignore_index && nv > 0;
-  __nv_bfloat16* row = buf + static_cast<size_t>(r) * ldv;
-  const int64_t base = static_cast<int64_t>(blockIdx.x) * (blockDim.x * 8 * kDlogitsVecs);
-  if (!live) {
+// A dead row (ignored token, or no valid token in the batch): zeros, the
+// buffer not read.
+__device__ __forceinline__ void zero_cols(__nv_bfloat16* __restrict__ row, int64_t base, int64_t ldv) {
 #pragma unroll
-    for (int i = 0; i < kDlogitsVecs; ++i) {
-      const int64_t c0 = base + (static_cast<int64_t>(i) * blockDim.x + threadIdx.x) * 8;
-      if (c0 < ldv) *reinterpret_cast<uint4*>(row + c0) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    return;
+  for (int i = 0; i < kDlogitsVecs; ++i) {
+    const int64_t c0 = base + (static_cast<int64_t>(i) * blockDim.x + threadIdx.x) * 8;
+    if (c0 < ldv) *reinterpret_cast<uint4*>(row + c0) = make_uint4(0u, 0u, 0u, 0u);
   }
-  const float scale = 1.0f / static_cast<float>(nv);
-  const float lg_nv = __log2f(static_cast<float>(nv));
-  const float l = lse[r];
-  const float2* prow = partials + static_cast<size_t>(r) * vocab_tiles;
+}
+
+// The pass over kDlogitsCols columns of a live row from column `base`. l is
+// the row's log-sum-exp, tg its target, scale = 1/n_valid and lg_nv =
+// log2 n_valid; s_ll is shared scratch of kDlogitsCols / kVocabTile floats
+// (a caller that reuses it waits for the block between calls).
+__device__ __forceinline__ void dlogits_cols(__nv_bfloat16* __restrict__ row, int64_t base, int64_t ldv,
+                                             int64_t V, const float2* __restrict__ prow, int vocab_tiles,
+                                             float l, int64_t tg, float scale, float lg_nv,
+                                             float* __restrict__ dcorr_r, float* s_ll) {
   uint4 v[kDlogitsVecs];
 #pragma unroll
   for (int i = 0; i < kDlogitsVecs; ++i) {
@@ -205,7 +216,6 @@ __global__ void __launch_bounds__(kDlogitsThreads) dlogits_bf16_kernel(
   }
   // the block's per-group exponent offsets (lse - m_g)·log2 e, staged once in
   // shared memory while the vectors above are in flight
-  __shared__ float s_ll[kDlogitsCols / kVocabTile];
   {
     const int64_t g0 = base / kVocabTile;
     for (int q = threadIdx.x; q < kDlogitsCols / kVocabTile; q += blockDim.x)
@@ -242,12 +252,71 @@ __global__ void __launch_bounds__(kDlogitsThreads) dlogits_bf16_kernel(
         d0 = (j0 < V) ? d0 * scale : 0.f;
         d1 = (j0 + 1 < V) ? d1 * scale : 0.f;
         h = __floats2bfloat162_rn(d0, d1);
-        if (j0 == tg) dcorr[r] = d0 - __low2float(h);
-        if (j0 + 1 == tg) dcorr[r] = d1 - __high2float(h);
+        if (j0 == tg) *dcorr_r = d0 - __low2float(h);
+        if (j0 + 1 == tg) *dcorr_r = d1 - __high2float(h);
         w[q] = *reinterpret_cast<uint32_t*>(&h);
       }
     }
     *reinterpret_cast<uint4*>(row + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__global__ void __launch_bounds__(kDlogitsThreads) dlogits_bf16_kernel(
+    __nv_bfloat16* __restrict__ buf, int64_t ldv, int64_t V, const float2* __restrict__ partials,
+    int vocab_tiles, const float* __restrict__ lse, const int64_t* __restrict__ t,
+    int64_t ignore_index, const uint32_t* __restrict__ ctrl, float* __restrict__ dcorr) {
+  __shared__ float s_ll[kDlogitsCols / kVocabTile];
+  const int r = blockIdx.y;
+  const int64_t tg = t[r];
+  const uint32_t nv = ctrl[kCtrlNValid];
+  __nv_bfloat16* row = buf + static_cast<size_t>(r) * ldv;
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kDlogitsCols;
+  if (tg == ignore_index || nv == 0) {
+    zero_cols(row, base, ldv);
+    return;
+  }
+  dlogits_cols(row, base, ldv, V, partials + static_cast<size_t>(r) * vocab_tiles, vocab_tiles, lse[r], tg,
+               1.0f / static_cast<float>(nv), __log2f(static_cast<float>(nv)), dcorr + r, s_ll);
+}
+
+// The log-sum-exp combine and the dlogits pass of one token row in one block,
+// for chunk buffers of at most kFusedSteps x kDlogitsCols columns: the row's
+// log-sum-exp and token loss from its partials, then the row's columns
+// kDlogitsCols at a time. Where rows are this short, one launch per chunk
+// does the work of two.
+constexpr int kFusedSteps = 4;
+
+__global__ void __launch_bounds__(kDlogitsThreads) combine_dlogits_bf16_kernel(
+    __nv_bfloat16* __restrict__ buf, int64_t ldv, int64_t V, const float2* __restrict__ partials,
+    int vocab_tiles, const float* __restrict__ zt, const int64_t* __restrict__ t, int64_t ignore_index,
+    const uint32_t* __restrict__ ctrl, float* __restrict__ lse, float* __restrict__ token_loss,
+    float* __restrict__ dcorr) {
+  __shared__ float2 warp_ms[kDlogitsThreads / 32];
+  __shared__ float s_ll[kDlogitsCols / kVocabTile];
+  __shared__ float s_l;
+  const int r = blockIdx.x;
+  const float2* prow = partials + static_cast<size_t>(r) * vocab_tiles;
+  const int64_t tg = t[r];
+  const float lr = row_lse<kDlogitsThreads>(prow, vocab_tiles, warp_ms);
+  if (threadIdx.x == 0) {
+    lse[r] = lr;
+    token_loss[r] = (tg == ignore_index) ? 0.f : (lr - zt[r]);
+    s_l = lr;
+  }
+  __syncthreads();
+  const float l = s_l;
+  const uint32_t nv = ctrl[kCtrlNValid];
+  const bool live = tg != ignore_index && nv > 0;  // uniform across the block
+  const float scale = live ? 1.0f / static_cast<float>(nv) : 0.f;
+  const float lg_nv = live ? __log2f(static_cast<float>(nv)) : 0.f;
+  __nv_bfloat16* row = buf + static_cast<size_t>(r) * ldv;
+  for (int64_t base = 0; base < ldv; base += kDlogitsCols) {
+    if (!live) {
+      zero_cols(row, base, ldv);
+      continue;
+    }
+    dlogits_cols(row, base, ldv, V, prow, vocab_tiles, l, tg, scale, lg_nv, dcorr + r, s_ll);
+    __syncthreads();  // s_ll is staged again for the next columns
   }
 }
 
@@ -276,64 +345,23 @@ __global__ void dlogits_f32_kernel(float* __restrict__ buf, int64_t ldv, int64_t
   *ptr = make_float4(f[0], f[1], f[2], f[3]);
 }
 
-// dx row i = sum over splits of the fp32 partials of dlogits·W (in split
-// order) + dcorr[i]·W[t_i], rounded once to bf16. dcorr[i] is the fp32
-// rounding error of the bf16 dlogits entry at the target column, so the sum
-// is dx as if that entry, the largest of the row, had been stored exactly.
-// blockIdx.y = token row, 4 columns per thread.
-__global__ void dx_reduce_kernel(const float* __restrict__ part, int splits, int64_t split_stride,
-                                 int64_t H, const __nv_bfloat16* __restrict__ W, int64_t V,
-                                 const int64_t* __restrict__ t, int64_t ignore_index,
-                                 const uint32_t* __restrict__ ctrl, const float* __restrict__ dcorr,
-                                 __nv_bfloat16* __restrict__ dx) {
-  const int r = blockIdx.y;
-  const int64_t h = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
-  if (h >= H) return;
-  const int64_t tg = t[r];
-  const bool corr = tg != ignore_index && tg >= 0 && tg < V && ctrl[kCtrlNValid] > 0;
-  const int64_t i = static_cast<int64_t>(r) * H + h;
-  float4 acc = *reinterpret_cast<const float4*>(part + i);
-  for (int s = 1; s < splits; ++s) {
-    const float4 v = *reinterpret_cast<const float4*>(part + s * split_stride + i);
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
-  }
-  if (corr) {
-    const float c = dcorr[r];
-    const uint2 wv = *reinterpret_cast<const uint2*>(W + tg * H + h);
-    const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.x));
-    const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.y));
-    acc.x = fmaf(w01.x, c, acc.x);
-    acc.y = fmaf(w01.y, c, acc.y);
-    acc.z = fmaf(w23.x, c, acc.z);
-    acc.w = fmaf(w23.y, c, acc.w);
-  }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-  uint2 o;
-  o.x = *reinterpret_cast<uint32_t*>(&lo);
-  o.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(dx + i) = o;
-}
-
-// loss = (sum of token losses) / n_valid, the sum in float64 and fixed order:
-// each thread sums a fixed strided set, then warp shuffles and one warp merge
-// the partial sums in a fixed tree. With `result` set it also writes the
-// device result of the sync-free entry points (as device_result_kernel).
-__global__ void __launch_bounds__(1024) loss_finalize_kernel(const float* __restrict__ token_loss,
-                                                             int64_t N, uint32_t* ctrl, int result,
-                                                             float* loss_dev, int32_t* n_valid_dev) {
-  __shared__ double warp_sum[32];
+// loss = (sum of token losses) / n_valid, the sum in float64 and fixed order
+// on a block of THREADS threads: each thread sums a fixed strided set, then
+// warp shuffles and one warp merge the partial sums in a fixed tree. With
+// `result` set it also writes the device result of the sync-free entry
+// points (as device_result_kernel). Every thread of the block calls it.
+template <int THREADS>
+__device__ __forceinline__ void loss_reduce(const float* __restrict__ token_loss, int64_t N, uint32_t* ctrl,
+                                            int result, float* loss_dev, int32_t* n_valid_dev) {
+  __shared__ double warp_sum[THREADS / 32];
   double s = 0.0;
-  for (int64_t i = threadIdx.x; i < N; i += blockDim.x) s += static_cast<double>(token_loss[i]);
+  for (int64_t i = threadIdx.x; i < N; i += THREADS) s += static_cast<double>(token_loss[i]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
   if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = s;
   __syncthreads();
   if (threadIdx.x < 32) {
-    double w = threadIdx.x < (blockDim.x >> 5) ? warp_sum[threadIdx.x] : 0.0;
+    double w = threadIdx.x < THREADS / 32 ? warp_sum[threadIdx.x] : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) w += __shfl_down_sync(0xffffffffu, w, o);
     if (threadIdx.x == 0) {
@@ -348,6 +376,72 @@ __global__ void __launch_bounds__(1024) loss_finalize_kernel(const float* __rest
       }
     }
   }
+}
+
+constexpr int kReduceThreads = 128;
+
+// dx row i = sum over splits of the fp32 partials of dlogits·W (in split
+// order) + dcorr[i]·W[t_i], rounded once to bf16. dcorr[i] is the fp32
+// rounding error of the bf16 dlogits entry at the target column, so the sum
+// is dx as if that entry, the largest of the row, had been stored exactly.
+// blockIdx.y = token row, 4 columns per thread.
+//
+// The call's last dx reduction can also take the loss reduction (fin.on):
+// block (0, 0) runs it beside its dx columns. It reads only the token losses
+// and control words of earlier launches, so no block waits for another; the
+// call saves the launch of loss_finalize_kernel.
+struct LossFinish {
+  int on;
+  int result;
+  const float* token_loss;
+  int64_t N;
+  float* loss_dev;
+  int32_t* n_valid_dev;
+};
+
+__global__ void __launch_bounds__(kReduceThreads) dx_reduce_kernel(
+    const float* __restrict__ part, int splits, int64_t split_stride, int64_t H,
+    const __nv_bfloat16* __restrict__ W, int64_t V, const int64_t* __restrict__ t, int64_t ignore_index,
+    uint32_t* ctrl, const float* __restrict__ dcorr, __nv_bfloat16* __restrict__ dx, LossFinish fin) {
+  const int r = blockIdx.y;
+  const int64_t h = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (h < H) {
+    const int64_t tg = t[r];
+    const bool corr = tg != ignore_index && tg >= 0 && tg < V && ctrl[kCtrlNValid] > 0;
+    const int64_t i = static_cast<int64_t>(r) * H + h;
+    float4 acc = *reinterpret_cast<const float4*>(part + i);
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(part + s * split_stride + i);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if (corr) {
+      const float c = dcorr[r];
+      const uint2 wv = *reinterpret_cast<const uint2*>(W + tg * H + h);
+      const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.x));
+      const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.y));
+      acc.x = fmaf(w01.x, c, acc.x);
+      acc.y = fmaf(w01.y, c, acc.y);
+      acc.z = fmaf(w23.x, c, acc.z);
+      acc.w = fmaf(w23.y, c, acc.w);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&lo);
+    o.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dx + i) = o;
+  }
+  if (fin.on && blockIdx.x == 0 && blockIdx.y == 0)
+    loss_reduce<kReduceThreads>(fin.token_loss, fin.N, ctrl, fin.result, fin.loss_dev, fin.n_valid_dev);
+}
+
+__global__ void __launch_bounds__(1024) loss_finalize_kernel(const float* __restrict__ token_loss,
+                                                             int64_t N, uint32_t* ctrl, int result,
+                                                             float* loss_dev, int32_t* n_valid_dev) {
+  loss_reduce<1024>(token_loss, N, ctrl, result, loss_dev, n_valid_dev);
 }
 
 // The call's result into caller device memory, for the entry point that
@@ -410,14 +504,31 @@ cudaError_t launch_dlogits_f32(float* buf, int64_t ldv, int rows, int64_t V, int
 
 cudaError_t launch_dx_reduce(const float* partials, int splits, int64_t split_stride, int rows,
                              int64_t H, const __nv_bfloat16* W, int64_t V, const int64_t* t_chunk,
-                             int64_t ignore_index, const uint32_t* ctrl, const float* dcorr,
-                             __nv_bfloat16* dx, cudaStream_t s) {
-  const int threads = 128;  // H % 8 == 0: 4 columns per thread, no partial vectors
-  dim3 grid(static_cast<unsigned>((H / 4 + threads - 1) / threads), static_cast<unsigned>(rows));
-  dx_reduce_kernel<<<grid, threads, 0, s>>>(partials, splits, split_stride, H, W, V, t_chunk,
-                                            ignore_index, ctrl, dcorr, dx);
+                             int64_t ignore_index, uint32_t* ctrl, const float* dcorr,
+                             __nv_bfloat16* dx, cudaStream_t s, const float* token_loss, int64_t N,
+                             int result, float* loss_dev, int32_t* n_valid_dev) {
+  // H % 8 == 0: 4 columns per thread, no partial vectors
+  dim3 grid(static_cast<unsigned>((H / 4 + kReduceThreads - 1) / kReduceThreads), static_cast<unsigned>(rows));
+  const LossFinish fin{token_loss ? 1 : 0, result, token_loss, N, loss_dev, n_valid_dev};
+  dx_reduce_kernel<<<grid, kReduceThreads, 0, s>>>(partials, splits, split_stride, H, W, V, t_chunk,
+                                                   ignore_index, ctrl, dcorr, dx, fin);
   return cudaGetLastError();
 }
+
+cudaError_t launch_combine_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int rows, int64_t V,
+                                        const float2* partials, int vocab_tiles, const float* zt,
+                                        const int64_t* t_chunk, int64_t ignore_index,
+                                        const uint32_t* ctrl, float* lse, float* token_loss_chunk,
+                                        float* dcorr, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (ldv > static_cast<int64_t>(kFusedSteps) * kDlogitsCols) return cudaErrorInvalidValue;
+  combine_dlogits_bf16_kernel<<<rows, kDlogitsThreads, 0, s>>>(buf, ldv, V, partials, vocab_tiles, zt,
+                                                               t_chunk, ignore_index, ctrl, lse,
+                                                               token_loss_chunk, dcorr);
+  return cudaGetLastError();
+}
+
+int64_t combine_dlogits_max_cols() { return static_cast<int64_t>(kFusedSteps) * kDlogitsCols; }
 
 cudaError_t launch_loss_finalize(const float* token_loss, int64_t N, uint32_t* ctrl, int result,
                                  float* loss_dev, int32_t* n_valid_dev, cudaStream_t s) {

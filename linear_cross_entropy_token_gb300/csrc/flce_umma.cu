@@ -944,7 +944,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
 //
 // The units differ in length (a dx unit runs ~1000 k-blocks, a dW unit 64),
 // so they are handed out dynamically: the even CTA's producer claims the next
-// unit from a global counter (dx units first) and publishes its index in a
+// unit from a global counter (dx units first; the counter runs on across the
+// launches of a call, each launch told where it starts) and publishes its index in a
 // 4-deep ring in shared memory, to its own MMA issuer and epilogue and, over
 // distributed shared memory, to the odd CTA's producer and epilogue. Each of
 // those four consumers releases the slot on an mbarrier of the even CTA. A
@@ -1062,8 +1063,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             failed = true;
             break;
           }
-          u = atomicAdd(d.sched_ctr, 1);
-          if (u >= num_units) u = -1;
+          u = atomicAdd(d.sched_ctr, 1) - d.sched_base;
+          if (u < 0 || u >= num_units) u = -1;
           sched_u[slot] = u;
           st_shared_cluster_u32(mapa_shared(su0 + 4u * slot, 1), static_cast<uint32_t>(u));
           mbar_arrive(sfull_bar(slot));
@@ -1331,8 +1332,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
               failed = true;
               break;
             }
-            u = atomicAdd(d.sched_ctr, 1);
-            if (u >= num_units) u = -1;
+            u = atomicAdd(d.sched_ctr, 1) - d.sched_base;
+            if (u < 0 || u >= num_units) u = -1;
             sched_u[slot] = u;
             st_shared_cluster_u32(mapa_shared(su0 + 4u * slot, 1), static_cast<uint32_t>(u));
             mbar_arrive(sfull_bar(slot));

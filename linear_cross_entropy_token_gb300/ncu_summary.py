@@ -25,7 +25,8 @@ import sys
 _GEMM = {(0, 0, 0): "gemm_logits_lse", (0, 0, 3): "gemm_dlogits_recompute", (0, 1, 2): "gemm_dx",
          (0, 1, 1): "gemm_dx_bf16", (1, 1, 2): "gemm_dw", (0, 0, 2): "gemm_check_kk",
          (1, 0, 2): "gemm_check_mk"}
-_PLAIN = {"count_valid_kernel": "count_valid", "lse_combine_kernel": "lse_combine",
+_PLAIN = {"combine_dlogits_bf16_kernel": "combine_dlogits",   # before its substring below
+          "count_valid_kernel": "count_valid", "lse_combine_kernel": "lse_combine",
           "dlogits_bf16_kernel": "dlogits_inplace", "dlogits_f32_kernel": "dlogits_inplace_f32",
           "dx_reduce_kernel": "dx_split_reduce", "loss_finalize_kernel": "loss_finalize",
           "simt_gemm_f32_kernel": "simt_gemm_f32", "simt_tile_stats_kernel": "simt_tile_stats_f32",
