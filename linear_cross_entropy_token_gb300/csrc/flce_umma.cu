@@ -67,7 +67,7 @@ constexpr int kStagesWide = FLCE_WIDE_STAGES;
 constexpr int kEpiBufsWide = FLCE_WIDE_EPI_BUFS;            // staging buffers per epilogue
 constexpr uint32_t kStageBytesWide = kABytes + kBBytes;    // 48 KB per CTA
 constexpr uint32_t kSmemBytesWide = 1024 + kStagesWide * kStageBytesWide +
-                                    2 * kEpiBufsWide * kEpiBytes + (2 * kStagesWide + 3) * 8 + 16;
+                                    2 * kEpiBufsWide * kEpiBytes + (2 * kStagesWide + 4) * 8 + 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 192;
 // wide tiles: warpgroup 0 (TMA producer warp, MMA warp, two idle warps) and
@@ -359,6 +359,118 @@ __device__ __forceinline__ void epilogue_tile(const UmmaArgs& a, const CUtensorM
       if (g + kAhead < kG) tmem_ld_32x32b_x32(tbase + (g + kAhead) * 32, cur);
     }
   }
+}
+
+// The log-sum-exp epilogue of a wide tile (256 x 512 on the pair, 128 rows x
+// 512 columns of TMEM per CTA), for one of its two epilogue warpgroups (grp):
+// the warpgroup reads its 64-column groups of the accumulator's first half
+// (columns grp*128 .. grp*128+127) and hands that half back (release0), then
+// its groups of the second half (256 + grp*128 ..) and hands that back
+// (release1). With both warpgroups done with the first half, the MMA issuer
+// starts the next tile's first-half MMAs while the second half is still
+// being read. The arithmetic per group is that of epilogue_tile<kEpiLse>:
+// max m_g, the target logit, y = z - m_g packed as bf16 in registers; the
+// sums of exp and the stores of y follow the second release. tbase is the
+// accumulator's column 0 at this thread's TMEM lane; n0 the tile's first
+// output column.
+template <class Release0, class Release1>
+__device__ __forceinline__ void epilogue_lse_wide(const UmmaArgs& a, const CUtensorMap* tmO, uint8_t* sE,
+                                                  uint32_t& ebuf, int row, bool leader, int m0, int n0,
+                                                  int grp, uint32_t tbase, Release0&& release0,
+                                                  Release1&& release1, uint32_t bar) {
+  constexpr int kGroups = 4;
+  const int grow = m0 + row;
+  const bool rvalid = grow < a.rows;
+  int64_t tg = -1;
+  if (rvalid) tg = a.targets[grow];
+  const int64_t tl = (rvalid && tg != a.ignore_index) ? tg - a.col_base : -1;
+  // tile column of group q: two groups in each half
+  auto col_of = [&](int q) { return (q < 2 ? 0 : kBN) + grp * 128 + (q & 1) * 64; };
+  uint32_t y[kGroups][32];
+  float mg[kGroups];
+  float zt = 0.f;
+  bool zt_here = false;
+#pragma unroll
+  for (int q = 0; q < kGroups; ++q) {
+    const int c = n0 + col_of(q);  // output column of the group's first entry (uniform)
+    if (c < a.cols) {
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(tbase + col_of(q), r0);
+      tmem_ld_32x32b_x32(tbase + col_of(q) + 32, r1);
+      tmem_ld_wait();
+      tmem_regs_ready(r0);
+      tmem_regs_ready(r1);
+      if (q == 1) release0();
+      if (q == 3) release1();
+      const int ncv = a.cols - c;  // valid columns in the group (uniform)
+      if (ncv < 64) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i >= ncv) r0[i] = 0xFF800000u;  // -inf
+          if (i + 32 >= ncv) r1[i] = 0xFF800000u;
+        }
+      }
+      float m8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m8[j] = fmaxf(__uint_as_float(r0[j]), __uint_as_float(r1[j]));
+#pragma unroll
+      for (int i = 8; i < 32; ++i) {
+        m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(r0[i]));
+        m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(r1[i]));
+      }
+      const float m = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                            fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      if (tl >= c && tl < c + 64) {
+        const int k = static_cast<int>(tl - c);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i == k) zt = __uint_as_float(r0[i]);
+          if (i + 32 == k) zt = __uint_as_float(r1[i]);
+        }
+        zt_here = true;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        y[q][i] = pack_bf16x2(__uint_as_float(r0[2 * i]) - m, __uint_as_float(r0[2 * i + 1]) - m);
+        y[q][16 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]) - m, __uint_as_float(r1[2 * i + 1]) - m);
+      }
+      mg[q] = m;
+    } else {
+      // a group past the last column: nothing to read
+      if (q == 1) release0();
+      if (q == 3) release1();
+    }
+  }
+  // both halves are free: sums of exp and stores
+  const size_t prow = static_cast<size_t>(grow) * a.vocab_tiles;
+#pragma unroll
+  for (int q = 0; q < kGroups; ++q) {
+    const int c = n0 + col_of(q);
+    if (c >= a.cols) continue;  // uniform
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      s4[i & 3] += ex2_approx(__uint_as_float(y[q][i] << 16) * kLog2e);
+      s4[(i + 2) & 3] += ex2_approx(__uint_as_float(y[q][i] & 0xFFFF0000u) * kLog2e);
+    }
+    if (rvalid) a.partials[prow + c / 64] = make_float2(mg[q], (s4[0] + s4[1]) + (s4[2] + s4[3]));
+    if (a.store_logits) {
+      // stage one 16 KB sub-tile and hand it to the TMA unit
+      uint8_t* buf = sE + ebuf * kEpiBytes;
+      if (leader) bulk_wait_group_read<kEpiBufsWide - 1>();
+      named_bar_sync(bar, kEpiThreads);
+      stage_row(buf, row, y[q]);
+      fence_proxy_async_smem();
+      named_bar_sync(bar, kEpiThreads);
+      if (leader) {
+        tma_store_2d(tmO, smem_u32(buf), c, m0);
+        bulk_commit_group();
+      }
+      __syncwarp();
+      if (kEpiBufsWide == 2) ebuf ^= 1u;
+    }
+  }
+  if (rvalid && zt_here) a.zt[grow] = zt;
 }
 
 // ===================================================== single-CTA kernel
@@ -745,14 +857,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
   uint8_t* sB = smem + kStagesWide * kABytes;
   uint8_t* sE = sB + kStagesWide * kBBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sE + 2 * kEpiBufsWide * kEpiBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesWide + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStagesWide + 4);
 
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStagesWide + s); };
   const uint32_t tfull_bar = bar0 + 8u * (2 * kStagesWide);
-  const uint32_t tempty_bar = bar0 + 8u * (2 * kStagesWide + 1);
+  // the accumulator's two 256-column halves are handed back separately
+  const uint32_t tempty0_bar = bar0 + 8u * (2 * kStagesWide + 1);
   const uint32_t drain_bar = bar0 + 8u * (2 * kStagesWide + 2);
+  const uint32_t tempty1_bar = bar0 + 8u * (2 * kStagesWide + 3);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -766,7 +880,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
       mbar_init(empty_bar(s), 1);    // each CTA's own, released by the pair's MMA commit
     }
     mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, 2 * 2 * kEpiThreads);  // used in CTA 0: both CTAs' two epilogues arrive
+    mbar_init(tempty0_bar, 2 * 2 * kEpiThreads);  // used in CTA 0: both CTAs' two epilogues arrive
+    mbar_init(tempty1_bar, 2 * 2 * kEpiThreads);
     mbar_init(drain_bar, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -842,16 +957,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
         uint32_t n_consumed = 0;
         bool issued = false, failed = false;
         int it = 0;
+        // the MMAs of one k-block (four k-steps) at ring stage `stage`: both
+        // halves sharing A through the collector (half < 0), or one half
+        // with A read from shared memory
+        auto mma_kblock = [&](int stage, int half, bool first) {
+          const uint32_t sa = smem_u32(sA + stage * kABytes);
+          const uint32_t sb = smem_u32(sB + stage * kBBytes);
+  #pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = AMN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                    : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+            const uint32_t ko = BMN ? 2048u * k : 32u * k;
+            const uint64_t bd0 = BMN ? smem_desc_sw128(sb + ko, 8192u, 1024u)
+                                     : smem_desc_sw128(sb + ko, 16u, 1024u);
+            const uint64_t bd1 = BMN ? smem_desc_sw128(sb + kBHalfBytes + ko, 8192u, 1024u)
+                                     : smem_desc_sw128(sb + kBHalfBytes + ko, 16u, 1024u);
+            const uint32_t acc_in = (!first || k > 0) ? 1u : 0u;
+            if (half < 0) {
+              tc_mma_bf16_pair_a_fill(tmem_base, ad, bd0, idesc, acc_in);
+              tc_mma_bf16_pair_a_lastuse(tmem_base + kBN, ad, bd1, idesc, acc_in);
+            } else {
+              tc_mma_bf16_pair(tmem_base + half * kBN, ad, half ? bd1 : bd0, idesc, acc_in);
+            }
+          }
+        };
         for (int u = pair; u < num_units && !failed; u += npairs, ++it) {
           const Unit t = unit_coords(a, u);
           const int kb0 = t.s * a.kb_per_split;
           const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
-          if (!mbar_wait_bounded_cluster(tempty_bar, (it & 1) ^ 1u, a.ctrl, a.timeout_ns)) {
+          const uint32_t tph = (it & 1) ^ 1u;
+          if (!mbar_wait_bounded_cluster(tempty0_bar, tph, a.ctrl, a.timeout_ns)) {
             failed = true;
             break;
           }
           tc_fence_after();
-          for (int kb = kb0; kb < kb1; ++kb) {
+          // While the epilogue still reads the second half, the first half's
+          // MMAs of the tile's first k-blocks run (at most the ring's depth:
+          // their stages stay until the second half's MMAs have read them).
+          int deferred = 0;
+          {
+            const uint64_t t0 = globaltimer_ns();
+  #pragma unroll 1
+            for (uint32_t spin = 0; !mbar_try_wait_cluster(tempty1_bar, tph); ++spin) {
+              if (deferred < kStagesWide && kb0 + deferred < kb1) {
+                const uint32_t n = n_consumed + static_cast<uint32_t>(deferred);
+                if (mbar_try_wait_cluster(full_bar(n % kStagesWide), (n / kStagesWide) & 1u)) {
+                  tc_fence_after();
+                  mma_kblock(n % kStagesWide, 0, deferred == 0);
+                  issued = true;
+                  ++deferred;
+                  continue;
+                }
+              }
+              if ((spin & 63u) == 0u) {
+                if (ld_volatile_u32(a.ctrl) != 0u || globaltimer_ns() - t0 > a.timeout_ns) {
+                  atomicCAS(a.ctrl, 0u, kErrTimeout);
+                  failed = true;
+                  break;
+                }
+              }
+            }
+          }
+          if (failed) break;
+          tc_fence_after();
+          // the second half's MMAs of the deferred k-blocks, in k order
+          for (int j = 0; j < deferred; ++j) {
+            const int stage = (n_consumed + static_cast<uint32_t>(j)) % kStagesWide;
+            mma_kblock(stage, 1, j == 0);
+            tc_commit_pair_multicast(empty_bar(stage), 0x3);
+          }
+          n_consumed += static_cast<uint32_t>(deferred);
+          for (int kb = kb0 + deferred; kb < kb1; ++kb) {
             const int stage = n_consumed % kStagesWide;
             const uint32_t phase = (n_consumed / kStagesWide) & 1u;
             if (!mbar_wait_bounded_cluster(full_bar(stage), phase, a.ctrl, a.timeout_ns)) {
@@ -859,21 +1035,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t sa = smem_u32(sA + stage * kABytes);
-            const uint32_t sb = smem_u32(sB + stage * kBBytes);
-  #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              const uint64_t ad = AMN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
-                                      : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-              const uint32_t ko = BMN ? 2048u * k : 32u * k;
-              const uint64_t bd0 = BMN ? smem_desc_sw128(sb + ko, 8192u, 1024u)
-                                       : smem_desc_sw128(sb + ko, 16u, 1024u);
-              const uint64_t bd1 = BMN ? smem_desc_sw128(sb + kBHalfBytes + ko, 8192u, 1024u)
-                                       : smem_desc_sw128(sb + kBHalfBytes + ko, 16u, 1024u);
-              const uint32_t acc_in = (kb > kb0 || k > 0) ? 1u : 0u;
-              tc_mma_bf16_pair_a_fill(tmem_base, ad, bd0, idesc, acc_in);
-              tc_mma_bf16_pair_a_lastuse(tmem_base + kBN, ad, bd1, idesc, acc_in);
-            }
+            mma_kblock(stage, -1, kb == kb0);
             issued = true;
             tc_commit_pair_multicast(empty_bar(stage), 0x3);
             ++n_consumed;
@@ -910,18 +1072,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(wq * 32) << 16) + grp * kBN;
       const int m0 = t.m * 2 * kBM + static_cast<int>(rank) * kBM;
       const int n0 = t.n * 2 * kBN + grp * kBN;
-      auto release = [&] {
+      auto release_half = [&](uint32_t b) {
         tc_fence_before();
         if (rank == 0)
-          mbar_arrive(tempty_bar);
+          mbar_arrive(b);
         else
-          mbar_arrive_cluster(mapa_shared(tempty_bar, 0));
+          mbar_arrive_cluster(mapa_shared(b, 0));
       };
-      if (n0 < a.cols)
-        epilogue_tile<EPI, kEpiBufsWide>(a, &tmO, sEg, ebuf, row, leader, m0, n0, t.s, tbase,
-                              release, bar);
-      else
-        release();   // the second half lies beyond the last column
+      if constexpr (EPI == kEpiLse) {
+        // both warpgroups read the first half, then the second
+        epilogue_lse_wide(a, &tmO, sEg, ebuf, row, leader, m0, t.n * 2 * kBN, grp,
+                          tmem_base + (static_cast<uint32_t>(wq * 32) << 16),
+                          [&] { release_half(tempty0_bar); }, [&] { release_half(tempty1_bar); }, bar);
+      } else {
+        // each warpgroup reads its own half and hands back both at once
+        auto release = [&] {
+          release_half(tempty0_bar);
+          release_half(tempty1_bar);
+        };
+        if (n0 < a.cols)
+          epilogue_tile<EPI, kEpiBufsWide>(a, &tmO, sEg, ebuf, row, leader, m0, n0, t.s, tbase,
+                                           release, bar);
+        else
+          release();   // the second half lies beyond the last column
+      }
     }
     if (leader) bulk_wait_group<0>();
   }
