@@ -844,8 +844,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // for twice the work: 48 KB written and 48 KB read per 16.8 MFLOP. The 512
 // accumulator columns fill TMEM, so the accumulator is single-buffered: the
 // next tile's MMAs wait until the epilogue has read it out (the fp32
-// epilogue's last stores run after that). The shape pays most where K per
-// tile is long.
+// epilogue's last stores run after that). Its two 256-column halves are
+// handed back on separate barriers: the log-sum-exp epilogue frees the first
+// half before reading the second, and meanwhile the MMA issuer runs the next
+// tile's first-half MMAs on the k-blocks already staged. The shape pays most
+// where K per tile is long.
 template <int AMN, int BMN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
     umma_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
