@@ -191,7 +191,7 @@ enum {
                                     empty batch; otherwise the loss reduction writes them) */
     FLCE_K_COMBINE_DLOGITS = 13, /* LSE_COMBINE and DLOGITS in one launch, one block per
                                     token row (in-place mode, chunk rows of at most
-                                    32768 columns)                                    */
+                                    262144 columns)                                   */
     FLCE_K_NUM_KINDS = 14
 };
 

@@ -280,11 +280,13 @@ __global__ void __launch_bounds__(kDlogitsThreads) dlogits_bf16_kernel(
 }
 
 // The log-sum-exp combine and the dlogits pass of one token row in one block,
-// for chunk buffers of at most kFusedSteps x kDlogitsCols columns: the row's
-// log-sum-exp and token loss from its partials, then the row's columns
-// kDlogitsCols at a time. Where rows are this short, one launch per chunk
-// does the work of two.
-constexpr int kFusedSteps = 4;
+// for chunk buffers of at most kFusedSteps x kDlogitsCols columns (262144):
+// the row's log-sum-exp and token loss from its partials, then the row's
+// columns kDlogitsCols at a time. One launch per chunk does the work of two,
+// at the dlogits pass's bandwidth (one block per row leaves thousands of
+// blocks, each keeping its loads in flight); beyond that width the two
+// launches remain.
+constexpr int kFusedSteps = 32;
 
 __global__ void __launch_bounds__(kDlogitsThreads) combine_dlogits_bf16_kernel(
     __nv_bfloat16* __restrict__ buf, int64_t ldv, int64_t V, const float2* __restrict__ partials,
