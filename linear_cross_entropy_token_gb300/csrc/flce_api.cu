@@ -1184,8 +1184,9 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       FLCE_LAUNCH(FLCE_K_GEMM_LOGITS, 2 * dr * dH * dV,
                   2 * dr * dH + 2 * dV * dH + ((recompute || slabs) ? 0 : 2 * dr * dV) + 8 * dr * vt + 12 * dr,
                   launch_gemm(h, shape_for(h, p.tile_n), kUmmaLogits, mX_k, mW_k, mZ_out, a, rows, s));
-      // 2a. cross-tile log-sum-exp and token losses (for short rows in one
-      // launch with the dlogits pass, 2b)
+      // 2a. cross-tile log-sum-exp and token losses (in in-place mode, for rows
+      // of at most combine_dlogits_max_cols() columns, in one launch with the
+      // dlogits pass, 2b)
       const bool fused_rows = !recompute && !slabs && ldv <= combine_dlogits_max_cols();
       if (!fused_rows)
         FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,

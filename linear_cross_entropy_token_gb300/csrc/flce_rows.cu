@@ -1,6 +1,7 @@
 // Row-wise kernels of fused linear cross-entropy: the n_valid count and
 // target range check, the cross-tile log-sum-exp combine, the in-place
-// dlogits pass, the dx split reduction and the loss reduction.
+// dlogits pass (the two also as one launch), the dx split reduction and the
+// loss reduction (also run by the call's last dx reduction).
 //
 // The formulas are those of the Unsloth page ("Unsloth 심층 아키텍처 …",
 // section "스트리밍 청크 기반 Fast CrossEntropy 손실 커널"): per token
