@@ -436,3 +436,24 @@ def test_caller_workspace(bf16):
         assert e.value.status_name == "FLCE_ERR_BUDGET"
     finally:
         h.close()
+
+
+@pytest.mark.parametrize("V,fused", [(262083, True), (262211, False)])
+def test_combine_and_dlogits_launches_by_row_width(V, fused):
+    """In-place mode runs the log-sum-exp combine and the dlogits pass as one
+    launch, a block per token row, for chunk rows of at most 262144 columns
+    (the buffer's row is V rounded up to 64), and as two launches beyond
+    that; both forms match the oracle."""
+    from linear_cross_entropy_token_gb300 import FLCE
+    w = workloads.generate(workloads.custom(200, 64, V, "bf16", ignore_frac=0.1, seed=31))
+    h = FLCE("bf16", 0)
+    try:
+        h.set_profiling(True)
+        h.profile_reset()
+        res = run(h, w)
+        prof = h.profile()
+    finally:
+        h.close()
+    assert ("combine_dlogits" in prof) == fused
+    assert ("lse_combine" in prof) == (not fused) and ("dlogits_inplace" in prof) == (not fused)
+    assert_parity(res, _oracle(w), "bf16", token_rtol=1e-3)
