@@ -166,16 +166,33 @@ class ClockSampler:
             if len(parts) >= 9:
                 rows.append(parts)
         os.unlink(self.path)
+        after = False
+        if not rows:
+            # a timed region shorter than nvidia-smi's start-up and sampling
+            # interval: one sample taken right after it, marked as such
+            try:
+                out = subprocess.run(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits"],
+                                     capture_output=True, text=True, timeout=10).stdout
+                rows = [[p.strip() for p in line.split(",")] for line in out.splitlines()
+                        if len(line.split(",")) >= 9]
+                after = bool(rows)
+            except (OSError, subprocess.SubprocessError):
+                rows = []
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
-                "samples": len(rows),
-                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+        res = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+               "samples": 0 if after else len(rows),
+               "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                                  default=None)}
+        if after:
+            res["note"] = "timed region shorter than the sampling interval: one sample right after it"
+        return res
 
 
 # ------------------------------------------------------------------- peaks
