@@ -199,6 +199,34 @@ def test_plan_invariants_over_extreme_shapes():
         assert p["dlogits"] == mode
 
 
+def test_backward_launch_invariants_over_shapes():
+    """The backward fields of every plan agree with one another: a plan that
+    runs the dx and dW GEMMs in one launch runs them on one tile shape and
+    puts nothing on the second stream; only CTA-pair bf16 plans in the
+    in-place and recompute modes take either form; the dx split stays within
+    1..8; and the default takes one launch exactly where dW runs wide."""
+    import itertools
+    for N, H, V, cta, backward, mode in itertools.product(
+            [1, 300, 2048, 16384], [8, 256, 1024, 4096], [300, 4099, 32000, 151936],
+            ["auto", "single", "pair", "wide"], ["auto", "separate", "one_launch"],
+            ["inplace", "recompute", "slabs"]):
+        p = flce.plan(N, H, V, cta=cta, backward=backward, dlogits_mode=mode,
+                      hbm_budget_bytes=4 * GiB)
+        one, beside = p["backward_one_launch"], p["dw_beside_dx"]
+        assert one in (0, 1) and beside in (0, 1) and not (one and beside)
+        assert 1 <= p["dx_splits"] <= 8
+        if one:
+            assert p["tile_n_dx"] == p["tile_n_dw"]
+        if cta == "single" or mode == "slabs" or backward == "separate":
+            assert one == 0, (N, H, V, cta, backward, mode)
+        if cta == "single" or mode == "slabs":
+            assert beside == 0
+        if backward == "one_launch" and cta != "single" and mode != "slabs":
+            assert one == 1
+        if backward == "auto" and cta in ("auto", "wide") and mode != "slabs":
+            assert one == (1 if p["tile_n_dw"] == 512 else 0), (N, H, V, cta, mode, p)
+
+
 def test_plan_reports_the_mode_it_runs():
     """AUTO resolves to INPLACE; an fp32 handle runs RECOMPUTE in place."""
     assert flce.plan(4096, 1024, 32000)["dlogits"] == "inplace"
