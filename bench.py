@@ -492,6 +492,22 @@ def run_ours(args, ws, rank, local):
         pipe_ms = timed(pipelined_steps)
         ems, evalue = aggregate(ws, tokens, pipe_ms, dev if ws > 1 else None)
         sync_max, _ = aggregate(ws, tokens, sync_ms, dev if ws > 1 else None)
+
+        # the copies alone, from CUDA events on the stream that runs them, in
+        # a further run of each form with the library's profiling on
+        def copy_time(fn):
+            h.set_profiling(True)
+            h.profile_reset()
+            fn()
+            torch.cuda.synchronize(dev)
+            c = h.profile().get("h2d_copy")
+            h.set_profiling(False)
+            h.profile_reset()
+            if not c or not c["launches"]:
+                return None, None
+            return c["total_ms"] / c["launches"], c["bytes"] / c["total_ms"] / 1e6
+        copy_pipe_ms, copy_pipe_gbs = copy_time(pipelined_steps)
+        copy_sync_ms, copy_sync_gbs = copy_time(sync_steps)
         e2e = {"value": evalue, "unit": UNIT,
                "h2d_bytes_per_step": int((x_h.numel() + W_h.numel()) * esize + t_h.numel() * 8),
                "d2h_bytes_per_step": 4 * 16, "ms_per_step": ems,
@@ -499,7 +515,12 @@ def run_ours(args, ws, rank, local):
                        "the library's copy stream (overlapping the previous step's compute); "
                        "the step's control words, with its loss, read back",
                "sync_ms_per_step": sync_max,
-               "sync_path": "flce_forward_backward_host: copy in, compute, read back, one after another"}
+               "sync_path": "flce_forward_backward_host: copy in, compute, read back, one after another",
+               "copy_ms_per_step": {"beside_compute": copy_pipe_ms, "alone": copy_sync_ms},
+               "copy_gbs": {"beside_compute": copy_pipe_gbs, "alone": copy_sync_gbs},
+               "copy_timing": "CUDA events around each step's host-to-device copies on the stream "
+                              "that runs them (the copy stream when pipelined), in a further run of "
+                              "each form with per-launch profiling on"}
 
     # --------------------------------------------------- cpu oracle sample
     cpu = None

@@ -192,7 +192,11 @@ enum {
     FLCE_K_COMBINE_DLOGITS = 13, /* LSE_COMBINE and DLOGITS in one launch, one block per
                                     token row (in-place mode, chunk rows of at most
                                     262144 columns)                                   */
-    FLCE_K_NUM_KINDS = 14
+    FLCE_K_H2D_COPY = 14,        /* not a kernel: the host-buffer entry points' copies of
+                                    x, W and t into device memory, timed on the stream
+                                    that runs them (the copy stream for flce_submit_host);
+                                    `bytes` counts the bytes copied                   */
+    FLCE_K_NUM_KINDS = 15
 };
 
 typedef struct flce_kernel_profile {

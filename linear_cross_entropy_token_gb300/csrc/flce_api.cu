@@ -836,9 +836,12 @@ flce_status stage_inputs(flce_handle_t h, void** buf, uint64_t* buf_bytes, const
   }
   uint8_t* st = static_cast<uint8_t*>(*buf);
   cudaError_t e = cudaSuccess;
+  // timed on `s` when profiling is on (a copy, not a launch)
+  prof_begin(h, FLCE_K_H2D_COPY, s);
   if (xb) e = cudaMemcpyAsync(st + ox, x_host, xb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(st + ow, W_host, wb, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && tb) e = cudaMemcpyAsync(st + ot, t_host, tb, cudaMemcpyHostToDevice, s);
+  prof_end(h, s, 0.0, static_cast<double>(xb + wb + tb));
   if (e != cudaSuccess) return fail(h, FLCE_ERR_CUDA, "staging copy: %s", cudaGetErrorString(e));
   out->x = st + ox;
   out->W = st + ow;
@@ -1379,6 +1382,7 @@ const char* flce_kernel_name(int32_t kind) {
     case FLCE_K_GEMM_DX_DW: return "gemm_dx_dw";
     case FLCE_K_DEVICE_RESULT: return "device_result";
     case FLCE_K_COMBINE_DLOGITS: return "combine_dlogits";
+    case FLCE_K_H2D_COPY: return "h2d_copy";
     default: return "?";
   }
 }

@@ -27,7 +27,7 @@ BACKWARD = {"auto": 0, "separate": 1, "one_launch": 2}
 KERNEL_KINDS = ["count_valid", "gemm_logits_lse", "lse_combine", "dlogits_inplace",
                 "gemm_dlogits_recompute", "gemm_dx", "dx_split_reduce", "gemm_dw",
                 "loss_finalize", "simt_gemm_f32", "simt_tile_stats_f32", "gemm_dx_dw",
-                "device_result", "combine_dlogits"]
+                "device_result", "combine_dlogits", "h2d_copy"]
 
 
 class FlceError(RuntimeError):

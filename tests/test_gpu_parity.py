@@ -233,6 +233,18 @@ def test_host_buffer_entry_point(bf16):
     loss, dx, dW = bf16.forward_backward_host(xh, Wh, th, chunk=256)
     res = {"loss": loss, "dx": to_np64(dx), "dW": to_np64(dW)}
     assert_parity(res, _oracle(w), "bf16")
+    # with profiling on, the copies are timed and counted, and launch no kernel
+    bf16.set_profiling(True)
+    bf16.profile_reset()
+    launches = bf16.launch_count()
+    bf16.forward_backward_host(xh, Wh, th, chunk=256)
+    prof = bf16.profile()
+    bf16.set_profiling(False)
+    bf16.profile_reset()
+    copy = prof["h2d_copy"]
+    assert copy["launches"] == 1 and copy["total_ms"] > 0
+    assert copy["bytes"] == (600 * 128 + 3000 * 128) * 2 + 600 * 8
+    assert bf16.launch_count() - launches == sum(v["launches"] for k, v in prof.items() if k != "h2d_copy")
 
 
 def test_workspace_bytes_matches_the_call(bf16):
