@@ -221,7 +221,9 @@ const char* flce_status_string(flce_status s);
  * chunk-size rule the FLCE page quotes from Liger (section "실전에서
  * 마주치는 트레이드오프", item 1), which sizes chunk logits to about N·H
  * elements: on GB300 the dW GEMM's intensity grows with C, so the budget, not
- * N·H, sets C. num_sms picks the dx split; 0 means 152.
+ * N·H, sets C. num_sms (0 means 152) sets the SM pairs the planner's time
+ * model fills: it picks each GEMM's tile shape, the dx split and whether the
+ * dx and dW GEMMs share one launch (flce_plan.backward_one_launch).
  * Errors: INVALID_ARG for a NULL or negative argument, BUDGET if even one
  * 128-token chunk (or N, if smaller) does not fit the budget. */
 flce_status flce_make_plan(const flce_config* cfg, int64_t N, int64_t H, int64_t V,
