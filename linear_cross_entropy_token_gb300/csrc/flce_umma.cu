@@ -849,6 +849,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // half before reading the second, and meanwhile the MMA issuer runs the next
 // tile's first-half MMAs on the k-blocks already staged. The shape pays most
 // where K per tile is long.
+// The TMA loads of one wide-tile work unit, k-blocks kb0 .. kb1: this CTA's
+// 128 rows of A (from row mA) and its 256 columns of B (two 128-column halves,
+// one per MMA, from column nB0 and nB0 + 256), into the ring after the
+// n_issued stages already filled. Both CTAs' loads complete on the even CTA's
+// full barrier (full0: stage 0's; empty0: this CTA's stage-0 empty barrier).
+// Returns false once a wait for a free stage has run out.
+template <int AMN, int BMN>
+__device__ __forceinline__ bool load_wide_unit(const CUtensorMap* tmA, const CUtensorMap* tmB, int kb0, int kb1,
+                                               int mA, int nB0, uint32_t rank, const uint8_t* sA,
+                                               const uint8_t* sB, uint32_t full0, uint32_t empty0,
+                                               uint32_t& n_issued, uint32_t* ctrl, uint64_t timeout_ns) {
+  const int nB1 = nB0 + kBN;
+  for (int kb = kb0; kb < kb1; ++kb) {
+    const uint32_t stage = n_issued % kStagesWide;
+    const uint32_t phase = (n_issued / kStagesWide) & 1u;
+    if (!mbar_wait_bounded_cluster(empty0 + 8u * stage, phase ^ 1u, ctrl, timeout_ns)) return false;
+    const uint32_t full = full0 + 8u * stage;
+    if (rank == 0) mbar_arrive_expect_tx(full, 2 * kStageBytesWide);
+    const uint32_t fb = mapa_shared(full, 0);
+    const uint32_t sa = smem_u32(sA + stage * kABytes);
+    const uint32_t sb = smem_u32(sB + stage * kBBytes);
+    const int k0 = kb * kBK;
+    if (AMN == 0) {
+      tma_load_2d_pair(sa, tmA, fb, k0, mA);
+    } else {
+      tma_load_2d_pair(sa, tmA, fb, mA, k0);
+      tma_load_2d_pair(sa + 8192, tmA, fb, mA + 64, k0);
+    }
+    if (BMN == 0) {
+      tma_load_2d_pair(sb, tmB, fb, k0, nB0);
+      tma_load_2d_pair(sb + kBHalfBytes, tmB, fb, k0, nB1);
+    } else {
+      tma_load_2d_pair(sb, tmB, fb, nB0, k0);
+      tma_load_2d_pair(sb + 8192, tmB, fb, nB0 + 64, k0);
+      tma_load_2d_pair(sb + kBHalfBytes, tmB, fb, nB1, k0);
+      tma_load_2d_pair(sb + kBHalfBytes + 8192, tmB, fb, nB1 + 64, k0);
+    }
+    ++n_issued;
+  }
+  return true;
+}
+
 template <int AMN, int BMN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
     umma_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -916,36 +958,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
           const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
           const int mA = t.m * 2 * kBM + static_cast<int>(rank) * kBM;      // this CTA's rows of A
           const int nB0 = t.n * 2 * kBN + static_cast<int>(rank) * (kBN / 2);  // its columns, MMA 0
-          const int nB1 = nB0 + kBN;                                          // and MMA 1
-          for (int kb = kb0; kb < kb1; ++kb) {
-            const int stage = n_issued % kStagesWide;
-            const uint32_t phase = (n_issued / kStagesWide) & 1u;
-            if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, a.ctrl, a.timeout_ns)) {
-              failed = true;
-              break;
-            }
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytesWide);
-            const uint32_t fb = mapa_shared(full_bar(stage), 0);
-            const uint32_t sa = smem_u32(sA + stage * kABytes);
-            const uint32_t sb = smem_u32(sB + stage * kBBytes);
-            const int k0 = kb * kBK;
-            if (AMN == 0) {
-              tma_load_2d_pair(sa, &tmA, fb, k0, mA);
-            } else {
-              tma_load_2d_pair(sa, &tmA, fb, mA, k0);
-              tma_load_2d_pair(sa + 8192, &tmA, fb, mA + 64, k0);
-            }
-            if (BMN == 0) {
-              tma_load_2d_pair(sb, &tmB, fb, k0, nB0);
-              tma_load_2d_pair(sb + kBHalfBytes, &tmB, fb, k0, nB1);
-            } else {
-              tma_load_2d_pair(sb, &tmB, fb, nB0, k0);
-              tma_load_2d_pair(sb + 8192, &tmB, fb, nB0 + 64, k0);
-              tma_load_2d_pair(sb + kBHalfBytes, &tmB, fb, nB1, k0);
-              tma_load_2d_pair(sb + kBHalfBytes + 8192, &tmB, fb, nB1 + 64, k0);
-            }
-            ++n_issued;
-          }
+          if (!load_wide_unit<AMN, BMN>(&tmA, &tmB, kb0, kb1, mA, nB0, rank, sA, sB, full_bar(0), empty_bar(0),
+                                        n_issued, a.ctrl, a.timeout_ns))
+            failed = true;
         }
         if (failed && rank == 0) {
           const uint32_t first = n_issued > kStagesWide ? n_issued - kStagesWide : 0;
@@ -1528,30 +1543,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsWide, 1)
           const int kb1 = min(a.kb_total, kb0 + a.kb_per_split);
           const int mA = t.m * 2 * kBM + static_cast<int>(rank) * kBM;      // this CTA's rows of A
           const int nB0 = t.n * 2 * kBN + static_cast<int>(rank) * (kBN / 2);  // its columns, MMA 0
-          const int nB1 = nB0 + kBN;                                          // and MMA 1
-          for (int kb = kb0; kb < kb1; ++kb) {
-            const int stage = n_issued % kStagesWide;
-            const uint32_t phase = (n_issued / kStagesWide) & 1u;
-            if (!mbar_wait_bounded_cluster(empty_bar(stage), phase ^ 1u, ctrl, timeout_ns)) {
-              failed = true;
-              break;
-            }
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytesWide);
-            const uint32_t fb = mapa_shared(full_bar(stage), 0);
-            const uint32_t sa = smem_u32(sA + stage * kABytes);
-            const uint32_t sb = smem_u32(sB + stage * kBBytes);
-            const int k0 = kb * kBK;
-            if (q == 0)
-              load_a_pair<0>(sa, &maps.a[0], fb, k0, mA);
-            else
-              load_a_pair<1>(sa, &maps.a[1], fb, k0, mA);
-            // B is MN-major in both problems
-            tma_load_2d_pair(sb, &maps.b[q], fb, nB0, k0);
-            tma_load_2d_pair(sb + 8192, &maps.b[q], fb, nB0 + 64, k0);
-            tma_load_2d_pair(sb + kBHalfBytes, &maps.b[q], fb, nB1, k0);
-            tma_load_2d_pair(sb + kBHalfBytes + 8192, &maps.b[q], fb, nB1 + 64, k0);
-            ++n_issued;
-          }
+          // A is K-major for dx and MN-major for dW; B is MN-major in both
+          const bool ok = q ? load_wide_unit<1, 1>(&maps.a[1], &maps.b[1], kb0, kb1, mA, nB0, rank, sA, sB,
+                                                   full_bar(0), empty_bar(0), n_issued, ctrl, timeout_ns)
+                            : load_wide_unit<0, 1>(&maps.a[0], &maps.b[0], kb0, kb1, mA, nB0, rank, sA, sB,
+                                                   full_bar(0), empty_bar(0), n_issued, ctrl, timeout_ns);
+          if (!ok) failed = true;
         }
         if (failed && rank == 0) {
           const uint32_t first = n_issued > kStagesWide ? n_issued - kStagesWide : 0;
