@@ -263,6 +263,9 @@ def test_plan_picks_tile_shapes_per_gemm():
     # separate launches put the small shape's 64-unit dx launch beside dW,
     # not the Llama-3 shape's 512-unit one; single-CTA tiles do neither
     assert (p["backward_one_launch"], p["dw_beside_dx"]) == (1, 0)
+    # one launch of 48 dx units (16 tiles x 3 splits) and 250 dW units: three
+    # splits keep the longest dx unit under the launch's work per SM pair
+    assert p["dx_splits"] == 3
     assert (q["backward_one_launch"], r["backward_one_launch"], n["backward_one_launch"]) == (1, 0, 0)
     sep = flce.plan(2048, 1024, 32000, backward="separate")
     assert (sep["backward_one_launch"], sep["dw_beside_dx"]) == (0, 1)
