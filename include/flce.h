@@ -190,8 +190,8 @@ enum {
     FLCE_K_DEVICE_RESULT = 12,   /* loss and n_valid into caller device memory (an
                                     empty batch; otherwise the loss reduction writes them) */
     FLCE_K_COMBINE_DLOGITS = 13, /* LSE_COMBINE and DLOGITS in one launch, one block per
-                                    token row (in-place mode, chunk rows of at most
-                                    262144 columns)                                   */
+                                    token row (in-place mode: bf16 chunk rows of at most
+                                    262144 columns; fp32, with the statistics too)    */
     FLCE_K_H2D_COPY = 14,        /* not a kernel: the host-buffer entry points' copies of
                                     x, W and t into device memory, timed on the stream
                                     that runs them (the copy stream for flce_submit_host);

@@ -1112,13 +1112,9 @@ flce_status enqueue_fb(flce_handle_t h, const void* x, const void* W, const int6
       }
       FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dH * dV, 4 * (dr * dH + dV * dH + dr * dV),
                   launch_simt_gemm_f32(xf + off * H, H, 1, Wf, 1, H, logits, ldv, rows, V, H, 0, 1, nullptr, s));
-      FLCE_LAUNCH(FLCE_K_SIMT_TILE_STATS, 0.0, 4 * dr * dV + 12 * dr * vt,
-                  launch_simt_tile_stats(logits, ldv, rows, V, vt, vt, 0, t + off, ignore_index, partials,
-                                         zt, s));
-      FLCE_LAUNCH(FLCE_K_LSE_COMBINE, 0.0, 8 * dr * vt + 24 * dr,
-                  launch_lse_combine(partials, vt, zt, t + off, rows, ignore_index, lse, token_loss + off, s));
-      FLCE_LAUNCH(FLCE_K_DLOGITS, 0.0, 8 * dr * dV,
-                  launch_dlogits_f32(logits, ldv, rows, V, 0, lse, t + off, ignore_index, ctrl, s));
+      // the row steps in one launch: log-sum-exp, token loss, dlogits in place
+      FLCE_LAUNCH(FLCE_K_COMBINE_DLOGITS, 0.0, 12 * dr * dV + 24 * dr,
+                  launch_rows_f32(logits, ldv, rows, V, t + off, ignore_index, ctrl, lse, token_loss + off, s));
       FLCE_LAUNCH(FLCE_K_SIMT_GEMM, 2 * dr * dV * dH, 4 * (dr * dV + dV * dH + dr * dH),
                   launch_simt_gemm_f32(logits, ldv, 1, Wf, H, 1, dxf + off * H, H, rows, H, V, 0, dx_splits,
                                        dxpart, s));

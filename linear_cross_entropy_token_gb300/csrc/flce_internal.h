@@ -144,6 +144,12 @@ cudaError_t launch_combine_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int row
                                         const uint32_t* ctrl, float* lse, float* token_loss_chunk,
                                         float* dcorr, cudaStream_t s);
 int64_t combine_dlogits_max_cols();
+// fp32 path, in place: per token row of the chunk's fp32 logits, the
+// log-sum-exp, token loss and (softmax - onehot)/n_valid in one launch (a
+// block per row); replaces the tile statistics, combine and dlogits passes
+cudaError_t launch_rows_f32(float* buf, int64_t ldv, int rows, int64_t V, const int64_t* t_chunk,
+                            int64_t ignore_index, const uint32_t* ctrl, float* lse,
+                            float* token_loss_chunk, cudaStream_t s);
 cudaError_t launch_device_result(uint32_t* ctrl, float* loss_dev, int32_t* n_valid_dev, cudaStream_t s);
 // result != 0: also write the sync-free entry points' device result (loss,
 // NaN after a recorded error; n_valid; the sticky error word)

@@ -383,6 +383,86 @@ __device__ __forceinline__ void loss_reduce(const float* __restrict__ token_loss
 
 constexpr int kReduceThreads = 128;
 
+// The fp32 path's row steps of one chunk in one block per token row: the
+// row's log-sum-exp over its V fp32 logits (a running max and rescaled sum
+// per thread, with expf, merged across the block in a fixed order), its
+// token loss, then the row overwritten in place with (softmax - onehot) /
+// n_valid (zeros for an ignored row, and for the row's padding columns past
+// V). It replaces the per-tile statistics, the combine and the dlogits pass
+// of that path: one launch instead of three, the row read twice.
+constexpr int kRowsF32Threads = 1024;
+
+__device__ __forceinline__ void online_add(float& m, float& s, float z) {
+  if (z > m) {
+    s = (m == -INFINITY ? 0.f : s * expf(m - z)) + 1.f;
+    m = z;
+  } else {
+    s += expf(z - m);
+  }
+}
+
+__device__ __forceinline__ void online_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+  } else if (m2 > m) {
+    s = s * expf(m - m2) + s2;
+    m = m2;
+  } else {
+    s += s2 * expf(m2 - m);
+  }
+}
+
+__global__ void __launch_bounds__(kRowsF32Threads) rows_f32_kernel(
+    float* __restrict__ buf, int64_t ldv, int64_t V, const int64_t* __restrict__ t, int64_t ignore_index,
+    const uint32_t* __restrict__ ctrl, float* __restrict__ lse, float* __restrict__ token_loss) {
+  __shared__ float2 warp_ms[kRowsF32Threads / 32];
+  __shared__ float s_l, s_zt;
+  const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* row = buf + static_cast<size_t>(r) * ldv;
+  const int64_t tg = t[r];
+  float m = -INFINITY, sum = 0.f;
+  for (int64_t j = threadIdx.x; j < V; j += kRowsF32Threads) {
+    const float z = row[j];
+    online_add(m, sum, z);
+    if (j == tg) s_zt = z;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+    online_merge(m, sum, m2, s2);
+  }
+  if (lane == 0) warp_ms[warp] = make_float2(m, sum);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    m = warp_ms[0].x;
+    sum = warp_ms[0].y;
+#pragma unroll
+    for (int w = 1; w < kRowsF32Threads / 32; ++w) online_merge(m, sum, warp_ms[w].x, warp_ms[w].y);
+    const float l = m + logf(sum);
+    lse[r] = l;
+    token_loss[r] = (tg == ignore_index) ? 0.f : (l - s_zt);
+    s_l = l;
+  }
+  __syncthreads();
+  const float l = s_l;
+  const uint32_t nv = ctrl[kCtrlNValid];
+  const bool live = tg != ignore_index && nv > 0;
+  const float scale = live ? 1.0f / static_cast<float>(nv) : 0.f;
+  for (int64_t j = threadIdx.x; j < ldv; j += kRowsF32Threads) {
+    float d = 0.f;
+    if (live && j < V) {
+      d = expf(row[j] - l);
+      if (j == tg) d -= 1.f;
+      d *= scale;
+    }
+    row[j] = d;
+  }
+}
+
 // dx row i = sum over splits of the fp32 partials of dlogits·W (in split
 // order) + dcorr[i]·W[t_i], rounded once to bf16. dcorr[i] is the fp32
 // rounding error of the bf16 dlogits entry at the target column, so the sum
@@ -528,6 +608,15 @@ cudaError_t launch_combine_dlogits_bf16(__nv_bfloat16* buf, int64_t ldv, int row
   combine_dlogits_bf16_kernel<<<rows, kDlogitsThreads, 0, s>>>(buf, ldv, V, partials, vocab_tiles, zt,
                                                                t_chunk, ignore_index, ctrl, lse,
                                                                token_loss_chunk, dcorr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows_f32(float* buf, int64_t ldv, int rows, int64_t V, const int64_t* t_chunk,
+                            int64_t ignore_index, const uint32_t* ctrl, float* lse,
+                            float* token_loss_chunk, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  rows_f32_kernel<<<rows, kRowsF32Threads, 0, s>>>(buf, ldv, V, t_chunk, ignore_index, ctrl, lse,
+                                                  token_loss_chunk);
   return cudaGetLastError();
 }
 
